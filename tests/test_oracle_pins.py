@@ -1,0 +1,456 @@
+"""Pins of the CPU oracle to things other than itself (no GPU).
+
+Each test checks the oracle against a closed form, a library routine, an
+invariant the method fixes, a special case that reduces to a simpler
+decoder, or a pure-Python brute force on tiny inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from block_denoising_gb300 import inputs
+from oracle import dinfer_oracle as O
+from tests import bruteforce as BF
+
+
+def tiny_desc(**kw):
+    base = dict(n_layers=2, d_model=8, n_heads=2, head_dim=4, ffn=12, vocab=16,
+                mask_id=15, rms_eps=1e-5, rope_theta=10000.0, logit_scale=40.0, dtype="fp32")
+    base.update(kw)
+    return O.Desc(**base)
+
+
+def tiny_model(desc, seed=0, std=0.3, gains_random=True):
+    cfg = inputs.ModelConfig(n_layers=desc.n_layers, d_model=desc.d_model, n_heads=desc.n_heads,
+                             head_dim=desc.head_dim, ffn=desc.ffn, vocab=desc.vocab,
+                             mask_id=desc.mask_id, n_experts=desc.n_experts, top_k=desc.top_k,
+                             expert_ffn=desc.expert_ffn, dtype="fp32", weight_std=std)
+    ws = [w.numpy().astype(np.float64) for w in inputs.make_weights(cfg, seed)]
+    if gains_random:  # non-unit gains so that a dropped gain is visible
+        for i, (name, shape, init) in enumerate(inputs.weight_specs(cfg)):
+            if init == "ones":
+                ws[i] = 0.5 + inputs.uniform_tensor(1000 + i, shape, 0.0, 1.0, seed).numpy()
+    if desc.dtype == "bf16":
+        ws = [O.round_bf16(w) for w in ws]
+    return O.Model(desc, ws), ws
+
+
+# ---------------------------------------------------------------------------
+# elementwise pieces
+# ---------------------------------------------------------------------------
+def test_round_bf16_matches_torch():
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(200000, generator=g, dtype=torch.float64) * torch.exp(torch.randn(200000, generator=g, dtype=torch.float64) * 4)
+    # exact halfway cases in float32
+    base = torch.randn(1000, generator=g).to(torch.bfloat16).float()
+    half = base + base.abs() * (2.0 ** -9)
+    x = torch.cat([x, half.double()])
+    ref = x.to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_bf16(x.numpy()), ref)
+
+
+def test_rmsnorm_unit_rms_and_gain():
+    h = np.random.default_rng(0).normal(size=(5, 64)) * 3.0
+    y = O.rmsnorm(h, np.ones(64), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, -1)), 1.0, rtol=1e-12)
+    g = np.linspace(0.5, 2.0, 64)
+    np.testing.assert_allclose(O.rmsnorm(h, g, 0.0), y * g, rtol=1e-12)
+    # eps enters under the square root
+    z = np.full((1, 4), 1e-3)
+    np.testing.assert_allclose(O.rmsnorm(z, np.ones(4), 1e-5), 1e-3 / math.sqrt(1e-6 + 1e-5), rtol=1e-12)
+
+
+def test_silu_closed_form():
+    x = np.linspace(-20, 20, 1001)
+    np.testing.assert_allclose(O.silu(x), x * scipy.special.expit(x), rtol=1e-13, atol=1e-300)
+
+
+def test_rope_relative_position_and_identity():
+    rng = np.random.default_rng(1)
+    q = rng.normal(size=(1, 3, 8))
+    k = rng.normal(size=(1, 3, 8))
+    np.testing.assert_allclose(O.rope(q, [0], 10000.0), q, rtol=0, atol=0)
+    for (p, r, c) in [(3, 7, 11), (100, 2, 513), (0, 1535, 17)]:
+        a = np.sum(O.rope(q, [p], 1e4) * O.rope(k, [r], 1e4), -1)
+        b = np.sum(O.rope(q, [p + c], 1e4) * O.rope(k, [r + c], 1e4), -1)
+        np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-9)
+    # a rotation keeps the norm of each pair
+    y = O.rope(q, [37], 1e4)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(q, axis=-1), rtol=1e-12)
+    # pair (i, i+hd/2) rotated by p * theta^(-2i/hd): check one pair by hand
+    e = np.zeros((1, 1, 8)); e[0, 0, 1] = 1.0
+    ang = 5 * 10000.0 ** (-2.0 * 1 / 8)
+    y = O.rope(e, [5], 1e4)
+    np.testing.assert_allclose([y[0, 0, 1], y[0, 0, 5]], [math.cos(ang), math.sin(ang)], rtol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(2)
+    k = rng.normal(size=(9, 2, 4))
+    v = rng.normal(size=(9, 2, 4))
+    # q = 0 -> uniform weights -> mean of the values
+    np.testing.assert_allclose(O.attention(np.zeros((3, 2, 4)), k, v), np.broadcast_to(v.mean(0), (3, 2, 4)), rtol=1e-12)
+    # identical keys -> mean of the values whatever q is
+    kk = np.broadcast_to(k[:1], k.shape)
+    np.testing.assert_allclose(O.attention(rng.normal(size=(3, 2, 4)), kk, v), np.broadcast_to(v.mean(0), (3, 2, 4)), rtol=1e-12)
+    # one dominant key -> its value
+    q = np.zeros((1, 2, 4)); q[0, :, 0] = 1e3
+    k2 = np.zeros((9, 2, 4)); k2[4, :, 0] = 1.0
+    np.testing.assert_allclose(O.attention(q, k2, v)[0], v[4], rtol=1e-12)
+    # weights equal scipy's softmax of q.k/sqrt(hd)
+    q = rng.normal(size=(3, 2, 4))
+    w = scipy.special.softmax(np.einsum("qhd,khd->hqk", q, k) / 2.0, axis=-1)
+    np.testing.assert_allclose(O.attention(q, k, v), np.einsum("hqk,khd->qhd", w, v), rtol=1e-12)
+    # no mask: permuting the keys and values together changes nothing
+    perm = rng.permutation(9)
+    np.testing.assert_allclose(O.attention(q, k[perm], v[perm]), O.attention(q, k, v), rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# decoding
+# ---------------------------------------------------------------------------
+def test_top1_confidence_closed_form():
+    rng = np.random.default_rng(4)
+    lg = rng.normal(size=(7, 50)) * 20
+    lg[:, 13] = -np.inf  # the mask token
+    tok, conf = O.top1_confidence(lg)
+    p = scipy.special.softmax(lg, axis=-1)
+    np.testing.assert_array_equal(tok, np.argmax(p, -1))
+    np.testing.assert_allclose(conf, p.max(-1), rtol=1e-13)
+    assert np.all(conf > 1 / 49) and np.all(conf <= 1)
+    # all equal (except the masked entry) -> 1/(V-1) and the lowest index
+    eq = np.zeros((1, 50)); eq[0, 13] = -np.inf
+    t, c = O.top1_confidence(eq)
+    assert t[0] == 0 and abs(c[0] - 1 / 49) < 1e-15
+    # tie between two maxima -> lowest index
+    tie = np.zeros((1, 6)); tie[0, [2, 4]] = 5.0
+    assert O.top1_confidence(tie)[0][0] == 2
+
+
+def test_lm_head_excludes_mask_token():
+    desc = tiny_desc(n_layers=1)
+    m, ws = tiny_model(desc)
+    h = np.zeros((1, 8)); h[0] = 1.0
+    m.lm_head = m.lm_head.copy()
+    m.lm_head[desc.mask_id] = 100.0  # the mask row would dominate
+    lg = O.lm_head_logits(m, h)
+    assert lg[0, desc.mask_id] == -np.inf
+    assert O.top1_confidence(lg)[0][0] != desc.mask_id
+
+
+@pytest.mark.parametrize("conf,masked,tau,expect", [
+    ([0.95, 0.5, 0.91, 0.2], [1, 1, 1, 1], 0.9, [1, 0, 1, 0]),     # parallel commit
+    ([0.95, 0.5, 0.91, 0.2], [0, 1, 1, 1], 0.9, [0, 0, 1, 0]),     # only masked positions
+    ([0.3, 0.8, 0.7, 0.8], [1, 1, 1, 1], 0.9, [0, 1, 0, 0]),       # fallback, tie -> lowest position
+    ([0.3, 0.8, 0.7, 0.8], [1, 0, 1, 1], 0.9, [0, 0, 0, 1]),       # fallback among masked only
+    ([0.9, 0.9, 0.1, 0.1], [1, 1, 1, 1], 0.9, [1, 0, 0, 0]),       # strict '>': equal is not above
+    ([0.95, 0.99, 0.1, 0.1], [0, 0, 0, 0], 0.9, [0, 0, 0, 0]),     # nothing masked -> nothing
+    ([0.1, 0.2, 0.3, 0.05], [1, 1, 1, 1], 0.0, [1, 1, 1, 1]),      # tau 0 -> whole block
+    ([1.0, 1.0, 0.99, 1.0], [1, 1, 1, 1], 1.0, [1, 0, 0, 0]),      # tau 1 -> one per step
+])
+def test_threshold_commit_cases(conf, masked, tau, expect):
+    got = O.threshold_commit(np.array(conf), np.array(masked, bool), tau)
+    np.testing.assert_array_equal(got.astype(int), expect)
+
+
+# ---------------------------------------------------------------------------
+# forward vs brute force
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_forward_matches_bruteforce(dtype):
+    desc = tiny_desc(dtype=dtype)
+    m, ws = tiny_model(desc, std=0.4)
+    ids = np.array([3, 7, 15, 15, 1, 15])
+    bf = np.array(BF.forward_logits(desc, [w.tolist() for w in ws], list(ids), bf16_mode=(dtype == "bf16")))
+    cache = O.Cache(desc, 1, len(ids))
+    hid = O.forward(m, ids[None], cache, np.arange(len(ids)))
+    lg = O.lm_head_logits(m, hid[0])
+    fin = np.isfinite(bf)
+    assert np.array_equal(fin, np.isfinite(lg))
+    tol = 1e-9 if dtype == "fp32" else 2e-2  # bf16: rare rounding flips from summation order
+    np.testing.assert_allclose(lg[fin], bf[fin], rtol=0, atol=tol)
+    if dtype == "bf16":
+        assert np.mean(np.abs(lg[fin] - bf[fin]) < 1e-9) > 0.9
+
+
+def test_bidirectional_no_causal_mask():
+    desc = tiny_desc()
+    m, _ = tiny_model(desc)
+    a = np.array([[3, 7, 15, 15, 1, 2]])
+    b = a.copy(); b[0, 5] = 9  # change the LAST token
+    ha = O.forward(m, a, O.Cache(desc, 1, 6), np.arange(6))
+    hb = O.forward(m, b, O.Cache(desc, 1, 6), np.arange(6))
+    assert np.max(np.abs(ha[0, 0] - hb[0, 0])) > 1e-6   # the first position sees it
+
+
+# ---------------------------------------------------------------------------
+# MoE special cases
+# ---------------------------------------------------------------------------
+def test_moe_single_expert_equals_dense():
+    rng = np.random.default_rng(5)
+    d, fe = 8, 6
+    a = rng.normal(size=(5, d))
+    w13 = rng.normal(size=(1, 2 * fe, d)) * 0.3
+    w2 = rng.normal(size=(1, d, fe)) * 0.3
+    desc = tiny_desc(n_experts=1, top_k=1, expert_ffn=fe, ffn=0)
+    lw = {"router": rng.normal(size=(1, d)), "w13": w13, "w2": w2}
+    got = O.moe_ffn(a, lw, desc, O.Precision("fp32"))
+    dense = O.dense_ffn(a, {"w_gate": w13[0, :fe], "w_up": w13[0, fe:], "w_down": w2[0]}, O.Precision("fp32"))
+    np.testing.assert_allclose(got, dense, rtol=1e-12)
+
+
+def test_moe_all_experts_is_softmax_mixture():
+    rng = np.random.default_rng(6)
+    d, fe, E = 8, 4, 5
+    a = rng.normal(size=(3, d))
+    lw = {"router": rng.normal(size=(E, d)), "w13": rng.normal(size=(E, 2 * fe, d)) * 0.3,
+          "w2": rng.normal(size=(E, d, fe)) * 0.3}
+    desc = tiny_desc(n_experts=E, top_k=E, expert_ffn=fe, ffn=0)
+    got = O.moe_ffn(a, lw, desc, O.Precision("fp32"))
+    p = scipy.special.softmax(a @ lw["router"].T, axis=-1)
+    g = np.einsum("rd,efd->ref", a, lw["w13"][:, :fe])
+    u = np.einsum("rd,efd->ref", a, lw["w13"][:, fe:])
+    y = np.einsum("ref,edf->red", g * scipy.special.expit(g) * u, lw["w2"])
+    np.testing.assert_allclose(got, np.einsum("re,red->rd", p, y), rtol=1e-12)
+
+
+def test_route_topk_matches_full_sort():
+    rng = np.random.default_rng(7)
+    a = rng.normal(size=(40, 16))
+    r = rng.normal(size=(64, 16)) / 4
+    p, idx = O.route(a, r, 8)
+    for i in range(40):
+        order = sorted(range(64), key=lambda e: (-p[i, e], e))
+        assert list(idx[i]) == order[:8]
+    # ties go to the lower expert index
+    p2, idx2 = O.route(np.zeros((1, 16)), r, 3)
+    assert list(idx2[0]) == [0, 1, 2]
+
+
+# ---------------------------------------------------------------------------
+# dual cache
+# ---------------------------------------------------------------------------
+def _state(desc, P, G, seed=0):
+    rng = np.random.default_rng(seed)
+    x = np.full((1, P + G), desc.mask_id)
+    x[0, :P] = rng.integers(0, desc.mask_id, size=P)
+    mask = np.zeros((1, P + G), bool); mask[0, P:] = True
+    return x, mask
+
+
+def test_cached_step_on_unchanged_state_reproduces_refresh():
+    desc = tiny_desc(n_layers=3, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc)
+    x, mask = _state(desc, 5, 8)
+    cache = O.Cache(desc, 1, 13)
+    r1 = O.refresh_step(m, x, mask, 9, 4, 0.9, cache, commit=False)
+    r2 = O.cached_step(m, x, mask, 9, 4, 0.9, cache, commit=False)
+    np.testing.assert_allclose(r2.logits[np.isfinite(r2.logits)], r1.logits[np.isfinite(r1.logits)], rtol=1e-10, atol=1e-10)
+
+
+def test_in_place_cache_equals_explicit_concatenation():
+    desc = tiny_desc(n_layers=1, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc)
+    x, mask = _state(desc, 5, 8)
+    cache = O.Cache(desc, 1, 13)
+    O.refresh_step(m, x, mask, 9, 4, 0.9, cache, commit=False)
+    x2 = x.copy(); x2[0, 9] = 4  # a commit changes the block
+    # cached step: block rows written in place, attend over [prefix | block | suffix]
+    K0, V0 = cache.K[0][0].copy(), cache.V[0][0].copy()
+    r = O.cached_step(m, x2, mask.copy(), 9, 4, 0.9, cache, commit=False)
+    # explicit: layer-0 block K/V recomputed, then concatenated with the stale-free prefix/suffix
+    d = desc
+    lw = m.layers[0]
+    pos = np.arange(9, 13)
+    a = O.rmsnorm(O.embed(m, x2[0, pos]), lw["attn_norm"], d.rms_eps)
+    kb = O.rope(O.linear(a, lw["wk"]).reshape(4, 2, 4), pos, d.rope_theta)
+    vb = O.linear(a, lw["wv"]).reshape(4, 2, 4)
+    Kc = np.concatenate([K0[:9], kb, K0[13:]])
+    Vc = np.concatenate([V0[:9], vb, V0[13:]])
+    np.testing.assert_allclose(cache.K[0][0], Kc, rtol=1e-13)
+    np.testing.assert_allclose(cache.V[0][0], Vc, rtol=1e-13)
+    assert r.logits.shape == (1, 4, 32)
+
+
+def test_one_layer_dual_cache_equals_no_cache():
+    # with one layer the cached prefix/suffix K/V depend only on the embeddings
+    # and positions, so the dual cache is exact and the trajectories coincide
+    desc = tiny_desc(n_layers=1, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc, std=0.5)
+    prompt = np.array([[1, 5, 9, 2, 7]])
+    for tau in (0.9, 0.5, 0.2):
+        xa, ta = O.generate(m, prompt, 12, 4, tau, cache_mode="dual")
+        xb, tb = O.generate(m, prompt, 12, 4, tau, cache_mode="none")
+        np.testing.assert_array_equal(xa, xb)
+        assert [t.commit.tolist() for t in ta] == [t.commit.tolist() for t in tb]
+
+
+def test_two_layer_dual_cache_is_an_approximation_after_commits():
+    # reported statistic: after a commit inside a block, a 2-layer model's cached
+    # prefix/suffix K/V are stale, so cached logits differ from recomputation
+    desc = tiny_desc(n_layers=2, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc, std=0.5)
+    x, mask = _state(desc, 5, 8)
+    cache = O.Cache(desc, 1, 13)
+    O.refresh_step(m, x, mask, 5, 4, 0.9, cache, commit=False)
+    x[0, 5] = 3; mask[0, 5] = False
+    rc = O.cached_step(m, x, mask.copy(), 5, 4, 0.9, cache, commit=False)
+    rn = O.nocache_step(m, x, mask.copy(), 5, 4, 0.9, commit=False)
+    fin = np.isfinite(rc.logits)
+    assert np.max(np.abs(rc.logits[fin] - rn.logits[fin])) > 1e-9
+
+
+# ---------------------------------------------------------------------------
+# generation: special thresholds and invariants
+# ---------------------------------------------------------------------------
+def test_threshold_one_is_one_token_per_step():
+    desc = tiny_desc(vocab=32, mask_id=31)
+    m, _ = tiny_model(desc)
+    x, tr = O.generate(m, np.array([[1, 2, 3]]), 8, 4, 1.0)
+    assert all(int(t.commit.sum()) == 1 for t in tr)
+    assert O.iterations_per_block(tr) == {0: 4, 1: 4}
+
+
+def test_threshold_zero_is_blockwise_argmax_of_full_forward():
+    desc = tiny_desc(vocab=32, mask_id=31)
+    m, ws = tiny_model(desc)
+    prompt = [1, 2, 3]
+    x, tr = O.generate(m, np.array([prompt]), 8, 4, 0.0)
+    assert O.iterations_per_block(tr) == {0: 1, 1: 1}
+    # brute force: each block is the argmax of one full forward over the current ids
+    ids = prompt + [31] * 8
+    for s in (3, 7):
+        lg = BF.forward_logits(desc, [w.tolist() for w in ws], ids)
+        for i in range(s, s + 4):
+            ids[i] = int(np.argmax(lg[i]))
+    assert x[0].tolist() == ids
+
+
+def check_invariants(x, trace, prompt, P, G, B, mask_id):
+    for t in trace:
+        assert t.commit.sum(axis=-1).min() >= 1 or not t.mask_before[:, P + t.block * B:P + (t.block + 1) * B].all(axis=-1).any()
+        for s in range(x.shape[0]):
+            blk = t.mask_before[s, P + t.block * B:P + (t.block + 1) * B]
+            if blk.any():
+                assert t.commit[s].sum() >= 1                   # >= 1 commit per iteration
+            assert not (t.commit[s] & ~blk).any()               # only masked positions commit
+            assert t.mask_before[s, P + (t.block + 1) * B:].all()  # later blocks still masked
+            assert not t.mask_before[s, :P + t.block * B].any()    # earlier blocks done
+    for blk, n in O.iterations_per_block(trace).items():
+        assert 1 <= n <= B                                       # <= B iterations per block
+    assert (x != mask_id).all()                                  # no mask token in the output
+    np.testing.assert_array_equal(x[:, :P], prompt)              # prompt kept
+    # never re-mask: once a position is committed its id stays fixed
+    final = x
+    for t in trace:
+        done = ~t.mask_before
+        assert (t.x_before[done] == final[done]).all()
+
+
+def test_invariants_tiny_workload():
+    cfg, run, _ = inputs.WORKLOADS["tiny_fp32"]
+    m = O.Model(O.Desc.from_config(cfg), [w.numpy() for w in inputs.make_weights(cfg)])
+    prompt = inputs.make_prompt(cfg, run.batch, run.prompt_len).numpy()
+    x, tr = O.generate(m, prompt, run.gen_length, run.block_length, run.threshold)
+    check_invariants(x, tr, prompt, run.prompt_len, run.gen_length, run.block_length, cfg.mask_id)
+
+
+def test_batch_equals_independent_sequences():
+    desc = tiny_desc(vocab=32, mask_id=31)
+    m, _ = tiny_model(desc)
+    prompts = np.array([[1, 2, 3], [4, 5, 6]])
+    xb, tb = O.generate(m, prompts, 8, 4, 0.6)
+    for s in range(2):
+        xs, _ = O.generate(m, prompts[s:s + 1], 8, 4, 0.6)
+        np.testing.assert_array_equal(xb[s], xs[0])
+    check_invariants(xb, tb, prompts, 3, 8, 4, 31)
+
+
+# ---------------------------------------------------------------------------
+# the input generator (shared by both sides)
+# ---------------------------------------------------------------------------
+def test_generator_statistics_and_determinism():
+    w = inputs.normal_tensor(5, (512, 512), 0.02, 0, dtype=torch.float32)
+    assert abs(w.mean().item()) < 2e-4 and abs(w.std().item() - 0.02) < 3e-4
+    np.testing.assert_array_equal(w.numpy(), inputs.normal_tensor(5, (512, 512), 0.02, 0, dtype=torch.float32).numpy())
+    assert not torch.equal(w, inputs.normal_tensor(6, (512, 512), 0.02, 0, dtype=torch.float32))
+    # tails of a normal: about 0.27% beyond 3 sigma
+    frac = (w.abs() > 0.06).float().mean().item()
+    assert 0.002 < frac < 0.0035
+    cfg = inputs.LLADA_8B
+    p = inputs.make_prompt(cfg, 4, 4096)
+    assert p.min() >= 0 and p.max() < cfg.vocab and not (p == cfg.mask_id).any()
+    assert p.unique().numel() > 3000
+
+
+def test_lowbias32_reference_values():
+    # the integer hash evaluated in int64 torch ops equals plain Python integers
+    xs = [0, 1, 2, 0xDEADBEEF, 0xFFFFFFFF, 123456789]
+    t = inputs._h32(torch.tensor(xs, dtype=torch.int64)).tolist()
+    assert t == [inputs._h32_int(x) for x in xs]
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each plausible slip in the oracle must trip a pin
+# ---------------------------------------------------------------------------
+def _bruteforce_gap(m, ws, desc):
+    ids = np.array([3, 7, 15, 15, 1, 15])
+    bf = np.array(BF.forward_logits(desc, [w.tolist() for w in ws], list(ids)))
+    hid = O.forward(m, ids[None], O.Cache(desc, 1, len(ids)), np.arange(len(ids)))
+    lg = O.lm_head_logits(m, hid[0])
+    fin = np.isfinite(bf) & np.isfinite(lg)
+    if not np.array_equal(np.isfinite(bf), np.isfinite(lg)):
+        return np.inf
+    return float(np.max(np.abs(lg[fin] - bf[fin])))
+
+
+def _rope_wrong_sign(x, pos, theta):
+    y = _ORIG["rope"](x, pos, theta)
+    half = y.shape[-1] // 2
+    return _ORIG["rope"](x, -np.asarray(pos), theta) if half else y
+
+
+def _attn_no_scale(q, k, v):
+    return _ORIG["attention"](q * np.sqrt(q.shape[-1]), k, v)
+
+
+def _rms_no_gain(h, g, eps):
+    return _ORIG["rmsnorm"](h, np.ones_like(np.asarray(g)), eps)
+
+
+def _swiglu_swapped(a, lw, prec):
+    return _ORIG["dense_ffn"](a, {"w_gate": lw["w_up"], "w_up": lw["w_gate"], "w_down": lw["w_down"]}, prec)
+
+
+def _transposed_linear(x, w):
+    w = np.asarray(w, dtype=np.float64)
+    return np.asarray(x, dtype=np.float64) @ (w.T if w.shape[0] != w.shape[1] else w)
+
+
+_ORIG = {k: getattr(O, k) for k in ("rope", "attention", "rmsnorm", "dense_ffn", "linear")}
+
+
+@pytest.mark.parametrize("name,fake", [
+    ("rope", _rope_wrong_sign),
+    ("attention", _attn_no_scale),
+    ("rmsnorm", _rms_no_gain),
+    ("dense_ffn", _swiglu_swapped),
+    ("linear", _transposed_linear),
+])
+def test_planted_mistake_is_caught(monkeypatch, name, fake):
+    desc = tiny_desc()
+    m, ws = tiny_model(desc, std=0.4)
+    assert _bruteforce_gap(m, ws, desc) < 1e-9
+    monkeypatch.setattr(O, name, fake)
+    assert _bruteforce_gap(m, ws, desc) > 1e-6
+
+
+def test_planted_commit_mistakes_are_caught():
+    conf = np.array([0.9, 0.95, 0.2]); masked = np.ones(3, bool)
+    good = O.threshold_commit(conf, masked, 0.9)
+    # '>=' instead of '>' would commit position 0 as well
+    assert good.tolist() == [False, True, False]
+    assert (masked & (conf >= 0.9)).tolist() != good.tolist()
