@@ -1,0 +1,1076 @@
+// Host runtime behind include/dinfer.h: context, workspaces, tensor maps,
+// kernel enqueue for the refresh and the cached iteration, and the CUDA
+// graphs that run the whole block loop on the device.
+//
+// The iteration loop follows the dInfer README's system notes (CUDA Graphs and
+// loop unrolling to remove stream bubbles between diffusion iterations): here
+// the block loop and the per-block iteration loop are CUDA graph conditional
+// WHILE nodes whose conditions are set on the device by the commit, so a
+// whole generation is one graph launch with no host round trip.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/dinfer.h"
+#include "../../include/dinfer_ops.h"
+#include "attention.cuh"
+#include "gemm_tc.cuh"
+#include "lmhead_tc.cuh"
+#include "small_kernels.cuh"
+
+using namespace dinfer;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 matrix [rows, cols] row-major, boxes of box_rows x 64 with the 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int bn_for_rows(int M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
+
+int g_num_sms = 0;
+int num_sms() {
+  if (!g_num_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return g_num_sms;
+}
+
+bool set_smem_attrs() {
+  static bool done = false;
+  if (done) return true;
+  bool ok = true;
+  ok &= cudaFuncSetAttribute(gemm_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GemmCfg<64>::kSmem) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GemmCfg<128>::kSmem) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GemmCfg<256>::kSmem) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(lmhead_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LmCfg<64>::kSmem) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(lmhead_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LmCfg<128>::kSmem) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(lmhead_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LmCfg<256>::kSmem) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem) ==
+        cudaSuccess;
+  ok &= cudaFuncSetAttribute(lmhead_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
+        cudaSuccess;
+  ok &= cudaFuncSetAttribute(attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
+        cudaSuccess;
+  done = ok;
+  return ok;
+}
+
+// Stream-K fixup workspace: floats per CTA slot pair and the ticket count.
+size_t gemm_ws_floats(int grid) { return (size_t)grid * 2 * 256 * 128; }
+
+// Launch the tensor-core GEMM (templated on the token tile).
+cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s) {
+  a.m_tiles = (a.M + BN - 1) / BN;
+  a.k_tiles = a.K / 64;
+  a.stream_k = 1;
+  const int grid = num_sms();
+  switch (BN) {
+    case 64:
+      gemm_tc_kernel<64><<<grid, kGemmThreads, GemmCfg<64>::kSmem, s>>>(maps, a);
+      break;
+    case 128:
+      gemm_tc_kernel<128><<<grid, kGemmThreads, GemmCfg<128>::kSmem, s>>>(maps, a);
+      break;
+    default:
+      gemm_tc_kernel<256><<<grid, kGemmThreads, GemmCfg<256>::kSmem, s>>>(maps, a);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lmhead_tc(const GemmMaps& maps, GemmArgs ga, const LmArgs& la, int BN, cudaStream_t s) {
+  ga.m_tiles = (ga.M + BN - 1) / BN;
+  ga.k_tiles = ga.K / 64;
+  ga.stream_k = 0;
+  const int grid = num_sms();
+  switch (BN) {
+    case 64:
+      lmhead_tc_kernel<64><<<grid, kGemmThreads, LmCfg<64>::kSmem, s>>>(maps, ga, la);
+      break;
+    case 128:
+      lmhead_tc_kernel<128><<<grid, kGemmThreads, LmCfg<128>::kSmem, s>>>(maps, ga, la);
+      break;
+    default:
+      lmhead_tc_kernel<256><<<grid, kGemmThreads, LmCfg<256>::kSmem, s>>>(maps, ga, la);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+struct AttnPlan {
+  int q_tiles, splits, cps;
+};
+AttnPlan plan_attention(int batch, int rows_per_seq, int heads, int L) {
+  AttnPlan p;
+  p.q_tiles = (rows_per_seq + 63) / 64;
+  const int n_chunks = (L + kKeyChunk - 1) / kKeyChunk;
+  const int base = batch * p.q_tiles * heads;
+  int want = (2 * num_sms() + base - 1) / base;
+  if (want < 1) want = 1;
+  if (want > n_chunks) want = n_chunks;
+  p.cps = (n_chunks + want - 1) / want;
+  p.splits = (n_chunks + p.cps - 1) / p.cps;
+  return p;
+}
+
+struct GraphSet {
+  cudaGraphExec_t exec = nullptr;
+  cudaGraph_t graph = nullptr;
+};
+
+}  // namespace
+
+// ===========================================================================
+// context
+// ===========================================================================
+struct dinfer_ctx {
+  dinfer_model_desc desc{};
+  std::vector<const void*> w;
+  bool bf16 = true;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  cudaStream_t cap_stream = nullptr, cap_stream2 = nullptr;
+  std::string err;
+  std::vector<void*> allocs;
+
+  size_t max_rows = 0;  // max_batch * max_seq
+  float* h = nullptr;
+  void* xn = nullptr;
+  void* q = nullptr;
+  void* attn_o = nullptr;
+  void* act = nullptr;
+  float* qkv32 = nullptr;
+  float* gu32 = nullptr;
+  void* kc = nullptr;
+  void* vc = nullptr;
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+  int32_t* ids = nullptr;
+  uint8_t* mask = nullptr;
+  int32_t* prompt_dev = nullptr;
+  int32_t* committed_dev = nullptr;
+  DevState* st = nullptr;
+  DevState* st_host = nullptr;  // pinned
+  float* gemm_ws = nullptr;
+  int* tickets = nullptr;
+  size_t n_tickets = 0;
+  SoftmaxState* lm_part = nullptr;
+  int* lm_ticket = nullptr;
+  float* attn_part_o = nullptr;
+  float* attn_part_ml = nullptr;
+  size_t attn_part_rows = 0;  // capacity in (splits * rows)
+  int* attn_tickets = nullptr;
+  size_t n_attn_tickets = 0;
+
+  // weight maps (bf16)
+  std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
+  CUtensorMap m_lm{};
+
+  float* dbg_logits = nullptr;
+  int32_t* dbg_tok = nullptr;
+  float* dbg_conf = nullptr;
+
+  // geometry of the last prefill (for dinfer_block_step)
+  int cur_batch = 0, cur_L = 0, cur_B = 0, cur_s = 0;
+  bool have_prefill = false;
+
+  std::map<std::tuple<int, int, int, int, int>, GraphSet> graphs;  // (kind, b, L, B, extra)
+  cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+
+  size_t cache_layer_elems() const { return (size_t)desc.max_batch * desc.max_seq * desc.d_model; }
+  size_t esize() const { return bf16 ? 2 : 4; }
+  void* kc_layer(int l) const { return (char*)kc + (size_t)l * cache_layer_elems() * esize(); }
+  void* vc_layer(int l) const { return (char*)vc + (size_t)l * cache_layer_elems() * esize(); }
+  const void* W(int i) const { return w[i]; }
+  const void* LW(int l, int j) const { return w[1 + 9 * l + j]; }
+};
+
+namespace {
+
+dinfer_status fail(dinfer_ctx* c, dinfer_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c) c->err = buf; else g_create_error = buf;
+  return s;
+}
+
+#define CK(call)                                                                              \
+  do {                                                                                        \
+    cudaError_t e_ = (call);                                                                  \
+    if (e_ != cudaSuccess) return fail(c, DINFER_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+template <typename T>
+dinfer_status dalloc(dinfer_ctx* c, T** p, size_t bytes) {
+  void* q = nullptr;
+  if (bytes == 0) bytes = 16;
+  if (cudaMalloc(&q, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(c, DINFER_ENOMEM, "cudaMalloc of %zu bytes failed", bytes);
+  }
+  c->allocs.push_back(q);
+  *p = reinterpret_cast<T*>(q);
+  return DINFER_OK;
+}
+
+const char* validate_desc(const dinfer_model_desc* d) {
+  if (!d) return "null model description";
+  if (d->n_layers < 1 || d->d_model < 1 || d->n_heads < 1 || d->head_dim < 2 || d->vocab < 2)
+    return "non-positive model dimension";
+  if (d->n_heads * d->head_dim != d->d_model) return "n_heads * head_dim != d_model";
+  if (d->head_dim % 2) return "head_dim must be even";
+  if (d->mask_id < 0 || d->mask_id >= d->vocab) return "mask_id outside [0, vocab)";
+  if (d->dtype != DINFER_FP32 && d->dtype != DINFER_BF16) return "dtype must be DINFER_FP32 or DINFER_BF16";
+  if (d->n_experts != 0 || d->top_k != 0 || d->expert_ffn != 0) {
+    if (d->n_experts < 1 || d->top_k < 1 || d->top_k > d->n_experts || d->expert_ffn < 1)
+      return "inconsistent MoE fields";
+    return "mixture-of-experts models are not supported by this build";
+  }
+  if (d->ffn < 1) return "ffn must be positive";
+  if (d->max_batch < 1 || d->max_batch > kMaxBatch) return "max_batch must be in [1, 64]";
+  if (d->max_seq < 1) return "max_seq must be positive";
+  if (!(d->rms_eps >= 0.f) || !(d->rope_theta > 0.f) || !std::isfinite(d->logit_scale)) return "bad float field";
+  if (d->dtype == DINFER_BF16) {
+    if (d->head_dim != 128) return "bf16 models need head_dim 128";
+    if (d->d_model % 128) return "bf16 models need d_model % 128 == 0";
+    if (d->ffn % 64) return "bf16 models need ffn % 64 == 0";
+    if (d->vocab % 8) return "bf16 models need vocab % 8 == 0";
+  } else {
+    if ((size_t)d->d_model * 4 * 64 > 192 * 1024) return "fp32 models need d_model <= 768";
+  }
+  return nullptr;
+}
+
+// ---------------------------------------------------------------------------
+// geometry of one forward
+// ---------------------------------------------------------------------------
+struct Fwd {
+  int batch, L, B;
+  int rows;          // rows computed: batch * B (iteration) or batch * L (refresh)
+  int rows_per_seq;  // B or L
+  int pos_from_state;
+  bool refresh;
+  // decode
+  int commit;
+  int count_iteration;
+  cudaGraphConditionalHandle cond;
+  int use_cond;
+  float threshold;
+};
+
+// Split-key attention partials are sized at creation: splits > 1 only when
+// batch * q_tiles * heads < 2 * SMs, which bounds splits * rows * heads by
+// 4 * SMs * 64.
+dinfer_status ensure_attn_ws(dinfer_ctx* c, const AttnPlan& p, int rows) {
+  const size_t need = (size_t)p.splits * rows;
+  if (p.splits > 1 && need * c->desc.n_heads > c->attn_part_rows)
+    return fail(c, DINFER_EINVAL, "attention split workspace too small (%zu rows)", need);
+  return DINFER_OK;
+}
+
+// Enqueue one forward over f.rows rows, final norm of the block rows, LM head,
+// decode and (optionally) the commit.  Works eagerly or under stream capture.
+dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
+  const dinfer_model_desc& d = c->desc;
+  const int D = d.d_model, F = d.ffn, H = d.n_heads, hd = d.head_dim;
+  const int rows = f.rows;
+  RowMap rm{f.rows_per_seq, f.L, f.pos_from_state};
+  // a1: embedding
+  if (c->bf16)
+    embed_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>((const __nv_bfloat16*)c->W(0), c->ids, c->h, rows, D, d.vocab,
+                                                     rm, c->st);
+  else
+    embed_kernel<float><<<rows, 256, 0, s>>>((const float*)c->W(0), c->ids, c->h, rows, D, d.vocab, rm, c->st);
+  CK(cudaGetLastError());
+
+  const int BN = bn_for_rows(rows);
+  GemmMaps mx{}, mo{}, mact{};
+  if (c->bf16) {
+    if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BN) ||
+        !make_map(&mact.b, c->act, rows, F, BN))
+      return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
+  }
+  const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
+  if (c->bf16) {
+    dinfer_status st = ensure_attn_ws(c, ap, rows);
+    if (st != DINFER_OK) return st;
+  }
+
+  for (int l = 0; l < d.n_layers; ++l) {
+    // a2: RMSNorm -> QKV GEMM (+RoPE, cache write)
+    if (c->bf16)
+      rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<rows, 256, 0, s>>>(
+          c->h, (const __nv_bfloat16*)c->LW(l, 0), (__nv_bfloat16*)c->xn, rows, D, d.rms_eps, 0, rm, c->st);
+    else
+      rmsnorm_kernel<float, float><<<rows, 256, 0, s>>>(c->h, (const float*)c->LW(l, 0), (float*)c->xn, rows, D,
+                                                        d.rms_eps, 0, rm, c->st);
+    CK(cudaGetLastError());
+    if (c->bf16) {
+      GemmMaps m = mx;
+      m.a[0] = c->m_wq[l];
+      m.a[1] = c->m_wk[l];
+      m.a[2] = c->m_wv[l];
+      GemmArgs a{};
+      a.M = rows; a.N = 3 * D; a.K = D;
+      a.n_tiles = 3 * D / 128;
+      a.a_mode = A_THREE; a.a_rows = D;
+      a.q_out = (__nv_bfloat16*)c->q;
+      a.k_cache = (__nv_bfloat16*)c->kc_layer(l);
+      a.v_cache = (__nv_bfloat16*)c->vc_layer(l);
+      a.rope_cos = c->rope_cos; a.rope_sin = c->rope_sin;
+      a.d_model = D; a.head_dim = hd;
+      a.rows_per_seq = f.rows_per_seq; a.seq_len = f.L; a.pos_from_state = f.pos_from_state;
+      a.state = c->st; a.ws = c->gemm_ws; a.tickets = c->tickets; a.status = c->st;
+      CK(launch_gemm_tc(m, a, BN, s));
+    } else {
+      dim3 g1((3 * D + 63) / 64, (rows + 63) / 64);
+      // three column blocks of one [rows, 3D] output
+      for (int j = 0; j < 3; ++j) {
+        dim3 g((D + 63) / 64, (rows + 63) / 64);
+        gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 1 + j), c->qkv32 + j * D,
+                                          rows, D, D, 3 * D, 0);
+      }
+      (void)g1;
+      CK(cudaGetLastError());
+      rope_cache_f32_kernel<<<rows, 256, 0, s>>>(c->qkv32, (float*)c->q, (float*)c->kc_layer(l),
+                                                  (float*)c->vc_layer(l), c->rope_cos, c->rope_sin, rows, D, hd, rm,
+                                                  c->st);
+      CK(cudaGetLastError());
+    }
+    // a3: attention over the dual cache
+    if (c->bf16) {
+      AttnArgs aa{};
+      aa.q = (const __nv_bfloat16*)c->q;
+      aa.k = (const __nv_bfloat16*)c->kc_layer(l);
+      aa.v = (const __nv_bfloat16*)c->vc_layer(l);
+      aa.o = (__nv_bfloat16*)c->attn_o;
+      aa.d = D; aa.heads = H; aa.L = f.L; aa.rows_per_seq = f.rows_per_seq;
+      aa.q_tiles = ap.q_tiles; aa.splits = ap.splits; aa.chunks_per_split = ap.cps;
+      aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+      aa.part_o = c->attn_part_o; aa.part_ml = c->attn_part_ml; aa.tickets = c->attn_tickets;
+      dim3 g(f.batch * ap.q_tiles, H, ap.splits);
+      attn_bf16_kernel<<<g, kAttnThreads, kAttnSmem, s>>>(aa);
+    } else {
+      AttnF32Args aa{(const float*)c->q, (const float*)c->kc_layer(l), (const float*)c->vc_layer(l),
+                     (float*)c->attn_o, D, H, hd, f.L, f.rows_per_seq, 1.f / sqrtf((float)hd)};
+      dim3 g(rows, H);
+      attn_f32_kernel<<<g, 128, (size_t)(f.L + hd) * sizeof(float), s>>>(aa);
+    }
+    CK(cudaGetLastError());
+    // a4: O projection + residual
+    if (c->bf16) {
+      GemmMaps m = mo;
+      m.a[0] = c->m_wo[l];
+      GemmArgs a{};
+      a.M = rows; a.N = D; a.K = D; a.n_tiles = D / 128; a.a_mode = A_SINGLE;
+      a.resid = c->h; a.ws = c->gemm_ws; a.tickets = c->tickets; a.status = c->st; a.state = c->st;
+      CK(launch_gemm_tc(m, a, BN, s));
+    } else {
+      dim3 g((D + 63) / 64, (rows + 63) / 64);
+      gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->attn_o, (const float*)c->LW(l, 4), c->h, rows, D, D, D, 1);
+      CK(cudaGetLastError());
+    }
+    // a5: RMSNorm -> SwiGLU FFN + residual
+    if (c->bf16)
+      rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<rows, 256, 0, s>>>(
+          c->h, (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, rows, D, d.rms_eps, 0, rm, c->st);
+    else
+      rmsnorm_kernel<float, float><<<rows, 256, 0, s>>>(c->h, (const float*)c->LW(l, 5), (float*)c->xn, rows, D,
+                                                        d.rms_eps, 0, rm, c->st);
+    CK(cudaGetLastError());
+    if (c->bf16) {
+      GemmMaps m = mx;
+      m.a[0] = c->m_wg[l];
+      m.a[1] = c->m_wu[l];
+      GemmArgs a{};
+      a.M = rows; a.N = F; a.K = D; a.n_tiles = F / 64; a.a_mode = A_PAIR;
+      a.out_bf16 = (__nv_bfloat16*)c->act; a.ldo = F;
+      a.ws = c->gemm_ws; a.tickets = c->tickets; a.status = c->st; a.state = c->st;
+      CK(launch_gemm_tc(m, a, BN, s));
+      GemmMaps m2 = mact;
+      m2.a[0] = c->m_wd[l];
+      GemmArgs b{};
+      b.M = rows; b.N = D; b.K = F; b.n_tiles = D / 128; b.a_mode = A_SINGLE;
+      b.resid = c->h; b.ws = c->gemm_ws; b.tickets = c->tickets; b.status = c->st; b.state = c->st;
+      CK(launch_gemm_tc(m2, b, BN, s));
+    } else {
+      dim3 g((F + 63) / 64, (rows + 63) / 64);
+      gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 6), c->gu32, rows, F, D, 2 * F, 0);
+      gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 7), c->gu32 + F, rows, F, D, 2 * F,
+                                        0);
+      swiglu_f32_kernel<<<256, 256, 0, s>>>(c->gu32, (float*)c->act, rows, F);
+      dim3 g2((D + 63) / 64, (rows + 63) / 64);
+      gemm_f32_kernel<<<g2, 256, 0, s>>>((const float*)c->act, (const float*)c->LW(l, 8), c->h, rows, D, F, D, 1);
+      CK(cudaGetLastError());
+    }
+  }
+
+  // a6: final norm of the block rows (gathered from the full sequence at a refresh)
+  const int brows = f.batch * f.B;
+  RowMap rb{f.B, f.L, 1};
+  const int gather = f.refresh ? 1 : 0;
+  const void* gfin = c->W(1 + 9 * d.n_layers);
+  if (c->bf16)
+    rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<brows, 256, 0, s>>>(
+        c->h, (const __nv_bfloat16*)gfin, (__nv_bfloat16*)c->xn, brows, D, d.rms_eps, gather, rb, c->st);
+  else
+    rmsnorm_kernel<float, float><<<brows, 256, 0, s>>>(c->h, (const float*)gfin, (float*)c->xn, brows, D, d.rms_eps,
+                                                       gather, rb, c->st);
+  CK(cudaGetLastError());
+
+  // a6 + a7: LM head, online softmax, threshold commit
+  DecodeArgs dec{};
+  dec.M = brows; dec.batch = f.batch; dec.L = f.L; dec.B = f.B;
+  dec.threshold = f.threshold; dec.commit = f.commit;
+  dec.ids = c->ids; dec.mask = c->mask;
+  dec.tok_out = c->dbg_tok; dec.conf_out = c->dbg_conf;
+  dec.committed_out = c->committed_dev;
+  dec.state = c->st; dec.count_iteration = f.count_iteration;
+  dec.cond = f.cond; dec.use_cond = f.use_cond;
+  dec.partials = c->lm_part; dec.ticket = c->lm_ticket;
+  if (c->bf16) {
+    const int BNl = bn_for_rows(brows);
+    GemmMaps m{};
+    m.a[0] = c->m_lm;
+    if (!make_map(&m.b, c->xn, brows, D, BNl)) return fail(c, DINFER_ECUDA, "tensor map encoding failed (lm)");
+    GemmArgs ga{};
+    ga.M = brows; ga.N = d.vocab; ga.K = D; ga.n_tiles = (d.vocab + 127) / 128; ga.a_mode = A_SINGLE;
+    ga.status = c->st; ga.state = c->st;
+    dec.n_parts = num_sms();
+    LmArgs la{d.vocab, d.mask_id, d.logit_scale, c->dbg_logits, dec};
+    CK(launch_lmhead_tc(m, ga, la, BNl, s));
+  } else {
+    const int grid = std::min(num_sms(), (d.vocab + 127) / 128);
+    dec.n_parts = grid;
+    LmF32Args la{(const float*)c->xn, (const float*)c->W(2 + 9 * d.n_layers), brows, D, d.vocab, d.mask_id,
+                 d.logit_scale, c->dbg_logits, dec};
+    lmhead_f32_kernel<<<grid, 128, (size_t)brows * D * sizeof(float), s>>>(la);
+    CK(cudaGetLastError());
+  }
+  return DINFER_OK;
+}
+
+bool debug_on(const dinfer_ctx* c) { return c->dbg_logits || c->dbg_tok || c->dbg_conf; }
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+dinfer_status read_status(dinfer_ctx* c) {
+  CK(cudaMemcpyAsync(c->st_host, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  if (c->st_host->status)
+    return fail(c, DINFER_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad token, 4 NaN confidence, 8 "
+                "iteration overflow)", c->st_host->status);
+  return DINFER_OK;
+}
+
+// Capture a graph that runs one forward (refresh or cached iteration).
+dinfer_status build_step_graph(dinfer_ctx* c, const Fwd& f, GraphSet& gs) {
+  cudaStream_t s = c->cap_stream;
+  CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+  dinfer_status st = enqueue_forward(c, f, s);
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(s, &g);
+  if (st != DINFER_OK) {
+    if (g) cudaGraphDestroy(g);
+    return st;
+  }
+  if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "stream capture failed: %s", cudaGetErrorString(e));
+  e = cudaGraphInstantiate(&gs.exec, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return fail(c, DINFER_ECUDA, "graph instantiation failed: %s", cudaGetErrorString(e));
+  }
+  gs.graph = g;
+  return DINFER_OK;
+}
+
+// Add a WHILE conditional node at the current capture point of stream s and
+// return its body graph; subsequent captured work depends on the node.
+dinfer_status add_while_node(dinfer_ctx* c, cudaStream_t s, cudaGraphConditionalHandle h, cudaGraph_t* body) {
+  cudaStreamCaptureStatus cs;
+  cudaGraph_t cg = nullptr;
+  const cudaGraphNode_t* deps = nullptr;
+  size_t ndeps = 0;
+  CK(cudaStreamGetCaptureInfo(s, &cs, nullptr, &cg, &deps, nullptr, &ndeps));
+  if (cs != cudaStreamCaptureStatusActive) return fail(c, DINFER_ECUDA, "stream is not capturing");
+  cudaGraphNodeParams p{};
+  p.type = cudaGraphNodeTypeConditional;
+  p.conditional.handle = h;
+  p.conditional.type = cudaGraphCondTypeWhile;
+  p.conditional.size = 1;
+  cudaGraphNode_t node;
+  CK(cudaGraphAddNode(&node, cg, deps, nullptr, ndeps, &p));
+  *body = p.conditional.phGraph_out[0];
+  CK(cudaStreamUpdateCaptureDependencies(s, &node, nullptr, 1, cudaStreamSetCaptureDependencies));
+  return DINFER_OK;
+}
+
+// Whole-generation graph: init; while (blocks left) { refresh + commit;
+// while (masks left) { cached iteration + commit } ; next block }.
+dinfer_status build_generate_graph(dinfer_ctx* c, int batch, int P, int G, int B, float thr, GraphSet& gs) {
+  const int L = P + G;
+  cudaStream_t s = c->cap_stream, s2 = c->cap_stream2;
+  cudaGraph_t g = nullptr;
+  CK(cudaGraphCreate(&g, 0));
+  dinfer_status st = DINFER_OK;
+  cudaGraph_t body_o = nullptr, body_i = nullptr;
+  cudaGraphConditionalHandle h_o, h_i;
+  // top level
+  CK(cudaGraphConditionalHandleCreate(&h_o, g, 1, cudaGraphCondAssignDefault));
+  CK(cudaStreamBeginCaptureToGraph(s, g, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
+  init_sequence_kernel<<<256, 256, 0, s>>>(c->prompt_dev, c->ids, c->mask, batch, P, L, c->desc.mask_id, c->st,
+                                           G / B);
+  st = add_while_node(c, s, h_o, &body_o);
+  {
+    cudaGraph_t g2 = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s, &g2);
+    if (st != DINFER_OK) return st;
+    if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "capture (top): %s", cudaGetErrorString(e));
+  }
+  // outer body: one block
+  CK(cudaGraphConditionalHandleCreate(&h_i, body_o, 0, cudaGraphCondAssignDefault));
+  CK(cudaStreamBeginCaptureToGraph(s2, body_o, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
+  begin_block_kernel<<<1, 1, 0, s2>>>(c->st);
+  Fwd fr{batch, L, B, batch * L, L, 0, true, 1, 1, 0, 0, thr};
+  st = enqueue_forward(c, fr, s2);
+  if (st == DINFER_OK) {
+    set_inner_cond_kernel<<<1, 1, 0, s2>>>(c->st, h_i);
+    st = add_while_node(c, s2, h_i, &body_i);
+  }
+  if (st == DINFER_OK) advance_block_kernel<<<1, 1, 0, s2>>>(c->st, B, h_o, 1);
+  {
+    cudaGraph_t g2 = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s2, &g2);
+    if (st != DINFER_OK) return st;
+    if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "capture (block): %s", cudaGetErrorString(e));
+  }
+  // inner body: one cached iteration
+  CK(cudaStreamBeginCaptureToGraph(s2, body_i, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
+  Fwd fi{batch, L, B, batch * B, B, 1, false, 1, 1, h_i, 1, thr};
+  st = enqueue_forward(c, fi, s2);
+  {
+    cudaGraph_t g2 = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s2, &g2);
+    if (st != DINFER_OK) return st;
+    if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "capture (iteration): %s", cudaGetErrorString(e));
+  }
+  cudaError_t e = cudaGraphInstantiate(&gs.exec, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return fail(c, DINFER_ECUDA, "graph instantiation failed: %s", cudaGetErrorString(e));
+  }
+  gs.graph = g;
+  return DINFER_OK;
+}
+
+dinfer_status check_geometry(dinfer_ctx* c, int batch, int L, int B) {
+  if (batch < 1 || batch > c->desc.max_batch) return fail(c, DINFER_EINVAL, "batch %d outside [1, %d]", batch,
+                                                          c->desc.max_batch);
+  if (L < 1 || L > c->desc.max_seq) return fail(c, DINFER_EINVAL, "sequence length %d outside [1, %d]", L,
+                                                c->desc.max_seq);
+  if (B < 1 || B > L) return fail(c, DINFER_EINVAL, "block length %d outside [1, %d]", B, L);
+  if (batch * B > 1024) return fail(c, DINFER_EINVAL, "batch * block_length must be <= 1024");
+  if (!c->bf16 && (size_t)batch * B * c->desc.d_model * 4 > 200 * 1024)
+    return fail(c, DINFER_EINVAL, "fp32 models: batch * block_length * d_model too large");
+  return DINFER_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+int32_t dinfer_num_weights(const dinfer_model_desc* desc) {
+  if (!desc || desc->n_layers < 1) return -1;
+  return 1 + 9 * desc->n_layers + 2;
+}
+
+const char* dinfer_last_error(const dinfer_ctx* ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
+
+void dinfer_destroy(dinfer_ctx* c) {
+  if (!c) return;
+  if (c->stream) cudaStreamSynchronize(c->stream);
+  for (auto& kv : c->graphs) {
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    if (kv.second.graph) cudaGraphDestroy(kv.second.graph);
+  }
+  for (void* p : c->allocs) cudaFree(p);
+  if (c->st_host) cudaFreeHost(c->st_host);
+  if (c->ev0) cudaEventDestroy(c->ev0);
+  if (c->ev1) cudaEventDestroy(c->ev1);
+  if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+  if (c->cap_stream2) cudaStreamDestroy(c->cap_stream2);
+  if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+  delete c;
+}
+
+dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* weights, void* stream,
+                            dinfer_ctx** out) {
+  if (!out) return fail(nullptr, DINFER_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (const char* why = validate_desc(desc)) return fail(nullptr, DINFER_EINVAL, "%s", why);
+  if (!weights) return fail(nullptr, DINFER_EINVAL, "weights is NULL");
+  const int nw = dinfer_num_weights(desc);
+  for (int i = 0; i < nw; ++i)
+    if (!weights[i]) return fail(nullptr, DINFER_EINVAL, "weight %d is NULL", i);
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
+    cudaGetLastError();
+    return fail(nullptr, DINFER_ECUDA, "no CUDA device");
+  }
+  if (!set_smem_attrs()) return fail(nullptr, DINFER_ECUDA, "cudaFuncSetAttribute failed");
+  if (!get_encode_fn()) return fail(nullptr, DINFER_ECUDA, "cuTensorMapEncodeTiled unavailable");
+
+  dinfer_ctx* c = new dinfer_ctx();
+  c->desc = *desc;
+  c->bf16 = desc->dtype == DINFER_BF16;
+  c->w.assign(weights, weights + nw);
+  auto bail = [&](dinfer_status s) {
+    g_create_error = c->err;
+    dinfer_destroy(c);
+    return s;
+  };
+#define CKC(call)                                                                                     \
+  do {                                                                                                \
+    cudaError_t e_ = (call);                                                                          \
+    if (e_ != cudaSuccess) {                                                                          \
+      fail(c, DINFER_ECUDA, "%s: %s", #call, cudaGetErrorString(e_));                                 \
+      return bail(DINFER_ECUDA);                                                                      \
+    }                                                                                                 \
+  } while (0)
+#define AL(ptr, bytes)                                   \
+  do {                                                   \
+    dinfer_status s_ = dalloc(c, &(ptr), (bytes));       \
+    if (s_ != DINFER_OK) return bail(s_);                \
+  } while (0)
+
+  if (stream) {
+    c->stream = reinterpret_cast<cudaStream_t>(stream);
+  } else {
+    CKC(cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking));
+    c->own_stream = true;
+  }
+  CKC(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
+  CKC(cudaStreamCreateWithFlags(&c->cap_stream2, cudaStreamNonBlocking));
+  CKC(cudaEventCreate(&c->ev0));
+  CKC(cudaEventCreate(&c->ev1));
+
+  const size_t D = desc->d_model, F = desc->ffn, es = c->esize();
+  c->max_rows = (size_t)desc->max_batch * desc->max_seq;
+  AL(c->h, c->max_rows * D * 4);
+  AL(c->xn, c->max_rows * D * es);
+  AL(c->q, c->max_rows * D * es);
+  AL(c->attn_o, c->max_rows * D * es);
+  AL(c->act, c->max_rows * F * es);
+  if (!c->bf16) {
+    AL(c->qkv32, c->max_rows * 3 * D * 4);
+    AL(c->gu32, c->max_rows * 2 * F * 4);
+  }
+  AL(c->kc, c->cache_layer_elems() * desc->n_layers * es);
+  AL(c->vc, c->cache_layer_elems() * desc->n_layers * es);
+  const int half = desc->head_dim / 2;
+  AL(c->rope_cos, (size_t)desc->max_seq * half * 4);
+  AL(c->rope_sin, (size_t)desc->max_seq * half * 4);
+  {
+    // rotary table in double precision: angle = pos * theta^(-2i/hd)
+    std::vector<float> cs((size_t)desc->max_seq * half), sn((size_t)desc->max_seq * half);
+    for (int p = 0; p < desc->max_seq; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double inv = std::pow((double)desc->rope_theta, -2.0 * i / desc->head_dim);
+        const double ang = (double)p * inv;
+        cs[(size_t)p * half + i] = (float)std::cos(ang);
+        sn[(size_t)p * half + i] = (float)std::sin(ang);
+      }
+    CKC(cudaMemcpy(c->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
+    CKC(cudaMemcpy(c->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
+  }
+  AL(c->ids, c->max_rows * 4);
+  AL(c->mask, c->max_rows);
+  AL(c->prompt_dev, c->max_rows * 4);
+  AL(c->committed_dev, kMaxBatch * 4);
+  AL(c->st, sizeof(DevState));
+  CKC(cudaMemset(c->st, 0, sizeof(DevState)));
+  CKC(cudaMallocHost((void**)&c->st_host, sizeof(DevState)));
+  const int G = num_sms();
+  AL(c->gemm_ws, gemm_ws_floats(G) * 4);
+  // tickets: the largest tile count of any GEMM (rows up to max_rows, token tile >= 64)
+  {
+    const size_t mt = (c->max_rows + 63) / 64;
+    size_t nt = std::max<size_t>(3 * D / 128, F / 64);
+    c->n_tickets = mt * nt + 1;
+    AL(c->tickets, c->n_tickets * 4);
+    CKC(cudaMemset(c->tickets, 0, c->n_tickets * 4));
+  }
+  AL(c->lm_part, (size_t)G * 1024 * sizeof(SoftmaxState));
+  AL(c->lm_ticket, 16);
+  CKC(cudaMemset(c->lm_ticket, 0, 16));
+  if (c->bf16) {
+    c->attn_part_rows = (size_t)4 * G * 64;  // in units of (row, head)
+    AL(c->attn_part_o, c->attn_part_rows * desc->head_dim * 4);
+    AL(c->attn_part_ml, c->attn_part_rows * 2 * 4);
+  }
+  c->n_attn_tickets = (size_t)desc->max_batch * ((desc->max_seq + 63) / 64 + 1) * desc->n_heads;
+  AL(c->attn_tickets, c->n_attn_tickets * 4);
+  CKC(cudaMemset(c->attn_tickets, 0, c->n_attn_tickets * 4));
+
+  if (c->bf16) {
+    const int nl = desc->n_layers;
+    c->m_wq.resize(nl); c->m_wk.resize(nl); c->m_wv.resize(nl); c->m_wo.resize(nl);
+    c->m_wg.resize(nl); c->m_wu.resize(nl); c->m_wd.resize(nl);
+    bool ok = true;
+    for (int l = 0; l < nl; ++l) {
+      ok &= make_map(&c->m_wq[l], c->LW(l, 1), D, D, 128);
+      ok &= make_map(&c->m_wk[l], c->LW(l, 2), D, D, 128);
+      ok &= make_map(&c->m_wv[l], c->LW(l, 3), D, D, 128);
+      ok &= make_map(&c->m_wo[l], c->LW(l, 4), D, D, 128);
+      ok &= make_map(&c->m_wg[l], c->LW(l, 6), F, D, 64);
+      ok &= make_map(&c->m_wu[l], c->LW(l, 7), F, D, 64);
+      ok &= make_map(&c->m_wd[l], c->LW(l, 8), D, F, 128);
+    }
+    ok &= make_map(&c->m_lm, c->W(2 + 9 * nl), desc->vocab, D, 128);
+    if (!ok) {
+      fail(c, DINFER_EINVAL, "weight tensor maps could not be built (weights must be 16-byte aligned bf16)");
+      return bail(DINFER_EINVAL);
+    }
+  }
+  CKC(cudaDeviceSynchronize());
+  *out = c;
+  return DINFER_OK;
+#undef CKC
+#undef AL
+}
+
+dinfer_status dinfer_set_debug_outputs(dinfer_ctx* c, float* logits, int32_t* tok, float* conf) {
+  if (!c) return DINFER_EINVAL;
+  c->dbg_logits = logits;
+  c->dbg_tok = tok;
+  c->dbg_conf = conf;
+  return DINFER_OK;
+}
+
+dinfer_status dinfer_sync(dinfer_ctx* c) {
+  if (!c) return DINFER_EINVAL;
+  return read_status(c);
+}
+
+dinfer_status dinfer_prefill_cache(dinfer_ctx* c, int32_t* ids, uint8_t* mask, int32_t batch, int32_t seq_len,
+                                   int32_t block_start, int32_t block_len, float threshold, int32_t commit,
+                                   int32_t* committed) {
+  if (!c) return DINFER_EINVAL;
+  if (!ids || !mask) return fail(c, DINFER_EINVAL, "ids / mask is NULL");
+  dinfer_status st = check_geometry(c, batch, seq_len, block_len);
+  if (st != DINFER_OK) return st;
+  if (block_start < 0 || block_start + block_len > seq_len)
+    return fail(c, DINFER_EINVAL, "block [%d, %d) outside the sequence", block_start, block_start + block_len);
+  if (!(threshold == threshold)) return fail(c, DINFER_EINVAL, "threshold is NaN");
+  if (!is_device_ptr(ids) || !is_device_ptr(mask)) return fail(c, DINFER_EINVAL, "ids / mask must be device memory");
+  const size_t n = (size_t)batch * seq_len;
+  cudaStream_t s = c->stream;
+  CK(cudaMemcpyAsync(c->ids, ids, n * 4, cudaMemcpyDeviceToDevice, s));
+  CK(cudaMemcpyAsync(c->mask, mask, n, cudaMemcpyDeviceToDevice, s));
+  set_block_kernel<<<1, 1, 0, s>>>(c->st, block_start, 1);
+  CK(cudaGetLastError());
+  Fwd f{batch, seq_len, block_len, batch * seq_len, seq_len, 0, true, commit ? 1 : 0, 1, 0, 0, threshold};
+  if (debug_on(c)) {
+    st = enqueue_forward(c, f, s);
+    if (st != DINFER_OK) return st;
+  } else {
+    auto key = std::make_tuple(1, batch, seq_len, block_len, (int)(commit ? 1 : 0) ^ (int)(threshold * 1e6f) * 2);
+    GraphSet& gs = c->graphs[key];
+    if (!gs.exec) {
+      st = build_step_graph(c, f, gs);
+      if (st != DINFER_OK) {
+        c->graphs.erase(key);
+        return st;
+      }
+    }
+    CK(cudaGraphLaunch(gs.exec, s));
+  }
+  CK(cudaMemcpyAsync(ids, c->ids, n * 4, cudaMemcpyDeviceToDevice, s));
+  CK(cudaMemcpyAsync(mask, c->mask, n, cudaMemcpyDeviceToDevice, s));
+  if (committed) CK(cudaMemcpyAsync(committed, c->committed_dev, batch * 4, cudaMemcpyDeviceToDevice, s));
+  c->cur_batch = batch;
+  c->cur_L = seq_len;
+  c->cur_B = block_len;
+  c->cur_s = block_start;
+  c->have_prefill = true;
+  return DINFER_OK;
+}
+
+dinfer_status dinfer_block_step(dinfer_ctx* c, int32_t* ids, uint8_t* mask, float threshold, int32_t* committed) {
+  if (!c) return DINFER_EINVAL;
+  if (!c->have_prefill) return fail(c, DINFER_ESTATE, "dinfer_block_step before dinfer_prefill_cache");
+  if (!ids || !mask) return fail(c, DINFER_EINVAL, "ids / mask is NULL");
+  if (!(threshold == threshold)) return fail(c, DINFER_EINVAL, "threshold is NaN");
+  if (!is_device_ptr(ids) || !is_device_ptr(mask)) return fail(c, DINFER_EINVAL, "ids / mask must be device memory");
+  const int batch = c->cur_batch, L = c->cur_L, B = c->cur_B;
+  const size_t n = (size_t)batch * L;
+  cudaStream_t s = c->stream;
+  CK(cudaMemcpyAsync(c->ids, ids, n * 4, cudaMemcpyDeviceToDevice, s));
+  CK(cudaMemcpyAsync(c->mask, mask, n, cudaMemcpyDeviceToDevice, s));
+  set_block_kernel<<<1, 1, 0, s>>>(c->st, c->cur_s, 0);
+  CK(cudaGetLastError());
+  Fwd f{batch, L, B, batch * B, B, 1, false, 1, 1, 0, 0, threshold};
+  dinfer_status st;
+  if (debug_on(c)) {
+    st = enqueue_forward(c, f, s);
+    if (st != DINFER_OK) return st;
+  } else {
+    auto key = std::make_tuple(2, batch, L, B, (int)(threshold * 1e6f));
+    GraphSet& gs = c->graphs[key];
+    if (!gs.exec) {
+      st = build_step_graph(c, f, gs);
+      if (st != DINFER_OK) {
+        c->graphs.erase(key);
+        return st;
+      }
+    }
+    CK(cudaGraphLaunch(gs.exec, s));
+  }
+  CK(cudaMemcpyAsync(ids, c->ids, n * 4, cudaMemcpyDeviceToDevice, s));
+  CK(cudaMemcpyAsync(mask, c->mask, n, cudaMemcpyDeviceToDevice, s));
+  if (committed) CK(cudaMemcpyAsync(committed, c->committed_dev, batch * 4, cudaMemcpyDeviceToDevice, s));
+  return DINFER_OK;
+}
+
+dinfer_status dinfer_generate(dinfer_ctx* c, const int32_t* prompt, int32_t batch, int32_t prompt_len,
+                              int32_t gen_length, int32_t block_length, float threshold, int32_t* out,
+                              dinfer_stats* stats) {
+  if (!c) return DINFER_EINVAL;
+  if (!prompt || !out) return fail(c, DINFER_EINVAL, "prompt / out is NULL");
+  if (prompt_len < 0 || gen_length < 1 || block_length < 1 || gen_length % block_length)
+    return fail(c, DINFER_EINVAL, "gen_length must be a positive multiple of block_length");
+  const int L = prompt_len + gen_length;
+  dinfer_status st = check_geometry(c, batch, L, block_length);
+  if (st != DINFER_OK) return st;
+  if (gen_length / block_length > kMaxBlocks) return fail(c, DINFER_EINVAL, "too many blocks");
+  if (!(threshold == threshold)) return fail(c, DINFER_EINVAL, "threshold is NaN");
+  cudaStream_t s = c->stream;
+  const bool p_dev = is_device_ptr(prompt), o_dev = is_device_ptr(out);
+  CK(cudaEventRecord(c->ev0, s));
+  if (prompt_len > 0)
+    CK(cudaMemcpyAsync(c->prompt_dev, prompt, (size_t)batch * prompt_len * 4,
+                       p_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, s));
+  const int B = block_length, nblk = gen_length / block_length;
+  const bool eager = debug_on(c) || getenv("DINFER_NO_GRAPH") != nullptr;
+  if (eager) {
+    init_sequence_kernel<<<256, 256, 0, s>>>(c->prompt_dev, c->ids, c->mask, batch, prompt_len, L, c->desc.mask_id,
+                                             c->st, nblk);
+    CK(cudaGetLastError());
+    for (int b = 0; b < nblk; ++b) {
+      begin_block_kernel<<<1, 1, 0, s>>>(c->st);
+      Fwd fr{batch, L, B, batch * L, L, 0, true, 1, 1, 0, 0, threshold};
+      st = enqueue_forward(c, fr, s);
+      if (st != DINFER_OK) return st;
+      for (int it = 1; it < B + 1; ++it) {
+        CK(cudaMemcpyAsync(c->st_host, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        if (!c->st_host->any_masked || c->st_host->status) break;
+        Fwd fi{batch, L, B, batch * B, B, 1, false, 1, 1, 0, 0, threshold};
+        st = enqueue_forward(c, fi, s);
+        if (st != DINFER_OK) return st;
+      }
+      advance_block_kernel<<<1, 1, 0, s>>>(c->st, B, 0, 0);
+      CK(cudaGetLastError());
+    }
+  } else {
+    auto key = std::make_tuple(3, batch, prompt_len, gen_length * 4096 + block_length, (int)(threshold * 1e6f));
+    GraphSet& gs = c->graphs[key];
+    if (!gs.exec) {
+      st = build_generate_graph(c, batch, prompt_len, gen_length, block_length, threshold, gs);
+      if (st != DINFER_OK) {
+        c->graphs.erase(key);
+        return st;
+      }
+    }
+    CK(cudaGraphLaunch(gs.exec, s));
+  }
+  // output: ids [batch, L]
+  CK(cudaMemcpyAsync(out, c->ids, (size_t)batch * L * 4, o_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost,
+                     s));
+  CK(cudaEventRecord(c->ev1, s));
+  st = read_status(c);
+  if (stats) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, c->ev0, c->ev1);
+    stats->n_blocks = nblk;
+    stats->iterations = c->st_host->total_iterations;
+    stats->refreshes = c->st_host->refreshes;
+    stats->ms_device = ms;
+    if (stats->iters_per_block)
+      for (int b = 0; b < nblk && b < kMaxBlocks; ++b) stats->iters_per_block[b] = c->st_host->iters_per_block[b];
+  }
+  return st;
+}
+
+}  // extern "C"
+
+// ===========================================================================
+// kernel-level entry points (include/dinfer_ops.h)
+// ===========================================================================
+namespace {
+constexpr size_t kOpStateBytes = 64 * 1024;          // DevState
+constexpr size_t kOpTicketBytes = 4u << 20;          // zeroed counters
+constexpr size_t kOpDataBytes = 160u << 20;
+struct OpWs {
+  DevState* st;
+  int* tickets;
+  uint8_t* data;
+  size_t data_bytes;
+};
+bool op_ws(void* ws, size_t bytes, OpWs& o) {
+  if (!ws || bytes < kOpStateBytes + kOpTicketBytes + 4096) return false;
+  uint8_t* p = reinterpret_cast<uint8_t*>(ws);
+  o.st = reinterpret_cast<DevState*>(p);
+  o.tickets = reinterpret_cast<int*>(p + kOpStateBytes);
+  o.data = p + kOpStateBytes + kOpTicketBytes;
+  o.data_bytes = bytes - kOpStateBytes - kOpTicketBytes;
+  return true;
+}
+}  // namespace
+
+extern "C" {
+
+size_t dinfer_op_workspace_bytes(void) { return kOpStateBytes + kOpTicketBytes + kOpDataBytes; }
+
+dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_t M, int32_t N, int32_t K,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  dinfer_ctx* c = nullptr;
+  if (!X || !W || !Y) return fail(c, DINFER_EINVAL, "NULL operand");
+  if (M < 1 || M > (1 << 20) || N < 128 || N % 128 || K < 64 || K % 64)
+    return fail(c, DINFER_EINVAL, "unsupported GEMM shape");
+  OpWs o;
+  if (!op_ws(workspace, workspace_bytes, o)) return fail(c, DINFER_EINVAL, "workspace too small");
+  const int G = num_sms();
+  if (gemm_ws_floats(G) * 4 > o.data_bytes) return fail(c, DINFER_EINVAL, "workspace too small");
+  const int BN = bn_for_rows(M);
+  if ((size_t)((M + BN - 1) / BN) * (N / 128) * 4 > kOpTicketBytes) return fail(c, DINFER_EINVAL, "too many tiles");
+  if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
+  GemmMaps m{};
+  if (!make_map(&m.a[0], W, N, K, 128) || !make_map(&m.b, X, M, K, BN))
+    return fail(c, DINFER_EINVAL, "tensor map encoding failed (alignment?)");
+  GemmArgs a{};
+  a.M = M; a.N = N; a.K = K; a.n_tiles = N / 128; a.a_mode = A_SINGLE;
+  a.out_f32 = Y; a.ldo = N;
+  a.ws = reinterpret_cast<float*>(o.data); a.tickets = o.tickets; a.status = o.st; a.state = o.st;
+  CK(launch_gemm_tc(m, a, BN, reinterpret_cast<cudaStream_t>(stream)));
+  return DINFER_OK;
+}
+
+dinfer_status dinfer_op_lmhead_bf16(const void* X, const void* W, int32_t M, int32_t V, int32_t K, int32_t mask_id,
+                                    float scale, int32_t* tok, float* conf, float* logits, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  dinfer_ctx* c = nullptr;
+  if (!X || !W || !tok || !conf) return fail(c, DINFER_EINVAL, "NULL operand");
+  if (M < 1 || M > 1024 || V < 8 || V % 8 || K < 64 || K % 64) return fail(c, DINFER_EINVAL, "unsupported shape");
+  OpWs o;
+  if (!op_ws(workspace, workspace_bytes, o)) return fail(c, DINFER_EINVAL, "workspace too small");
+  const int G = num_sms();
+  if ((size_t)G * 1024 * sizeof(SoftmaxState) > o.data_bytes) return fail(c, DINFER_EINVAL, "workspace too small");
+  if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
+  const int BN = bn_for_rows(M);
+  GemmMaps m{};
+  if (!make_map(&m.a[0], W, V, K, 128) || !make_map(&m.b, X, M, K, BN))
+    return fail(c, DINFER_EINVAL, "tensor map encoding failed (alignment?)");
+  GemmArgs ga{};
+  ga.M = M; ga.N = V; ga.K = K; ga.n_tiles = (V + 127) / 128; ga.a_mode = A_SINGLE;
+  ga.status = o.st; ga.state = o.st;
+  DecodeArgs dec{};
+  dec.M = M; dec.batch = 1; dec.L = M; dec.B = M; dec.commit = 0;
+  dec.tok_out = tok; dec.conf_out = conf; dec.state = o.st;
+  dec.partials = reinterpret_cast<SoftmaxState*>(o.data); dec.n_parts = G; dec.ticket = o.tickets;
+  LmArgs la{V, mask_id, scale, logits, dec};
+  CK(launch_lmhead_tc(m, ga, la, BN, reinterpret_cast<cudaStream_t>(stream)));
+  return DINFER_OK;
+}
+
+dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void* v, void* out, int32_t batch,
+                                       int32_t rows_per_seq, int32_t L, int32_t heads, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  dinfer_ctx* c = nullptr;
+  if (!q || !k || !v || !out) return fail(c, DINFER_EINVAL, "NULL operand");
+  if (batch < 1 || rows_per_seq < 1 || L < 1 || heads < 1) return fail(c, DINFER_EINVAL, "unsupported shape");
+  OpWs o;
+  if (!op_ws(workspace, workspace_bytes, o)) return fail(c, DINFER_EINVAL, "workspace too small");
+  if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
+  const AttnPlan ap = plan_attention(batch, rows_per_seq, heads, L);
+  const size_t rows = (size_t)batch * rows_per_seq, d = (size_t)heads * kHd;
+  const size_t need_o = ap.splits > 1 ? ap.splits * rows * d * 4 : 0;
+  const size_t need_ml = ap.splits > 1 ? ap.splits * rows * heads * 2 * 4 : 0;
+  if (need_o + need_ml > o.data_bytes) return fail(c, DINFER_EINVAL, "workspace too small");
+  if ((size_t)batch * ap.q_tiles * heads * 4 > kOpTicketBytes) return fail(c, DINFER_EINVAL, "too many tiles");
+  AttnArgs aa{};
+  aa.q = (const __nv_bfloat16*)q; aa.k = (const __nv_bfloat16*)k; aa.v = (const __nv_bfloat16*)v;
+  aa.o = (__nv_bfloat16*)out;
+  aa.d = (int)d; aa.heads = heads; aa.L = L; aa.rows_per_seq = rows_per_seq;
+  aa.q_tiles = ap.q_tiles; aa.splits = ap.splits; aa.chunks_per_split = ap.cps;
+  aa.scale_log2 = 1.4426950408889634f / sqrtf((float)kHd);
+  aa.part_o = reinterpret_cast<float*>(o.data);
+  aa.part_ml = reinterpret_cast<float*>(o.data + need_o);
+  aa.tickets = o.tickets;
+  dim3 g(batch * ap.q_tiles, heads, ap.splits);
+  attn_bf16_kernel<<<g, kAttnThreads, kAttnSmem, reinterpret_cast<cudaStream_t>(stream)>>>(aa);
+  CK(cudaGetLastError());
+  return DINFER_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,442 @@
+// Weight-streaming tensor-core GEMM for sm_103a:  Y[m, n] = sum_k X[m, k] W[n, k]
+//
+// Operand roles are swapped relative to the usual token-major GEMM: the
+// weight rows are the MMA's M dimension (128 per tile) and the tokens are its
+// N dimension (BN per tile), so a batch-1 block of 64 tokens is one full MMA
+// tile and the weights stream through shared memory exactly once.
+//
+// Structure (one CTA per SM, 192 threads):
+//   warp 0  TMA producer: weight tile [128 x 64] + token tile [BN x 64] per
+//           stage, 128-byte swizzle, completion on the stage's mbarrier;
+//   warp 1  TMEM allocation + single-thread tcgen05.mma issue (4 x K16 per
+//           stage), fp32 accumulators double-buffered in TMEM;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (one TMEM lane per
+//           thread = one output feature), fused output op.
+// Work is split "stream-K": the (tile, k-step) units are divided evenly over
+// the CTAs, so every SM streams the same number of weight bytes whatever the
+// tile count.  A tile shared by several CTAs is reduced by the last CTA to
+// finish it (atomic ticket), summing the fp32 partials in CTA order so that
+// results do not depend on timing.
+#pragma once
+#include "common.cuh"
+
+namespace dinfer {
+
+enum EpiKind : int {
+  EPI_STORE_F32 = 0,   // out_f32[m * ldo + n] = acc
+  EPI_STORE_BF16 = 1,  // out_bf16[m * ldo + n] = bf16(acc)
+  EPI_RESID = 2,       // resid[m * N + n] += acc
+  EPI_QKV = 3,         // q (RoPE) -> q_out; k (RoPE), v -> dual cache slots
+  EPI_SWIGLU = 4,      // tile rows 0-63 gate, 64-127 up -> act = bf16(silu(g) * u)
+};
+
+enum AMode : int {
+  A_SINGLE = 0,  // one weight map, 128-row boxes
+  A_THREE = 1,   // three maps (wq, wk, wv) of a_rows rows each, 128-row boxes
+  A_PAIR = 2,    // two maps (gate, up), 64-row boxes stacked into one tile
+};
+
+struct GemmMaps {
+  CUtensorMap a[3];
+  CUtensorMap b;
+};
+
+struct GemmArgs {
+  int M, N, K;            // tokens, output features, reduction length
+  int m_tiles, n_tiles, k_tiles;
+  int stream_k;           // 1: split (tile, k) units evenly; 0: whole tiles per CTA
+  int a_mode, a_rows;     // see AMode; a_rows = rows per map in A_THREE
+  // epilogue operands
+  float* out_f32;
+  __nv_bfloat16* out_bf16;
+  int ldo;
+  float* resid;
+  __nv_bfloat16* q_out;    // [M, d]
+  __nv_bfloat16* k_cache;  // this layer: [batch, L, d]
+  __nv_bfloat16* v_cache;
+  const float* rope_cos;   // [max_seq, head_dim / 2]
+  const float* rope_sin;
+  int d_model, head_dim;
+  int rows_per_seq;        // rows of one sequence in X (block length or L)
+  int seq_len;             // L (cache stride in positions)
+  int pos_from_state;      // 1: position = block_start + local row; 0: local row
+  const DevState* state;
+  // stream-K fixup
+  float* ws;               // [grid][2][BN * 128] fp32
+  int* tickets;            // [tiles], zero between launches
+  DevState* status;
+};
+
+constexpr int kGemmThreads = 192;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kStageA = 128 * 64 * 2;
+  static constexpr int kStageB = BN * 64 * 2;
+  static constexpr int kStage = kStageA + kStageB;
+  static constexpr int kStages = (BN == 64) ? 8 : (BN == 128 ? 6 : 4);
+  static constexpr int kXchgFloats = 128 * 17;
+  static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStage + kXchgFloats * 4 + 256;
+  static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+};
+
+// ---------------------------------------------------------------------------
+// schedule: contiguous unit ranges per CTA
+// ---------------------------------------------------------------------------
+struct Sched {
+  long long U;  // total units
+  int KT;       // units per tile (k-steps) in stream-K mode, 1 otherwise
+  int G;
+  __device__ __forceinline__ long long start(int c) const { return (U * c) / G; }
+  __device__ __forceinline__ int owner(long long u) const { return (int)(((u + 1) * G - 1) / U); }
+};
+
+template <int BN>
+__device__ __forceinline__ void load_stage(const GemmMaps& maps, const GemmArgs& a, uint8_t* stage, uint64_t* bar,
+                                           int nt, int mt, int k, uint64_t pol_w, uint64_t pol_x) {
+  uint8_t* sa = stage;
+  uint8_t* sb = stage + GemmCfg<BN>::kStageA;
+  const int kx = k * 64;
+  if (a.a_mode == A_PAIR) {
+    tma_load_2d(sa, &maps.a[0], bar, kx, nt * 64, pol_w);
+    tma_load_2d(sa + 64 * 128, &maps.a[1], bar, kx, nt * 64, pol_w);
+  } else if (a.a_mode == A_THREE) {
+    const int per = a.a_rows / 128;
+    tma_load_2d(sa, &maps.a[nt / per], bar, kx, (nt % per) * 128, pol_w);
+  } else {
+    tma_load_2d(sa, &maps.a[0], bar, kx, nt * 128, pol_w);
+  }
+  tma_load_2d(sb, &maps.b, bar, kx, mt * BN, pol_x);
+}
+
+// One 16-column chunk of the finished accumulator for output feature row
+// `row` (0..127 inside the tile) and tokens m0 .. m0+15.
+template <int BN>
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16], int row, int nt, int m0,
+                                               float* xchg) {
+  if (a.q_out != nullptr) {
+    // ---- QKV: RoPE pairs (i, i + 64) sit in rows row and row ^ 64 ----
+    float* mine = xchg + row * 17;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mine[i] = v[i];
+    named_bar_sync(1, 128);
+    const float* part = xchg + (row ^ 64) * 17;
+    const int n = nt * 128 + row;
+    const int d = a.d_model;
+    const int which = n / d;          // 0 q, 1 k, 2 v
+    const int nn = n - which * d;     // feature inside q/k/v
+    const int hd = a.head_dim;
+    const int i = nn % hd;
+    const int half = hd >> 1;
+    const int j = i % half;
+    const int base_pos = a.pos_from_state ? a.state->block_start : 0;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int m = m0 + c;
+      if (m < a.M) {
+        const int bi = m / a.rows_per_seq;
+        const int pos = base_pos + (m - bi * a.rows_per_seq);
+        float o = v[c];
+        if (which < 2) {
+          const float cs = a.rope_cos[pos * half + j];
+          const float sn = a.rope_sin[pos * half + j];
+          const float p = part[c];
+          o = (i < half) ? (v[c] * cs - p * sn) : (v[c] * cs + p * sn);
+        }
+        const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+        if (which == 0) {
+          a.q_out[(size_t)m * d + nn] = ob;
+        } else {
+          const size_t ci = ((size_t)bi * a.seq_len + pos) * d + nn;
+          if (which == 1) a.k_cache[ci] = ob; else a.v_cache[ci] = ob;
+        }
+      }
+    }
+    named_bar_sync(1, 128);
+  } else if (a.a_mode == A_PAIR) {
+    // ---- SwiGLU: gate row r (< 64) pairs with up row r + 64 ----
+    float* mine = xchg + row * 17;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mine[i] = v[i];
+    named_bar_sync(1, 128);
+    if (row < 64) {
+      const float* up = xchg + (row + 64) * 17;
+      const int jf = nt * 64 + row;
+      if (jf < a.N) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int m = m0 + c;
+          if (m < a.M) {
+            const float g = v[c];
+            const float s = g / (1.0f + expf(-g));
+            a.out_bf16[(size_t)m * a.ldo + jf] = __float2bfloat16_rn(s * up[c]);
+          }
+        }
+      }
+    }
+    named_bar_sync(1, 128);
+  } else {
+    const int n = nt * 128 + row;
+    if (n < a.N) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c;
+        if (m < a.M) {
+          if (a.resid) {
+            a.resid[(size_t)m * a.N + n] += v[c];
+          } else if (a.out_bf16) {
+            a.out_bf16[(size_t)m * a.ldo + n] = __float2bfloat16_rn(v[c]);
+          } else {
+            a.out_f32[(size_t)m * a.ldo + n] = v[c];
+          }
+        }
+      }
+    }
+  }
+}
+
+// Segment (tile t, k-steps [kb, ke)) containing unit u of this CTA's range.
+struct SegIter {
+  int stream_k, k_tiles;
+  long long u_end;
+  __device__ __forceinline__ void seg(long long u, int& t, int& kb, int& ke) const {
+    if (stream_k) {
+      t = (int)(u / k_tiles);
+      kb = (int)(u - (long long)t * k_tiles);
+      long long lim = (long long)(t + 1) * k_tiles;
+      if (lim > u_end) lim = u_end;
+      ke = kb + (int)(lim - u);
+    } else {
+      t = (int)u;
+      kb = 0;
+      ke = k_tiles;
+    }
+  }
+  __device__ __forceinline__ long long units(int kb, int ke) const { return stream_k ? (ke - kb) : 1; }
+};
+
+struct Pipe {
+  uint8_t* stages;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* tfull;
+  uint64_t* tempty;
+  uint64_t* drain;
+  volatile int* abort_flag;
+};
+
+// TMA producer loop (one elected thread of warp 0).
+template <int BN>
+__device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArgs& a, const SegIter& si,
+                                             long long u_begin, const Pipe& p, int m_tiles) {
+  using C = GemmCfg<BN>;
+  const uint64_t pol_w = l2_policy_evict_first();
+  const uint64_t pol_x = l2_policy_evict_last();
+  uint32_t it = 0;
+  for (long long u = u_begin; u < si.u_end && !*p.abort_flag;) {
+    int t, kb, ke;
+    si.seg(u, t, kb, ke);
+    const int nt = t / m_tiles, mt = t % m_tiles;
+    bool ok = true;
+    for (int k = kb; k < ke; ++k, ++it) {
+      const int s = it % C::kStages;
+      const uint32_t round = it / C::kStages;
+      if (!mbar_wait(&p.empty[s], (round & 1) ^ 1, p.abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(&p.full[s], C::kStage);
+      load_stage<BN>(maps, a, p.stages + s * C::kStage, &p.full[s], nt, mt, k, pol_w, pol_x);
+    }
+    if (!ok) break;
+    u += si.units(kb, ke);
+  }
+}
+
+// MMA issue loop (one elected thread of warp 1).
+template <int BN>
+__device__ __forceinline__ void run_mma(const SegIter& si, long long u_begin, const Pipe& p, uint32_t tmem_base) {
+  using C = GemmCfg<BN>;
+  constexpr uint32_t idesc = make_idesc_bf16(128, BN);
+  uint32_t it = 0;
+  int j = 0;
+  for (long long u = u_begin; u < si.u_end && !*p.abort_flag; ++j) {
+    int t, kb, ke;
+    si.seg(u, t, kb, ke);
+    const int acc = j & 1;
+    const uint32_t use = j >> 1;
+    if (!mbar_wait(&p.tempty[acc], (use & 1) ^ 1, p.abort_flag)) break;
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + acc * BN;
+    bool ok = true;
+    for (int k = kb; k < ke; ++k, ++it) {
+      const int s = it % C::kStages;
+      if (!mbar_wait(&p.full[s], (it / C::kStages) & 1, p.abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sa = smem_u32(p.stages + s * C::kStage);
+      const uint32_t sb = sa + C::kStageA;
+      const uint64_t ad = make_sw128_desc(sa);
+      const uint64_t bd = make_sw128_desc(sb);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        tc_mma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (k > kb || kk > 0) ? 1u : 0u);
+      }
+      tc_commit(&p.empty[s]);
+    }
+    if (!ok) break;
+    tc_commit(&p.tfull[acc]);
+    u += si.units(kb, ke);
+  }
+  tc_commit(p.drain);
+  mbar_wait(p.drain, 0, p.abort_flag);
+}
+
+// Carve the shared memory of a GEMM CTA and initialise its barriers.
+template <int BN>
+__device__ __forceinline__ Pipe setup_pipe(uint8_t* smem_raw, float*& xchg, uint32_t*& tmem_slot,
+                                           volatile int*& misc) {
+  using C = GemmCfg<BN>;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Pipe p;
+  p.stages = smem;
+  xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xchg + C::kXchgFloats);
+  p.full = bars;
+  p.empty = bars + C::kStages;
+  p.tfull = bars + 2 * C::kStages;
+  p.tempty = p.tfull + 2;
+  p.drain = p.tempty + 2;
+  tmem_slot = reinterpret_cast<uint32_t*>(p.drain + 1);
+  misc = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  p.abort_flag = misc;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&p.full[s], 1);
+      mbar_init(&p.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p.tfull[i], 1);
+      mbar_init(&p.tempty[i], 128);
+    }
+    mbar_init(p.drain, 1);
+    misc[0] = 0;
+    fence_mbar_init();
+  }
+  return p;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  float* xchg;
+  uint32_t* tmem_slot;
+  volatile int* misc;
+  const Pipe p = setup_pipe<BN>(smem_raw, xchg, tmem_slot, misc);
+  volatile int* last_flag = misc + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const GemmArgs& a = args;
+
+  Sched sc;
+  sc.G = gridDim.x;
+  const int tiles = a.m_tiles * a.n_tiles;
+  sc.KT = a.stream_k ? a.k_tiles : 1;
+  sc.U = (long long)tiles * sc.KT;
+  const long long u_begin = sc.start(blockIdx.x);
+  SegIter si{a.stream_k, a.k_tiles, sc.start(blockIdx.x + 1)};
+
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.b);
+    prefetch_tmap(&maps.a[0]);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (elect_one_sync()) run_producer<BN>(maps, a, si, u_begin, p, a.m_tiles);
+  } else if (warp == 1) {
+    if (elect_one_sync()) run_mma<BN>(si, u_begin, p, tmem_base);
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    const int row = q * 32 + lane;          // output feature row inside the tile
+    const int ep_tid = threadIdx.x - 64;    // 0..127
+    int j = 0;
+    for (long long u = u_begin; u < si.u_end; ++j) {
+      int t, kb, ke;
+      si.seg(u, t, kb, ke);
+      u += si.units(kb, ke);
+      const int nt = t / a.m_tiles, mt = t % a.m_tiles;
+      const int acc = j & 1;
+      const uint32_t use = j >> 1;
+      if (!mbar_wait(&p.tfull[acc], use & 1, p.abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const bool whole = (kb == 0 && ke == a.k_tiles);
+      if (whole) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+          tmem_ld16(tbase + c * 16, v);
+          epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
+        }
+        tc_fence_before();
+        mbar_arrive(&p.tempty[acc]);
+      } else {
+        const int which = (j == 0) ? 0 : 1;
+        float* slot = a.ws + ((size_t)blockIdx.x * 2 + which) * (BN * 128);
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+          tmem_ld16(tbase + c * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) slot[(c * 16 + i) * 128 + row] = v[i];
+        }
+        tc_fence_before();
+        mbar_arrive(&p.tempty[acc]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        const long long tu0 = (long long)t * a.k_tiles;
+        const int c_first = sc.owner(tu0);
+        const int c_last = sc.owner(tu0 + a.k_tiles - 1);
+        if (ep_tid == 0) {
+          const int prev = atomicAdd(&a.tickets[t], 1);
+          const int is_last = (prev == c_last - c_first);
+          if (is_last) a.tickets[t] = 0;
+          *last_flag = is_last;
+        }
+        named_bar_sync(1, 128);
+        if (*last_flag) {
+          __threadfence();
+#pragma unroll 1
+          for (int c = 0; c < BN / 16; ++c) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            for (int cc = c_first; cc <= c_last; ++cc) {
+              const int first_tile = (int)(sc.start(cc) / a.k_tiles);
+              const int w = (t == first_tile) ? 0 : 1;
+              const float* sl = a.ws + ((size_t)cc * 2 + w) * (BN * 128);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * 128 + row);
+            }
+            epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*p.abort_flag && threadIdx.x == 0) set_status(a.status, ST_WAIT_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace dinfer

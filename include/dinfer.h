@@ -1,0 +1,145 @@
+/*
+ * dinfer.h -- C-ABI of the GB300 (sm_103a) block-wise diffusion-LLM decoder.
+ *
+ * What it computes (dInfer: An Efficient Inference Framework for Diffusion
+ * Language Models -- abstract: model, diffusion iteration manager, decoding
+ * strategy and KV-cache manager; dInfer README, "Step 3: Use the model in
+ * dInfer": BlockWiseDiffusionLLM(model, ThresholdParallelDecoder(0,
+ * threshold, mask_id, eos_id), BlockIteratorFactory(True),
+ * cache_factory=KVCacheFactory('dual')).generate(ids, gen_length,
+ * block_length)):
+ *
+ *   x = prompt | mask_id * gen_length.  The generated part is decoded
+ *   block_length positions at a time, left to right.  At a block boundary
+ *   the model runs over the whole sequence and the per-layer keys/values of
+ *   every position are stored (the dual cache: prefix and suffix); that
+ *   forward's block rows are decoded as iteration 1.  Then, while the block
+ *   still has masked positions, a denoising iteration recomputes only the
+ *   block's rows, which attend bidirectionally over the cached prefix, the
+ *   block's fresh keys/values and the cached suffix.  Each iteration the LM
+ *   head gives, per block position, the top-1 token and its softmax
+ *   probability (confidence); every masked position whose confidence exceeds
+ *   the threshold is committed, or, if none does, the single most confident
+ *   one (ties: lowest vocabulary index, lowest position).  The mask token's
+ *   own logit is excluded from argmax and softmax.  eos_id is not used.
+ *
+ * Conventions
+ *   - All calls are asynchronous on the context's stream unless stated.
+ *   - The library owns the KV cache, workspaces and CUDA graphs; the caller
+ *     owns weights, ids, masks and outputs.  Weights are borrowed: they must
+ *     stay valid and unchanged until dinfer_destroy.
+ *   - Errors are returned as dinfer_status; nothing is thrown across the
+ *     ABI.  dinfer_last_error() describes the last failure of a context.
+ *   - A context must be used by one host thread at a time.
+ */
+#ifndef DINFER_H
+#define DINFER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dinfer_ctx dinfer_ctx;
+
+typedef enum dinfer_status {
+  DINFER_OK = 0,
+  DINFER_EINVAL = -1,  /* bad argument: null pointer, size out of range, unsupported shape */
+  DINFER_ENOMEM = -2,  /* device allocation failed */
+  DINFER_ECUDA = -3,   /* a CUDA runtime / driver call failed (see dinfer_last_error) */
+  DINFER_EDEVICE = -4, /* the device status word was set: token id out of range, NaN
+                          confidence, iteration overflow or a pipeline wait timeout */
+  DINFER_ESTATE = -5   /* call out of order (dinfer_block_step before dinfer_prefill_cache) */
+} dinfer_status;
+
+enum { DINFER_FP32 = 0, DINFER_BF16 = 1 };
+
+/* Model description.  Dense models: n_experts = top_k = expert_ffn = 0.
+ * bf16 models: head_dim 128, d_model and ffn multiples of 128 and 64, vocab
+ * a multiple of 8.  max_batch / max_seq bound the dual cache and workspaces
+ * allocated by dinfer_create (max_batch <= 64). */
+typedef struct dinfer_model_desc {
+  int32_t n_layers, d_model, n_heads, head_dim, ffn, vocab, mask_id;
+  int32_t n_experts, top_k, expert_ffn;
+  float rms_eps, rope_theta, logit_scale;
+  int32_t dtype; /* DINFER_FP32 or DINFER_BF16: weights, K/V cache and GEMM inputs */
+  int32_t max_batch, max_seq;
+} dinfer_model_desc;
+
+typedef struct dinfer_stats {
+  int32_t n_blocks;
+  int32_t iterations;      /* denoising iterations, refreshes included */
+  int32_t refreshes;
+  float ms_device;         /* device time of the call (CUDA events on the stream) */
+  int32_t* iters_per_block; /* optional caller array [n_blocks] (host), or NULL */
+} dinfer_stats;
+
+/* Number of weight pointers a model takes:
+ *   1 + 9 * n_layers + 2, in this order, each row-major [out, in]:
+ *   embed [V, d];
+ *   per layer: attn_norm [d], wq [d, d], wk [d, d], wv [d, d], wo [d, d],
+ *              ffn_norm [d], w_gate [f, d], w_up [f, d], w_down [d, f]
+ *              (MoE: router [E, d], w13 [E, 2 fe, d] gate rows then up rows,
+ *               w2 [E, d, fe] in place of the last three);
+ *   final_norm [d]; lm_head [V, d].
+ * Element type: bf16 for DINFER_BF16 models, fp32 for DINFER_FP32.
+ * Returns -1 for an invalid description. */
+int32_t dinfer_num_weights(const dinfer_model_desc* desc);
+
+/* Validate the description, borrow the device weight pointers, allocate the
+ * cache and workspaces for max_batch x max_seq, build tensor-memory
+ * descriptors.  stream: a cudaStream_t, or NULL for a library-owned stream.
+ * On failure *out is NULL and dinfer_last_error(NULL) explains why. */
+dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* weights, void* stream,
+                            dinfer_ctx** out);
+
+void dinfer_destroy(dinfer_ctx* ctx);
+
+/* Text of the last error of ctx (or of the last failed dinfer_create of this
+ * thread when ctx is NULL).  Valid until the next call on the context. */
+const char* dinfer_last_error(const dinfer_ctx* ctx);
+
+/* Block boundary (cache refresh): full forward over ids[batch, seq_len]
+ * (device, int32), storing every layer's K/V of all positions in the dual
+ * cache; then decodes the block [block_start, block_start + block_len) and,
+ * if commit != 0, applies one threshold commit to ids / mask (device, uint8,
+ * 1 = masked) in place -- iteration 1 of the block.  committed: optional
+ * device int32[batch] receiving the per-sequence commit count.  Requires
+ * batch <= max_batch, seq_len <= max_seq, batch * block_len <= 1024. */
+dinfer_status dinfer_prefill_cache(dinfer_ctx* ctx, int32_t* ids, uint8_t* mask, int32_t batch, int32_t seq_len,
+                                   int32_t block_start, int32_t block_len, float threshold, int32_t commit,
+                                   int32_t* committed);
+
+/* One cached denoising iteration of the block set by the last
+ * dinfer_prefill_cache: the block rows of ids [batch, seq_len] (device) are
+ * re-run against the dual cache (their fresh K/V overwrite the block slot)
+ * and one threshold commit updates ids / mask in place.  committed:
+ * optional device int32[batch]; 0 for a sequence whose block had no mask. */
+dinfer_status dinfer_block_step(dinfer_ctx* ctx, int32_t* ids, uint8_t* mask, float threshold, int32_t* committed);
+
+/* Whole generation: prompt [batch, prompt_len] int32 -> out [batch,
+ * prompt_len + gen_length] int32 (prompt kept).  prompt and out may be host
+ * or device pointers; host buffers are copied inside the call.  The block
+ * loop and the iteration loop run on the device (one CUDA graph with
+ * conditional nodes); the call synchronises once at the end.  gen_length
+ * must be a multiple of block_length.  stats may be NULL. */
+dinfer_status dinfer_generate(dinfer_ctx* ctx, const int32_t* prompt, int32_t batch, int32_t prompt_len,
+                              int32_t gen_length, int32_t block_length, float threshold, int32_t* out,
+                              dinfer_stats* stats);
+
+/* Test hook: while set, every decode also writes the fp32 logits [rows, V]
+ * (mask token = -inf), tokens [rows] and confidences [rows] of the block
+ * rows to these device buffers (each may be NULL); rows = batch * block_len.
+ * Calls made while any is set run without CUDA graphs. */
+dinfer_status dinfer_set_debug_outputs(dinfer_ctx* ctx, float* logits, int32_t* tok, float* conf);
+
+/* Wait for the context's stream and report the device status word. */
+dinfer_status dinfer_sync(dinfer_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DINFER_H */

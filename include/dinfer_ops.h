@@ -1,0 +1,58 @@
+/*
+ * dinfer_ops.h -- kernel-level entry points of the same library, for parity
+ * tests and per-kernel measurement at full model shapes.  Each runs exactly
+ * one of the kernels that dinfer_block_step / dinfer_prefill_cache launch.
+ *
+ * All pointers are device pointers unless stated; all calls are asynchronous
+ * on `stream` (a cudaStream_t, NULL = legacy default stream).  `workspace`
+ * is caller-owned device memory of `workspace_bytes` bytes that must be
+ * zero-filled once before its first use; the calls leave its counter region
+ * zeroed again.  Calls sharing one workspace must not overlap on the GPU.
+ * Errors: DINFER_EINVAL for bad sizes / NULL pointers / a too-small
+ * workspace, DINFER_ECUDA for a failed launch.
+ */
+#ifndef DINFER_OPS_H
+#define DINFER_OPS_H
+
+#include "dinfer.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Workspace size that covers every op below for M <= 1024 rows, d <= 8192
+ * and up to 64 query tiles x 64 heads of attention. */
+size_t dinfer_op_workspace_bytes(void);
+
+/* Y[m, n] = sum_k X[m, k] W[n, k]  (bf16 inputs, fp32 accumulate and output).
+ * X [M, K] bf16, W [N, K] bf16 (row-major, 16-byte aligned), Y [M, N] fp32.
+ * K % 64 == 0, N % 128 == 0, 1 <= M <= 1 << 20.  The tensor-core GEMM
+ * (tcgen05, TMA, stream-K) used for every projection of the model. */
+dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_t M, int32_t N, int32_t K,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Fused LM head (dInfer decoding strategy: top-1 token and its softmax
+ * probability per position, without materialising the logits):
+ *   l[m, v] = scale * sum_k X[m, k] W[v, k], l[m, mask_id] = -inf,
+ *   tok[m] = argmax_v l[m, v] (lowest index on ties),
+ *   conf[m] = 1 / sum_v exp(l[m, v] - l[m, tok[m]]).
+ * X [M, K] bf16 (M <= 1024), W [V, K] bf16, tok [M] int32, conf [M] fp32;
+ * logits [M, V] fp32 optional (NULL = not written). K % 64 == 0, V % 8 == 0. */
+dinfer_status dinfer_op_lmhead_bf16(const void* X, const void* W, int32_t M, int32_t V, int32_t K, int32_t mask_id,
+                                    float scale, int32_t* tok, float* conf, float* logits, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/* Bidirectional attention of the block rows against the dual cache:
+ *   o[r, h, :] = sum_j softmax_j(q[r, h, :] . k[b, j, h, :] / sqrt(128)) v[b, j, h, :]
+ * over all j < L of sequence b = r / rows_per_seq, no mask.  q, o
+ * [batch * rows_per_seq, heads * 128] bf16; k, v [batch, L, heads * 128] bf16.
+ * Keys are split over CTAs when the grid would be small. */
+dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void* v, void* o, int32_t batch,
+                                       int32_t rows_per_seq, int32_t L, int32_t heads, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DINFER_OPS_H */
