@@ -1,0 +1,458 @@
+"""Benchmark: generated tokens/s of block-wise dual-cache diffusion decoding.
+
+One step = one whole generation (every block: cache refresh + cached
+denoising iterations until the block is committed) of the workload, through
+the library's C-ABI (dinfer_generate).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+N > 1 (torchrun): the batch-1 workload does not shard; every rank runs an
+independent replica and `value` is the tokens of all ranks over the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "generated tokens/s at batch 1 (LLaDA-8B shape)"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            j = json.load(open(p))
+            hbm = j.get("hbm_gbs") or j.get("hbm_GBs")
+            tf = j.get("bf16_tflops")
+            tfs = j.get("bf16_tflops_sustained", tf)
+            if hbm and tf:
+                return float(hbm), float(tf), float(tfs), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (per unit) of the hot path
+# ---------------------------------------------------------------------------
+def iteration_bytes(cfg, b, L, B):
+    """Bytes one cached denoising iteration must move: every weight read once
+    (embedding rows aside) plus the cached K/V of the L - B non-block positions."""
+    d, f, nl, V = cfg.d_model, cfg.ffn, cfg.n_layers, cfg.vocab
+    w = nl * (4 * d * d + 3 * d * f) + V * d
+    kv = b * (L - B) * 2 * d * nl
+    return 2 * (w + kv)
+
+
+def iteration_flops(cfg, b, L, B):
+    d, f, nl, V = cfg.d_model, cfg.ffn, cfg.n_layers, cfg.vocab
+    M = b * B
+    return 2 * M * (nl * (4 * d * d + 3 * d * f) + V * d) + 4 * M * L * d * nl
+
+
+def refresh_flops(cfg, b, L, B):
+    d, f, nl, V = cfg.d_model, cfg.ffn, cfg.n_layers, cfg.vocab
+    M = b * L
+    return 2 * M * nl * (4 * d * d + 3 * d * f) + 4 * b * L * L * d * nl + 2 * b * B * V * d
+
+
+class ClockSampler:
+    def __init__(self, path):
+        self.path = path
+        self.p = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms",
+                                       "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        if self.p:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+            self.f.close()
+
+    def summary(self, gpu_index=0):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+        try:
+            rows = [r.split(",") for r in open(self.path).read().strip().splitlines()]
+            rows = [[c.strip() for c in r] for r in rows if len(r) >= 9 and r[0].strip() == str(gpu_index)]
+            sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+            if sm:
+                out["sm_mhz"] = statistics.median(sm)
+            mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+            if mx:
+                out["sm_max_mhz"] = max(mx)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            seen = set()
+            for r in rows:
+                for i, n in enumerate(names):
+                    if r[5 + i].lower().startswith("active"):
+                        seen.add(n)
+            out["reasons"] = sorted(seen)
+            out["samples"] = len(rows)
+        except Exception:
+            pass
+        return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+def oracle_sample(cfg, run, iters_per_block=None):
+    """Time the oracle on one layer of a refresh, one layer of a cached
+    iteration and the LM head of one block, at the workload's full shapes;
+    extrapolate to the whole generation.  iters_per_block None: assume every
+    block completes at its refresh (an upper bound on the oracle's tokens/s)."""
+    import numpy as np
+    from block_denoising_gb300 import inputs
+    from oracle import dinfer_oracle as O
+
+    b, P, G, B = run.batch, run.prompt_len, run.gen_length, run.block_length
+    L = P + G
+    # The time of the oracle's float64 matmuls does not depend on the values,
+    # so the sample uses same-shape arrays tiled from a small N(0, 0.02) block
+    # instead of regenerating the seeded weights on the host.
+    rng = np.random.default_rng(0)
+    blk = (rng.standard_normal(1 << 16) * 0.02).astype(np.float32)
+
+    def arr(shape):
+        n = int(np.prod(shape))
+        return np.resize(blk, n).reshape(shape)
+
+    one = inputs.shrink(cfg, n_layers=1)
+    shapes = [sh for (_, sh, _) in inputs.weight_specs(one)]
+    W = [np.broadcast_to(arr((1, cfg.d_model)), shapes[0])]  # embedding rows are gathered only
+    for sh, (_, _, init) in zip(shapes[1:-2], inputs.weight_specs(one)[1:-2]):
+        W.append(np.ones(sh, np.float32) if init == "ones" else arr(sh))
+    W += [np.ones(cfg.d_model, np.float32), arr(shapes[-1])]
+    m = O.Model(O.Desc.from_config(one), W)
+    x = np.full((b, L), cfg.mask_id)
+    x[:, :P] = inputs.make_prompt(cfg, b, P).numpy()
+    h_all = O.embed(m, x[0])
+    K = np.zeros((L, cfg.n_heads, cfg.head_dim))
+    V = np.zeros_like(K)
+    t0 = time.perf_counter()
+    O.layer_forward(m, 0, h_all, np.arange(L), K, V)
+    t_layer_refresh = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    hb = O.layer_forward(m, 0, h_all[P:P + B], np.arange(P, P + B), K, V)
+    t_layer_iter = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    lg = O.lm_head_logits(m, hb)
+    O.top1_confidence(lg)
+    t_lm = time.perf_counter() - t0
+    per_refresh = b * (cfg.n_layers * t_layer_refresh) + b * t_lm
+    per_iter = b * (cfg.n_layers * t_layer_iter + t_lm)
+    nblk = G // B
+    if iters_per_block is None:
+        total = nblk * per_refresh
+        note = "each block assumed complete at its refresh (upper bound on oracle tokens/s)"
+    else:
+        total = nblk * per_refresh + (sum(iters_per_block) - nblk) * per_iter
+        note = "with the iteration counts of this run"
+    cores = os.cpu_count()  # numpy's BLAS runs on every host core
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        cores = max([i.get("num_threads", 0) for i in info] + [1])
+    except Exception:
+        pass
+    return {
+        "value": b * G / total,
+        "unit": UNIT,
+        "cores": cores,
+        "kind": "oracle",
+        "sample": (f"float64 numpy oracle: 1 of {cfg.n_layers} layers of a refresh over L={L} rows "
+                   f"({t_layer_refresh:.2f} s), 1 layer of a cached iteration over B={B} rows "
+                   f"({t_layer_iter:.3f} s), LM head of the block ({t_lm:.2f} s), batch {b}; "
+                   f"extrapolated to {nblk} blocks, {note}"),
+        "us_per_refresh": per_refresh * 1e6,
+        "us_per_iteration": per_iter * 1e6,
+    }
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    from block_denoising_gb300 import inputs
+    cfg, run, desc = inputs.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    vals = []
+    for i in range(args.warmup + args.steps):
+        s = oracle_sample(cfg, run)
+        if i >= args.warmup:
+            vals.append(s)
+    v = statistics.median([s["value"] for s in vals])
+    ms = 1000.0 * run.batch * run.gen_length / v
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "description": desc, "global_batch": run.batch,
+                   "seq_len": run.seq_len},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": vals[-1]["cores"], "kind": "oracle",
+                         "sample": vals[-1]["sample"]},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from block_denoising_gb300 import build, dinfer, inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    cfg, run, desc = inputs.WORKLOADS[args.workload]
+    b, P, G, B = run.batch, run.prompt_len, run.gen_length, run.block_length
+    L = P + G
+    W = inputs.make_weights(cfg, 0, device="cuda")
+    stream = torch.cuda.Stream()
+    dec = dinfer.Decoder(cfg, W, max_batch=b, max_seq=L, stream=stream)
+    prompt_d = inputs.make_prompt(cfg, b, P, device="cuda")
+    out_d = torch.empty((b, L), dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    # warm-up (also captures and instantiates the graphs)
+    for _ in range(args.warmup):
+        dec.generate(prompt_d, G, B, run.threshold, out=out_d)
+    # ---- device-timed region: inputs resident in HBM -------------------------
+    # the 15 GB of weights streamed every iteration exceed the 129 MB L2, so no
+    # flush is needed between steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    iters = []
+    with clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            _, st = dec.generate(prompt_d, G, B, run.threshold, out=out_d)
+            iters.append(st["iters_per_block"])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    t_dev = ev0.elapsed_time(ev1) / 1000.0
+    # ---- end to end: host prompt in, host ids out, through the public API ----
+    prompt_h = inputs.make_prompt(cfg, b, P).pin_memory()
+    out_h = torch.empty((b, L), dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        dec.generate(prompt_h, G, B, run.threshold, out=out_h)
+    t_e2e = time.perf_counter() - t0
+    # ---- the cached iteration alone (spec roofline) and the refresh ----
+    ids = out_d.clone()
+    ids[:, P:] = cfg.mask_id
+    mask = torch.zeros((b, L), dtype=torch.uint8, device="cuda")
+    mask[:, P:] = 1
+    with torch.cuda.stream(stream):
+        dec.prefill_cache(ids, mask, P, B, run.threshold, commit=False)
+        n_it = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ids2, mask2 = ids.clone(), mask.clone()
+        dec.block_step(ids2, mask2, 2.0)  # threshold above 1: one commit per step, block never empties
+        e0.record(stream)
+        for _ in range(n_it):
+            dec.block_step(ids2, mask2, 2.0)
+        e1.record(stream)
+        stream.synchronize()
+        us_iter = 1000.0 * e0.elapsed_time(e1) / n_it
+        e0.record(stream)
+        for _ in range(3):
+            dec.prefill_cache(ids, mask, P, B, run.threshold, commit=False)
+        e1.record(stream)
+        stream.synchronize()
+        us_refresh = 1000.0 * e0.elapsed_time(e1) / 3
+    dec.sync()
+
+    # ---- dominant kernel: the refresh GEMMs (tensor-bound) --------------------
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+    dom = gemm_roofline(cfg, run, dinfer, stream, tf_sus)
+
+    # max over ranks
+    t = torch.tensor([t_dev, t_e2e], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_dev, t_e2e = float(t[0]), float(t[1])
+    tokens = world * args.steps * b * G
+    value = tokens / t_dev
+    e2e = tokens / t_e2e
+    if rank == 0:
+        ipb = iters[-1]
+        bytes_it = iteration_bytes(cfg, b, L, B)
+        ach_gbs = bytes_it / (us_iter * 1e-6) / 1e9
+        it_roof_us = max(bytes_it / (hbm * 1e9), iteration_flops(cfg, b, L, B) / (tf_burst * 1e12)) * 1e6
+        it_roof_us_8t = max(bytes_it / 8e12, iteration_flops(cfg, b, L, B) / (tf_burst * 1e12)) * 1e6
+        rf_roof_us = refresh_flops(cfg, b, L, B) / (tf_burst * 1e12) * 1e6
+        n_launch = launches_per_generation(cfg, ipb)
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = oracle_sample(cfg, run, ipb)
+            cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * t_dev / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "description": desc, "global_batch": b * world,
+                       "seq_len": L, "prompt_len": P, "gen_length": G, "block_length": B,
+                       "threshold": run.threshold, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (weights 15 GB streamed per iteration); no flush"},
+            "iterations_per_block": ipb,
+            "us_per_iteration": us_iter,
+            "us_per_refresh": us_refresh,
+            "iteration_roofline": {"bound": "hbm", "bytes": bytes_it, "achieved_gbs": ach_gbs,
+                                   "roofline_us_measured_peak": it_roof_us, "roofline_us_8tbs": it_roof_us_8t,
+                                   "frac_of_measured": it_roof_us / us_iter, "frac_of_8tbs": it_roof_us_8t / us_iter,
+                                   "peak_source": peak_src},
+            "refresh_roofline": {"bound": "tensor", "flops": refresh_flops(cfg, b, L, B), "roofline_us": rf_roof_us,
+                                 "frac": rf_roof_us / us_refresh},
+            "tokens_per_s_roofline": b * G / ((G // B) * rf_roof_us * 1e-6 + (sum(ipb) - G // B) * it_roof_us * 1e-6),
+            "roofline": dom,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": b * P * 4, "d2h_bytes_per_step": b * L * 4},
+            "gpu_launches": n_launch * args.steps,
+            "clocks": clocks.summary(local),
+        }
+        print(json.dumps(line), flush=True)
+    dec.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def launches_per_generation(cfg, ipb):
+    """Kernels of ours launched by one generation: per forward embed + 7 per
+    layer (2 norms, 4 GEMMs, attention) + final norm + LM head; per block
+    begin/inner-condition/advance; one init."""
+    per_fwd = 1 + 7 * cfg.n_layers + 2
+    return 1 + len(ipb) * 3 + sum(ipb) * per_fwd
+
+
+def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
+    """The refresh's largest GEMM (gate/up: M = b L tokens, N = 2 ffn, K = d)
+    at the launch configuration the step uses, timed with CUDA events."""
+    import torch
+    from block_denoising_gb300 import inputs
+    M = run.batch * run.seq_len
+    N, K = 2 * cfg.ffn, cfg.d_model
+    X = inputs.normal_tensor(1, (M, K), 1.0, 9, device="cuda")
+    Wt = inputs.normal_tensor(2, (N, K), 0.02, 9, device="cuda")
+    Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = dinfer.OpWorkspace()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dinfer.op_gemm_bf16(X, Wt, ws, Y)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 10
+        e0.record(stream)
+        for _ in range(n):
+            dinfer.op_gemm_bf16(X, Wt, ws, Y)
+        e1.record(stream)
+        stream.synchronize()
+    dt = e0.elapsed_time(e1) / 1000.0 / n
+    flops = 2.0 * M * N * K
+    ach = flops / dt / 1e12
+    return {"bound": "tensor", "kernel": "gemm_tc_kernel<256> (refresh gate/up GEMM, fp32 out)",
+            "achieved": ach, "peak": peak_tflops, "unit": "TFLOP/s", "frac": ach / peak_tflops,
+            "traffic": None, "us_per_launch": dt * 1e6, "flops_per_launch": flops}
+
+
+def run_profile(args):
+    """One region for ncu (--profile-from-start off): a cached iteration, a
+    refresh, or one GEMM launch, after a warm-up outside the region."""
+    import torch
+    from block_denoising_gb300 import build, dinfer, inputs
+    build.build()
+    cfg, run, _ = inputs.WORKLOADS[args.workload]
+    b, P, G, B = run.batch, run.prompt_len, run.gen_length, run.block_length
+    L = P + G
+    if args.profile == "gemm":
+        M, N, K = args.gemm
+        X = inputs.normal_tensor(1, (M, K), 1.0, 9, device="cuda")
+        Wt = inputs.normal_tensor(2, (N, K), 0.02, 9, device="cuda")
+        ws = dinfer.OpWorkspace()
+        Y = dinfer.op_gemm_bf16(X, Wt, ws)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        dinfer.op_gemm_bf16(X, Wt, ws, Y)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        return
+    W = inputs.make_weights(cfg, 0, device="cuda")
+    dec = dinfer.Decoder(cfg, W, max_batch=b, max_seq=L)
+    ids = torch.full((b, L), cfg.mask_id, dtype=torch.int32, device="cuda")
+    ids[:, :P] = inputs.make_prompt(cfg, b, P, device="cuda")
+    mask = torch.zeros((b, L), dtype=torch.uint8, device="cuda")
+    mask[:, P:] = 1
+    dec.prefill_cache(ids, mask, P, B, run.threshold, commit=False)
+    dec.block_step(ids, mask, 2.0)
+    dec.sync()
+    torch.cuda.profiler.start()
+    if args.profile == "iteration":
+        dec.block_step(ids, mask, 2.0)
+    else:
+        dec.prefill_cache(ids, mask, P, B, run.threshold, commit=False)
+    dec.sync()
+    torch.cuda.profiler.stop()
+    dec.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llada8b_b1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["iteration", "refresh", "gemm"], default=None)
+    ap.add_argument("--gemm", type=int, nargs=3, default=[64, 24576, 4096], metavar=("M", "N", "K"))
+    args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

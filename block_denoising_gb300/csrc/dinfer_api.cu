@@ -10,6 +10,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -110,7 +111,10 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
   a.m_tiles = (a.M + BN - 1) / BN;
   a.k_tiles = a.K / 64;
   a.stream_k = 1;
-  const int grid = num_sms();
+  // every CTA must own at least one (tile, k-step) unit: the fixup counts
+  // the CTAs between a tile's first and last contributor
+  const long long units = (long long)a.m_tiles * a.n_tiles * a.k_tiles;
+  const int grid = (int)std::min<long long>(num_sms(), units);
   switch (BN) {
     case 64:
       gemm_tc_kernel<64><<<grid, kGemmThreads, GemmCfg<64>::kSmem, s>>>(maps, a);
@@ -125,11 +129,18 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_lmhead_tc(const GemmMaps& maps, GemmArgs ga, const LmArgs& la, int BN, cudaStream_t s) {
+int lmhead_grid(int M, int V) {
+  const int BN = bn_for_rows(M);
+  const long long tiles = (long long)((M + BN - 1) / BN) * ((V + 127) / 128);
+  return (int)std::min<long long>(num_sms(), tiles);
+}
+
+cudaError_t launch_lmhead_tc(const GemmMaps& maps, GemmArgs ga, LmArgs la, int BN, cudaStream_t s) {
   ga.m_tiles = (ga.M + BN - 1) / BN;
   ga.k_tiles = ga.K / 64;
   ga.stream_k = 0;
-  const int grid = num_sms();
+  const int grid = lmhead_grid(ga.M, ga.N);
+  la.dec.n_parts = grid;
   switch (BN) {
     case 64:
       lmhead_tc_kernel<64><<<grid, kGemmThreads, LmCfg<64>::kSmem, s>>>(maps, ga, la);
@@ -486,7 +497,6 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
     GemmArgs ga{};
     ga.M = brows; ga.N = d.vocab; ga.K = D; ga.n_tiles = (d.vocab + 127) / 128; ga.a_mode = A_SINGLE;
     ga.status = c->st; ga.state = c->st;
-    dec.n_parts = num_sms();
     LmArgs la{d.vocab, d.mask_id, d.logit_scale, c->dbg_logits, dec};
     CK(launch_lmhead_tc(m, ga, la, BNl, s));
   } else {
@@ -703,12 +713,7 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
     if (s_ != DINFER_OK) return bail(s_);                \
   } while (0)
 
-  if (stream) {
-    c->stream = reinterpret_cast<cudaStream_t>(stream);
-  } else {
-    CKC(cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking));
-    c->own_stream = true;
-  }
+  c->stream = reinterpret_cast<cudaStream_t>(stream);  // NULL: the legacy default stream
   CKC(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
   CKC(cudaStreamCreateWithFlags(&c->cap_stream2, cudaStreamNonBlocking));
   CKC(cudaEventCreate(&c->ev0));
@@ -1037,7 +1042,7 @@ dinfer_status dinfer_op_lmhead_bf16(const void* X, const void* W, int32_t M, int
   DecodeArgs dec{};
   dec.M = M; dec.batch = 1; dec.L = M; dec.B = M; dec.commit = 0;
   dec.tok_out = tok; dec.conf_out = conf; dec.state = o.st;
-  dec.partials = reinterpret_cast<SoftmaxState*>(o.data); dec.n_parts = G; dec.ticket = o.tickets;
+  dec.partials = reinterpret_cast<SoftmaxState*>(o.data); dec.ticket = o.tickets;
   LmArgs la{V, mask_id, scale, logits, dec};
   CK(launch_lmhead_tc(m, ga, la, BN, reinterpret_cast<cudaStream_t>(stream)));
   return DINFER_OK;

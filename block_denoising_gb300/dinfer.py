@@ -111,10 +111,10 @@ class Decoder:
             raise ValueError(f"model takes {n} weights, got {len(weights)}")
         self.weights: List[torch.Tensor] = [w.contiguous() for w in weights]
         arr = (ctypes.c_void_p * n)(*[w.data_ptr() for w in self.weights])
-        self.stream = stream
+        # calls are ordered on this stream (default: torch's current stream)
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
         h = ctypes.c_void_p()
-        st = L.dinfer_create(ctypes.byref(self.desc), arr, None if stream is None else ctypes.c_void_p(stream.cuda_stream),
-                             ctypes.byref(h))
+        st = L.dinfer_create(ctypes.byref(self.desc), arr, ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h))
         _check(st, None)
         self.h = h
 

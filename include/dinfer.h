@@ -90,7 +90,8 @@ int32_t dinfer_num_weights(const dinfer_model_desc* desc);
 
 /* Validate the description, borrow the device weight pointers, allocate the
  * cache and workspaces for max_batch x max_seq, build tensor-memory
- * descriptors.  stream: a cudaStream_t, or NULL for a library-owned stream.
+ * descriptors.  stream: the cudaStream_t every call of the context is
+ * ordered on (NULL = the legacy default stream).
  * On failure *out is NULL and dinfer_last_error(NULL) explains why. */
 dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* weights, void* stream,
                             dinfer_ctx** out);

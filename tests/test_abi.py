@@ -78,3 +78,23 @@ def test_calls_on_null_context_are_rejected(L):
     assert L.dinfer_block_step(None, None, None, 0.9, None) == dinfer.EINVAL
     assert L.dinfer_generate(None, None, 1, 1, 1, 1, 0.9, None, None) == dinfer.EINVAL
     assert L.dinfer_op_gemm_bf16(None, None, None, 1, 128, 64, None, 0, None) == dinfer.EINVAL
+
+
+def _start(U, G, c):
+    return (U * c) // G
+
+
+def _owner(U, G, u):
+    return ((u + 1) * G - 1) // U
+
+
+@pytest.mark.parametrize("U,G", [(4, 4), (7, 3), (6144, 152), (64 * 96, 152), (999, 152), (152, 152), (153, 152)])
+def test_stream_k_schedule_arithmetic(U, G):
+    # the GEMM launches min(SMs, units) CTAs; CTA c owns units [U c / G, U (c+1) / G)
+    G = min(G, U)
+    starts = [_start(U, G, c) for c in range(G + 1)]
+    assert starts[0] == 0 and starts[-1] == U
+    assert all(starts[c + 1] > starts[c] for c in range(G))  # no empty CTA
+    for c in range(G):
+        assert _owner(U, G, starts[c]) == c
+        assert _owner(U, G, starts[c + 1] - 1) == c

@@ -2,11 +2,12 @@
 
 Every GPU iteration starts from the oracle's (ids, mask) state -- the
 trajectory teacher-forced from the oracle -- and is compared on logits,
-tokens, confidences and the commit set.  Decisions the tolerance cannot
-resolve are flagged and counted, never silently accepted:
-  * top-2 logit gap below the token tolerance,
-  * confidence within the confidence tolerance of the threshold,
-  * the fallback's top-2 confidences (masked positions) within that tolerance.
+tokens, confidences and the commit set.  A decision is flagged (counted and
+reported, allowed to differ) only if a logit error within the tolerance
+delta could flip it: a top-2 logit gap below 2 delta (at least 1e-2), a
+threshold inside the confidence interval that delta allows (or within 1e-2
+of the confidence), or a fallback choice among positions whose intervals
+overlap.  Every unflagged decision must match exactly.
 """
 import numpy as np
 import pytest
@@ -18,13 +19,22 @@ from oracle import dinfer_oracle as O
 pytestmark = pytest.mark.gpu
 dev = torch.device("cuda:0")
 
-# bf16 tolerances, derived from the bf16 contract (see test_bf16_noise_floor_*
-# in test_tolerances.py): two correct fp32-accumulating implementations of the
-# same bf16 rounding points differ by rare rounding flips that cascade through
-# norm and attention; at d_model 512 the measured floor is ~0.02 mean / ~0.15
-# max logit difference.
-BF16_SMALL = dict(logit_max=0.5, logit_mean=0.06, conf=3e-2, gap=0.5)
-FP32 = dict(logit_max=1e-4, logit_mean=1e-5, conf=1e-2, gap=1e-2)
+# Tolerances.  fp32: the stated ones (logits 1e-4, confidence 1e-2).  bf16:
+# the logit bound delta is derived from the bf16 contract itself -- two
+# correct fp32-accumulating implementations of the same bf16 rounding points
+# differ by rare rounding flips that cascade through norm and attention; the
+# floor is measured on the CPU in tests/test_tolerances.py and delta is set to
+# about twice it.  Flags then follow from delta exactly (see flags_for).
+FP32 = dict(delta=1e-4, logit_mean=1e-5)
+BF16_SMALL = dict(delta=0.6, logit_mean=0.08)
+NS_GAP, NS_CONF = 1e-2, 1e-2  # flag widths stated for the method's parity check
+
+
+def conf_interval(conf, delta):
+    """Confidences reachable when the top logit moves by +-delta and all others by -+delta."""
+    c = np.clip(conf, 1e-300, 1.0)
+    r = np.maximum(1.0 / c - 1.0, 0.0)
+    return 1.0 / (1.0 + r * np.exp(2 * delta)), 1.0 / (1.0 + r * np.exp(-2 * delta))
 
 
 @pytest.fixture(scope="module")
@@ -35,20 +45,26 @@ def D():
 
 
 def flags_for(rec, tau, tol, B, s0):
-    """Positions (per sequence, per block slot) whose decision is within tolerance of a tie."""
+    """Block positions whose decision a logit error of at most delta could flip.
+
+    token: top-2 logit gap < max(2 delta, 1e-2); threshold: tau inside the
+    confidence interval (or |conf - tau| < 1e-2); fallback (no confidence
+    above tau): every masked position whose interval reaches the lower end of
+    the best one's.
+    """
+    d = tol["delta"]
     lg = rec.logits
     b = lg.shape[0]
     fl = np.zeros((b, B), dtype=bool)
     for i in range(b):
         srt = np.sort(lg[i], axis=-1)
-        fl[i] |= (srt[:, -1] - srt[:, -2]) < tol["gap"]
-        fl[i] |= np.abs(rec.conf[i] - tau) < tol["conf"]
+        fl[i] |= (srt[:, -1] - srt[:, -2]) < max(2 * d, NS_GAP)
+        lo, hi = conf_interval(rec.conf[i], d)
+        fl[i] |= ((lo <= tau) & (tau < hi)) | (np.abs(rec.conf[i] - tau) < NS_CONF)
         masked = rec.mask_before[i, s0:s0 + B]
-        c = np.where(masked, rec.conf[i], -np.inf)
-        if masked.any() and not (c > tau).any():
-            top = np.sort(c)[::-1]
-            if len(top) > 1 and top[0] - top[1] < tol["conf"]:
-                fl[i] |= masked & (c > top[0] - tol["conf"])
+        if masked.any() and not (hi[masked] > tau).any():
+            best = int(np.argmax(np.where(masked, rec.conf[i], -np.inf)))
+            fl[i] |= masked & (hi >= lo[best] - NS_CONF)
     return fl
 
 
@@ -63,7 +79,7 @@ def teacher_forced(D, cfg, W, prompt, G, B, tau, tol, max_blocks=None):
     tk = torch.empty(b * B, dtype=torch.int32, device=dev)
     cf = torch.empty(b * B, dtype=torch.float32, device=dev)
     dec.set_debug_outputs(lg, tk, cf)
-    out = dict(max_err=0.0, sum_err=0.0, n=0, conf_err=0.0, tok_mismatch=0, commit_mismatch=0, flagged=0,
+    out = dict(max_err=0.0, sum_err=0.0, n=0, conf_err=0.0, conf_outside=0, tok_mismatch=0, commit_mismatch=0, flagged=0,
                unflagged_mismatch=0, iterations=len(trace))
     for rec in trace:
         s0 = P + rec.block * B
@@ -83,6 +99,8 @@ def teacher_forced(D, cfg, W, prompt, G, B, tau, tol, max_blocks=None):
         out["n"] += e.size
         g_conf = cf.cpu().numpy().reshape(b, B)
         out["conf_err"] = max(out["conf_err"], float(np.abs(g_conf - rec.conf).max()))
+        lo, hi = conf_interval(rec.conf, tol["delta"])
+        out["conf_outside"] += int(((g_conf < lo - 1e-6) | (g_conf > hi + 1e-6)).sum())
         g_tok = tk.cpu().numpy().reshape(b, B)
         g_mask = mask.cpu().numpy().astype(bool)
         g_commit = rec.mask_before[:, s0:s0 + B] & ~g_mask[:, s0:s0 + B]
@@ -125,8 +143,9 @@ def test_tiny_fp32_teacher_forced(D, tiny):
     cfg, run, W, prompt = tiny
     st, _, _ = teacher_forced(D, cfg, W, prompt.numpy(), run.gen_length, run.block_length, run.threshold, FP32)
     print(st)
-    assert st["max_err"] < FP32["logit_max"]
-    assert st["conf_err"] < FP32["conf"]
+    assert st["max_err"] < FP32["delta"]
+    assert st["mean_err"] < FP32["logit_mean"]
+    assert st["conf_err"] < NS_CONF and st["conf_outside"] == 0
     assert st["unflagged_mismatch"] == 0
 
 
@@ -176,9 +195,9 @@ def test_small_bf16_teacher_forced(D, batch, P, G, B, tau):
     prompt = inputs.make_prompt(SMALL_BF16, batch, P).numpy()
     st, _, _ = teacher_forced(D, SMALL_BF16, W, prompt, G, B, tau, BF16_SMALL)
     print(st)
-    assert st["max_err"] < BF16_SMALL["logit_max"]
+    assert st["max_err"] < BF16_SMALL["delta"]
     assert st["mean_err"] < BF16_SMALL["logit_mean"]
-    assert st["conf_err"] < BF16_SMALL["conf"] or st["flagged"] > 0
+    assert st["conf_outside"] == 0
     assert st["unflagged_mismatch"] == 0
 
 
@@ -220,13 +239,14 @@ def test_cached_step_on_unchanged_state_reproduces_refresh(D):
     lg = torch.empty((B, SMALL_BF16.vocab), dtype=torch.float32, device=dev)
     dec.set_debug_outputs(logits=lg)
     dec.prefill_cache(ids, mask, P, B, 0.9, commit=False)
+    dec.sync()
     a = lg.clone()
     dec.block_step(ids, mask, 0.9)
     dec.sync()
     fin = torch.isfinite(a)
     assert torch.equal(fin, torch.isfinite(lg))
     # same arithmetic except the token tile of the GEMMs (rows L vs B): rounding only
-    assert torch.max(torch.abs(a[fin] - lg[fin])).item() < BF16_SMALL["logit_max"]
+    assert torch.max(torch.abs(a[fin] - lg[fin])).item() < BF16_SMALL["delta"]
     dec.close()
 
 
