@@ -11,9 +11,14 @@
 // 16 rows; K/V chunks of 64 keys double-buffered with cp.async; S = Q K^T and
 // O = P V on mma.sync m16n8k16 (bf16 in, fp32 accumulate), online softmax in
 // the log2 domain, P rounded to bf16 for the second product.  When the keys
-// are split over several CTAs, each writes an unnormalised partial and the
-// last CTA of the (sequence, head, query tile) merges them in split order.
+// are split over several CTAs (small grids: a batch-1 block), the splits of
+// one (sequence, head, query tile) form a thread-block cluster; each CTA
+// leaves its unnormalised partial in its own shared memory and, after a
+// cluster barrier, merges a slice of the rows by reading all partials over
+// distributed shared memory, in split order.
 #pragma once
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace dinfer {
@@ -26,13 +31,11 @@ struct AttnArgs {
   int d, heads, L;
   int rows_per_seq;         // query rows per sequence
   int q_tiles;              // query tiles of 64 per sequence
-  int splits, chunks_per_split;
+  int splits, chunks_per_split;  // splits > 1: launched with cluster dims (1, 1, splits)
   float scale_log2;         // log2(e) / sqrt(hd)
-  float* part_o;            // [splits][Mq][d]
-  float* part_ml;           // [splits][Mq][heads][2]
-  int* tickets;             // [batch * q_tiles * heads]
 };
 
+constexpr int kMaxAttnSplits = 8;  // portable cluster size
 constexpr int kAttnThreads = 128;
 constexpr int kHd = 128;
 constexpr int kKeyChunk = 64;
@@ -94,8 +97,6 @@ __global__ void __launch_bounds__(kAttnThreads)
   const uint32_t s_q = smem_u32(sm);
   const uint32_t s_k[2] = {s_q + kAttnTileBytes, s_q + 3 * kAttnTileBytes};
   const uint32_t s_v[2] = {s_q + 2 * kAttnTileBytes, s_q + 4 * kAttnTileBytes};
-  __shared__ int last_sh;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int qt = blockIdx.x % a.q_tiles;
@@ -250,62 +251,62 @@ __global__ void __launch_bounds__(kAttnThreads)
     }
     return;
   }
-  // ---- split keys: write the partial, last CTA merges ----
-  const size_t Mq_total = (size_t)gridDim.x / a.q_tiles * a.rows_per_seq;
+  // ---- split keys: partials stay in shared memory, merged across the cluster ----
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  float* po = reinterpret_cast<float*>(sm + kAttnTileBytes);          // [64][128] fp32, over the K/V buffers
+  float* pml = po + 64 * kHd;                                         // [64][2]
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = h ? r_hi : r_lo;
-    if (r < q_valid) {
-      const size_t gr = qrow_base + r;
-      float* po = a.part_o + ((size_t)split * Mq_total + gr) * a.d + head * kHd;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int col = i * 8 + 2 * t4;
-        *reinterpret_cast<float2*>(po + col) = make_float2(oacc[i][2 * h], oacc[i][2 * h + 1]);
-      }
-      if (t4 == 0) {
-        float* pm = a.part_ml + (((size_t)split * Mq_total + gr) * a.heads + head) * 2;
-        pm[0] = m_r[h];
-        pm[1] = l_r[h];
-      }
+    for (int i = 0; i < 16; ++i) {
+      const int col = i * 8 + 2 * t4;
+      *reinterpret_cast<float2*>(po + r * kHd + col) = make_float2(oacc[i][2 * h], oacc[i][2 * h + 1]);
+    }
+    if (t4 == 0) {
+      pml[r * 2] = m_r[h];
+      pml[r * 2 + 1] = l_r[h];
     }
   }
-  __threadfence();
-  __syncthreads();
-  const int tk = (bi * a.q_tiles + qt) * a.heads + head;
-  if (threadIdx.x == 0) {
-    const int prev = atomicAdd(&a.tickets[tk], 1);
-    last_sh = (prev == a.splits - 1);
-    if (last_sh) a.tickets[tk] = 0;
-  }
-  __syncthreads();
-  if (!last_sh) return;
-  __threadfence();
-  // merge: each thread takes (row, 4 columns) work items
-  for (int idx = threadIdx.x; idx < q_valid * (kHd / 4); idx += kAttnThreads) {
-    const int r = idx / (kHd / 4), c4 = (idx % (kHd / 4)) * 4;
-    const size_t gr = qrow_base + r;
+  cluster.sync();
+  const int rank = (int)cluster.block_rank();
+  const int per = (64 + a.splits - 1) / a.splits;
+  const int r0 = rank * per, r1 = min(min(64, r0 + per), q_valid);
+  for (int idx = threadIdx.x; idx < (r1 - r0) * (kHd / 4); idx += kAttnThreads) {
+    const int r = r0 + idx / (kHd / 4), c4 = (idx % (kHd / 4)) * 4;
+    float ms[kMaxAttnSplits], ls[kMaxAttnSplits];
+    float4 os[kMaxAttnSplits];
     float mmax = -INFINITY;
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float* pm = a.part_ml + (((size_t)sp * Mq_total + gr) * a.heads + head) * 2;
-      mmax = fmaxf(mmax, __ldcg(pm));
+#pragma unroll
+    for (int sp = 0; sp < kMaxAttnSplits; ++sp) {
+      if (sp < a.splits) {
+        const float* rpml = cluster.map_shared_rank(pml, sp);
+        const float* rpo = cluster.map_shared_rank(po, sp);
+        ms[sp] = rpml[r * 2];
+        ls[sp] = rpml[r * 2 + 1];
+        os[sp] = *reinterpret_cast<const float4*>(rpo + r * kHd + c4);
+        mmax = fmaxf(mmax, ms[sp]);
+      }
     }
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, lsum = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float* pm = a.part_ml + (((size_t)sp * Mq_total + gr) * a.heads + head) * 2;
-      const float ms = __ldcg(pm);
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - mmax);
-      lsum += __ldcg(pm + 1) * w;
-      const float* po = a.part_o + ((size_t)sp * Mq_total + gr) * a.d + head * kHd + c4;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] += __ldcg(po + e) * w;
+    for (int sp = 0; sp < kMaxAttnSplits; ++sp) {
+      if (sp < a.splits && ms[sp] != -INFINITY) {
+        const float w = exp2f(ms[sp] - mmax);
+        lsum += ls[sp] * w;
+        acc[0] += os[sp].x * w;
+        acc[1] += os[sp].y * w;
+        acc[2] += os[sp].z * w;
+        acc[3] += os[sp].w * w;
+      }
     }
     const float inv = 1.f / lsum;
-    __nv_bfloat16* og = a.o + gr * a.d + head * kHd + c4;
+    __nv_bfloat16* og = a.o + (qrow_base + r) * a.d + head * kHd + c4;
     *reinterpret_cast<__nv_bfloat162*>(og) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
     *reinterpret_cast<__nv_bfloat162*>(og + 2) = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
   }
+  cluster.sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 
 // ---------------------------------------------------------------------------

@@ -114,7 +114,10 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
   // every CTA must own at least one (tile, k-step) unit: the fixup counts
   // the CTAs between a tile's first and last contributor
   const long long units = (long long)a.m_tiles * a.n_tiles * a.k_tiles;
-  const int grid = (int)std::min<long long>(num_sms(), units);
+  // at least k_tiles / 14 units per CTA, so that at most 16 CTAs share a tile
+  // (the fixup merges up to 16 partial slots)
+  const long long min_units = (a.k_tiles + 13) / 14;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(num_sms(), units / min_units));
   switch (BN) {
     case 64:
       gemm_tc_kernel<64><<<grid, kGemmThreads, GemmCfg<64>::kSmem, s>>>(maps, a);
@@ -158,17 +161,39 @@ cudaError_t launch_lmhead_tc(const GemmMaps& maps, GemmArgs ga, LmArgs la, int B
 struct AttnPlan {
   int q_tiles, splits, cps;
 };
+// Split the keys of small grids (a batch-1 block: heads x 1 query tile) over
+// up to 8 CTAs of a cluster so that about two CTAs run per SM.
 AttnPlan plan_attention(int batch, int rows_per_seq, int heads, int L) {
   AttnPlan p;
   p.q_tiles = (rows_per_seq + 63) / 64;
   const int n_chunks = (L + kKeyChunk - 1) / kKeyChunk;
   const int base = batch * p.q_tiles * heads;
   int want = (2 * num_sms() + base - 1) / base;
-  if (want < 1) want = 1;
-  if (want > n_chunks) want = n_chunks;
+  want = std::max(1, std::min(std::min(want, n_chunks), kMaxAttnSplits));
   p.cps = (n_chunks + want - 1) / want;
   p.splits = (n_chunks + p.cps - 1) / p.cps;
   return p;
+}
+
+cudaError_t launch_attention(const AttnArgs& aa, int batch, cudaStream_t s) {
+  dim3 g(batch * aa.q_tiles, aa.heads, aa.splits);
+  if (aa.splits == 1) {
+    attn_bf16_kernel<<<g, kAttnThreads, kAttnSmem, s>>>(aa);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = g;
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = aa.splits;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_bf16_kernel, aa);
 }
 
 struct GraphSet {
@@ -214,11 +239,6 @@ struct dinfer_ctx {
   size_t n_tickets = 0;
   SoftmaxState* lm_part = nullptr;
   int* lm_ticket = nullptr;
-  float* attn_part_o = nullptr;
-  float* attn_part_ml = nullptr;
-  size_t attn_part_rows = 0;  // capacity in (splits * rows)
-  int* attn_tickets = nullptr;
-  size_t n_attn_tickets = 0;
 
   // weight maps (bf16)
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
@@ -319,16 +339,6 @@ struct Fwd {
   float threshold;
 };
 
-// Split-key attention partials are sized at creation: splits > 1 only when
-// batch * q_tiles * heads < 2 * SMs, which bounds splits * rows * heads by
-// 4 * SMs * 64.
-dinfer_status ensure_attn_ws(dinfer_ctx* c, const AttnPlan& p, int rows) {
-  const size_t need = (size_t)p.splits * rows;
-  if (p.splits > 1 && need * c->desc.n_heads > c->attn_part_rows)
-    return fail(c, DINFER_EINVAL, "attention split workspace too small (%zu rows)", need);
-  return DINFER_OK;
-}
-
 // Enqueue one forward over f.rows rows, final norm of the block rows, LM head,
 // decode and (optionally) the commit.  Works eagerly or under stream capture.
 dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
@@ -352,10 +362,6 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
   }
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
-  if (c->bf16) {
-    dinfer_status st = ensure_attn_ws(c, ap, rows);
-    if (st != DINFER_OK) return st;
-  }
 
   for (int l = 0; l < d.n_layers; ++l) {
     // a2: RMSNorm -> QKV GEMM (+RoPE, cache write)
@@ -408,9 +414,7 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       aa.d = D; aa.heads = H; aa.L = f.L; aa.rows_per_seq = f.rows_per_seq;
       aa.q_tiles = ap.q_tiles; aa.splits = ap.splits; aa.chunks_per_split = ap.cps;
       aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-      aa.part_o = c->attn_part_o; aa.part_ml = c->attn_part_ml; aa.tickets = c->attn_tickets;
-      dim3 g(f.batch * ap.q_tiles, H, ap.splits);
-      attn_bf16_kernel<<<g, kAttnThreads, kAttnSmem, s>>>(aa);
+      CK(launch_attention(aa, f.batch, s));
     } else {
       AttnF32Args aa{(const float*)c->q, (const float*)c->kc_layer(l), (const float*)c->vc_layer(l),
                      (float*)c->attn_o, D, H, hd, f.L, f.rows_per_seq, 1.f / sqrtf((float)hd)};
@@ -768,14 +772,6 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
   AL(c->lm_part, (size_t)G * 1024 * sizeof(SoftmaxState));
   AL(c->lm_ticket, 16);
   CKC(cudaMemset(c->lm_ticket, 0, 16));
-  if (c->bf16) {
-    c->attn_part_rows = (size_t)4 * G * 64;  // in units of (row, head)
-    AL(c->attn_part_o, c->attn_part_rows * desc->head_dim * 4);
-    AL(c->attn_part_ml, c->attn_part_rows * 2 * 4);
-  }
-  c->n_attn_tickets = (size_t)desc->max_batch * ((desc->max_seq + 63) / 64 + 1) * desc->n_heads;
-  AL(c->attn_tickets, c->n_attn_tickets * 4);
-  CKC(cudaMemset(c->attn_tickets, 0, c->n_attn_tickets * 4));
 
   if (c->bf16) {
     const int nl = desc->n_layers;
@@ -1054,26 +1050,17 @@ dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void*
   dinfer_ctx* c = nullptr;
   if (!q || !k || !v || !out) return fail(c, DINFER_EINVAL, "NULL operand");
   if (batch < 1 || rows_per_seq < 1 || L < 1 || heads < 1) return fail(c, DINFER_EINVAL, "unsupported shape");
-  OpWs o;
-  if (!op_ws(workspace, workspace_bytes, o)) return fail(c, DINFER_EINVAL, "workspace too small");
+  (void)workspace;
+  (void)workspace_bytes;
   if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
   const AttnPlan ap = plan_attention(batch, rows_per_seq, heads, L);
-  const size_t rows = (size_t)batch * rows_per_seq, d = (size_t)heads * kHd;
-  const size_t need_o = ap.splits > 1 ? ap.splits * rows * d * 4 : 0;
-  const size_t need_ml = ap.splits > 1 ? ap.splits * rows * heads * 2 * 4 : 0;
-  if (need_o + need_ml > o.data_bytes) return fail(c, DINFER_EINVAL, "workspace too small");
-  if ((size_t)batch * ap.q_tiles * heads * 4 > kOpTicketBytes) return fail(c, DINFER_EINVAL, "too many tiles");
   AttnArgs aa{};
   aa.q = (const __nv_bfloat16*)q; aa.k = (const __nv_bfloat16*)k; aa.v = (const __nv_bfloat16*)v;
   aa.o = (__nv_bfloat16*)out;
-  aa.d = (int)d; aa.heads = heads; aa.L = L; aa.rows_per_seq = rows_per_seq;
+  aa.d = heads * kHd; aa.heads = heads; aa.L = L; aa.rows_per_seq = rows_per_seq;
   aa.q_tiles = ap.q_tiles; aa.splits = ap.splits; aa.chunks_per_split = ap.cps;
   aa.scale_log2 = 1.4426950408889634f / sqrtf((float)kHd);
-  aa.part_o = reinterpret_cast<float*>(o.data);
-  aa.part_ml = reinterpret_cast<float*>(o.data + need_o);
-  aa.tickets = o.tickets;
-  dim3 g(batch * ap.q_tiles, heads, ap.splits);
-  attn_bf16_kernel<<<g, kAttnThreads, kAttnSmem, reinterpret_cast<cudaStream_t>(stream)>>>(aa);
+  CK(launch_attention(aa, batch, reinterpret_cast<cudaStream_t>(stream)));
   CK(cudaGetLastError());
   return DINFER_OK;
 }

@@ -195,24 +195,56 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
   }
 }
 
-// Segment (tile t, k-steps [kb, ke)) containing unit u of this CTA's range.
-struct SegIter {
+// The segments (tile t, k-steps [kb, ke)) of one CTA's unit range.  In
+// stream-K mode the range [u0, u1) covers the tail of tile tf, whole tiles,
+// and the head of tile tl; the partial segments are processed FIRST so that
+// the cross-CTA reduction of a shared tile happens while the other CTAs are
+// still streaming, and the kernel ends on whole tiles.
+struct SegList {
   int stream_k, k_tiles;
-  long long u_end;
-  __device__ __forceinline__ void seg(long long u, int& t, int& kb, int& ke) const {
-    if (stream_k) {
-      t = (int)(u / k_tiles);
-      kb = (int)(u - (long long)t * k_tiles);
-      long long lim = (long long)(t + 1) * k_tiles;
-      if (lim > u_end) lim = u_end;
-      ke = kb + (int)(lim - u);
-    } else {
-      t = (int)u;
+  long long u0, u1;
+  int tf, nseg, first_partial, last_partial, np;
+  __device__ __forceinline__ void init(int sk, int kt, long long b, long long e) {
+    stream_k = sk;
+    k_tiles = kt;
+    u0 = b;
+    u1 = e;
+    if (u1 <= u0) {
+      nseg = 0;
+      return;
+    }
+    if (!sk) {
+      tf = (int)u0;
+      nseg = (int)(u1 - u0);
+      first_partial = last_partial = np = 0;
+      return;
+    }
+    tf = (int)(u0 / kt);
+    const int tl = (int)((u1 - 1) / kt);
+    nseg = tl - tf + 1;
+    first_partial = (u0 % kt) != 0 || (nseg == 1 && (u1 % kt) != 0);
+    last_partial = nseg > 1 && (u1 % kt) != 0;
+    np = first_partial + last_partial;
+  }
+  // natural index of the j-th processed segment
+  __device__ __forceinline__ int natural(int j) const {
+    if (j < np) return (j == 0 && last_partial) ? nseg - 1 : 0;
+    return (first_partial ? 1 : 0) + (j - np);
+  }
+  __device__ __forceinline__ void seg(int j, int& t, int& kb, int& ke) const {
+    const int k = natural(j);
+    t = tf + k;
+    if (!stream_k) {
       kb = 0;
       ke = k_tiles;
+      return;
     }
+    const long long ts = (long long)t * k_tiles;
+    const long long a = ts > u0 ? ts : u0;
+    const long long b = (ts + k_tiles) < u1 ? (ts + k_tiles) : u1;
+    kb = (int)(a - ts);
+    ke = (int)(b - ts);
   }
-  __device__ __forceinline__ long long units(int kb, int ke) const { return stream_k ? (ke - kb) : 1; }
 };
 
 struct Pipe {
@@ -227,15 +259,15 @@ struct Pipe {
 
 // TMA producer loop (one elected thread of warp 0).
 template <int BN>
-__device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArgs& a, const SegIter& si,
-                                             long long u_begin, const Pipe& p, int m_tiles) {
+__device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArgs& a, const SegList& sl,
+                                             const Pipe& p, int m_tiles) {
   using C = GemmCfg<BN>;
   const uint64_t pol_w = l2_policy_evict_first();
   const uint64_t pol_x = l2_policy_evict_last();
   uint32_t it = 0;
-  for (long long u = u_begin; u < si.u_end && !*p.abort_flag;) {
+  for (int j = 0; j < sl.nseg && !*p.abort_flag; ++j) {
     int t, kb, ke;
-    si.seg(u, t, kb, ke);
+    sl.seg(j, t, kb, ke);
     const int nt = t / m_tiles, mt = t % m_tiles;
     bool ok = true;
     for (int k = kb; k < ke; ++k, ++it) {
@@ -246,20 +278,18 @@ __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArg
       load_stage<BN>(maps, a, p.stages + s * C::kStage, &p.full[s], nt, mt, k, pol_w, pol_x);
     }
     if (!ok) break;
-    u += si.units(kb, ke);
   }
 }
 
 // MMA issue loop (one elected thread of warp 1).
 template <int BN>
-__device__ __forceinline__ void run_mma(const SegIter& si, long long u_begin, const Pipe& p, uint32_t tmem_base) {
+__device__ __forceinline__ void run_mma(const SegList& sl, const Pipe& p, uint32_t tmem_base) {
   using C = GemmCfg<BN>;
   constexpr uint32_t idesc = make_idesc_bf16(128, BN);
   uint32_t it = 0;
-  int j = 0;
-  for (long long u = u_begin; u < si.u_end && !*p.abort_flag; ++j) {
+  for (int j = 0; j < sl.nseg && !*p.abort_flag; ++j) {
     int t, kb, ke;
-    si.seg(u, t, kb, ke);
+    sl.seg(j, t, kb, ke);
     const int acc = j & 1;
     const uint32_t use = j >> 1;
     if (!mbar_wait(&p.tempty[acc], (use & 1) ^ 1, p.abort_flag)) break;
@@ -282,7 +312,6 @@ __device__ __forceinline__ void run_mma(const SegIter& si, long long u_begin, co
     }
     if (!ok) break;
     tc_commit(&p.tfull[acc]);
-    u += si.units(kb, ke);
   }
   tc_commit(p.drain);
   mbar_wait(p.drain, 0, p.abort_flag);
@@ -342,8 +371,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tiles = a.m_tiles * a.n_tiles;
   sc.KT = a.stream_k ? a.k_tiles : 1;
   sc.U = (long long)tiles * sc.KT;
-  const long long u_begin = sc.start(blockIdx.x);
-  SegIter si{a.stream_k, a.k_tiles, sc.start(blockIdx.x + 1)};
+  SegList sl;
+  sl.init(a.stream_k, a.k_tiles, sc.start(blockIdx.x), sc.start(blockIdx.x + 1));
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.b);
@@ -356,19 +385,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (elect_one_sync()) run_producer<BN>(maps, a, si, u_begin, p, a.m_tiles);
+    if (elect_one_sync()) run_producer<BN>(maps, a, sl, p, a.m_tiles);
   } else if (warp == 1) {
-    if (elect_one_sync()) run_mma<BN>(si, u_begin, p, tmem_base);
+    if (elect_one_sync()) run_mma<BN>(sl, p, tmem_base);
   } else {
     // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;          // output feature row inside the tile
     const int ep_tid = threadIdx.x - 64;    // 0..127
-    int j = 0;
-    for (long long u = u_begin; u < si.u_end; ++j) {
+    for (int j = 0; j < sl.nseg; ++j) {
       int t, kb, ke;
-      si.seg(u, t, kb, ke);
-      u += si.units(kb, ke);
+      sl.seg(j, t, kb, ke);
       const int nt = t / a.m_tiles, mt = t % a.m_tiles;
       const int acc = j & 1;
       const uint32_t use = j >> 1;
@@ -386,14 +413,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_before();
         mbar_arrive(&p.tempty[acc]);
       } else {
-        const int which = (j == 0) ? 0 : 1;
-        float* slot = a.ws + ((size_t)blockIdx.x * 2 + which) * (BN * 128);
+        // partial tile: slot 0 holds this CTA's part of its first tile, slot 1
+        // of its last; layout [row][BN] so each thread moves whole float4s
+        const int which = (t == sl.tf) ? 0 : 1;
+        float4* slot = reinterpret_cast<float4*>(a.ws + ((size_t)blockIdx.x * 2 + which) * (BN * 128)) +
+                       (size_t)row * (BN / 4);
 #pragma unroll 1
         for (int c = 0; c < BN / 16; ++c) {
           float v[16];
           tmem_ld16(tbase + c * 16, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) slot[(c * 16 + i) * 128 + row] = v[i];
+          for (int i = 0; i < 4; ++i)
+            slot[c * 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         tc_fence_before();
         mbar_arrive(&p.tempty[acc]);
@@ -411,17 +442,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         named_bar_sync(1, 128);
         if (*last_flag) {
           __threadfence();
+          // the contributors' slots for this tile, summed in CTA order, four
+          // contributors' float4s in flight at a time
+          const int nc = c_last - c_first + 1;
 #pragma unroll 1
           for (int c = 0; c < BN / 16; ++c) {
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int first_tile = (int)(sc.start(cc) / a.k_tiles);
-              const int w = (t == first_tile) ? 0 : 1;
-              const float* sl = a.ws + ((size_t)cc * 2 + w) * (BN * 128);
+#pragma unroll 1
+            for (int x0 = 0; x0 < nc; x0 += 4) {
+              float4 buf[4][4];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * 128 + row);
+              for (int x = 0; x < 4; ++x) {
+                if (x0 + x < nc) {
+                  const int cc = c_first + x0 + x;
+                  const int w = (t == (int)(sc.start(cc) / a.k_tiles)) ? 0 : 1;
+                  const float4* src = reinterpret_cast<const float4*>(a.ws + ((size_t)cc * 2 + w) * (BN * 128)) +
+                                      (size_t)row * (BN / 4) + c * 4;
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) buf[x][i] = __ldcg(src + i);
+                }
+              }
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                if (x0 + x < nc) {
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    v[4 * i] += buf[x][i].x;
+                    v[4 * i + 1] += buf[x][i].y;
+                    v[4 * i + 2] += buf[x][i].z;
+                    v[4 * i + 3] += buf[x][i].w;
+                  }
+                }
+              }
             }
             epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
           }

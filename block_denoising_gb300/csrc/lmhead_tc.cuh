@@ -55,8 +55,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   sc.G = gridDim.x;
   sc.KT = 1;
   sc.U = (long long)ga.m_tiles * ga.n_tiles;
-  const long long u_begin = sc.start(blockIdx.x);
-  SegIter si{0, ga.k_tiles, sc.start(blockIdx.x + 1)};
+  SegList sl;
+  sl.init(0, ga.k_tiles, sc.start(blockIdx.x), sc.start(blockIdx.x + 1));
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.b);
@@ -74,18 +74,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (elect_one_sync()) run_producer<BN>(maps, ga, si, u_begin, p, ga.m_tiles);
+    if (elect_one_sync()) run_producer<BN>(maps, ga, sl, p, ga.m_tiles);
   } else if (warp == 1) {
-    if (elect_one_sync()) run_mma<BN>(si, u_begin, p, tmem_base);
+    if (elect_one_sync()) run_mma<BN>(sl, p, tmem_base);
   } else {
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int ep_tid = threadIdx.x - 64;
     const float kLog2e = 1.4426950408889634f;
     const float sl2 = la.scale * kLog2e;
-    int j = 0;
-    for (long long u = u_begin; u < si.u_end; ++u, ++j) {
-      const int t = (int)u;
+    for (int j = 0; j < sl.nseg; ++j) {
+      const int t = sl.tf + j;
       const int nt = t / ga.m_tiles, mt = t % ga.m_tiles;
       const int acc = j & 1;
       if (!mbar_wait(&p.tfull[acc], (j >> 1) & 1, p.abort_flag)) break;

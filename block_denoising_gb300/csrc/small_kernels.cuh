@@ -44,29 +44,80 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { re
 
 // out[r, :] = h[src(r), :] / sqrt(mean(h^2) + eps) * g, rounded to the GEMM
 // input type.  src(r) = seq_index(r) when gather != 0 (block rows of a
-// full-sequence residual), else r.
+// full-sequence residual), else r.  One CTA of 256 threads per row; rows of
+// up to 8192 values are held in registers (float4) so every load is issued
+// before the reduction.
+__device__ __forceinline__ void load4(const float* g, int k, float (&w)[4]) {
+  const float4 t = reinterpret_cast<const float4*>(g)[k];
+  w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* g, int k, float (&w)[4]) {
+  const uint2 t = reinterpret_cast<const uint2*>(g)[k];
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&t.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&t.y);
+  w[0] = __low2float(a); w[1] = __high2float(a); w[2] = __low2float(b); w[3] = __high2float(b);
+}
+__device__ __forceinline__ void store4(float* o, int k, float a, float b, float c, float d) {
+  reinterpret_cast<float4*>(o)[k] = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* o, int k, float a, float b, float c, float d) {
+  __nv_bfloat162 x = __floats2bfloat162_rn(a, b), y = __floats2bfloat162_rn(c, d);
+  uint2 t;
+  t.x = *reinterpret_cast<uint32_t*>(&x);
+  t.y = *reinterpret_cast<uint32_t*>(&y);
+  reinterpret_cast<uint2*>(o)[k] = t;
+}
+
 template <typename Tg, typename To>
-__global__ void rmsnorm_kernel(const float* __restrict__ h, const Tg* __restrict__ g, To* __restrict__ out,
-                               int rows, int d, float eps, int gather, RowMap rm, const DevState* st) {
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ h, const Tg* __restrict__ g,
+                                                      To* __restrict__ out, int rows, int d, float eps, int gather,
+                                                      RowMap rm, const DevState* st) {
   const int r = blockIdx.x;
   if (r >= rows) return;
   const size_t src = gather ? rm.seq_index(r, st) : (size_t)r;
   const float* x = h + src * d;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  To* o = out + (size_t)r * d;
   __shared__ float red[32];
+  const int n4 = d >> 2;
+  const bool vec = (d & 3) == 0 && n4 <= 8 * 256;
+  float v[8][4];
+  float ss = 0.f;
+  if (vec) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = threadIdx.x + i * 256;
+      if (k < n4) {
+        const float4 t = reinterpret_cast<const float4*>(x)[k];
+        v[i][0] = t.x; v[i][1] = t.y; v[i][2] = t.z; v[i][3] = t.w;
+        ss = fmaf(t.x, t.x, fmaf(t.y, t.y, fmaf(t.z, t.z, fmaf(t.w, t.w, ss))));
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
   if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-    v = warp_sum(v);
-    if (threadIdx.x == 0) red[0] = v;
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) red[0] = t;
   }
   __syncthreads();
   const float inv = rsqrtf(red[0] / (float)d + eps);
-  To* o = out + (size_t)r * d;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = from_float<To>(x[i] * inv * (float)g[i]);
+  if (vec) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = threadIdx.x + i * 256;
+      if (k < n4) {
+        float w[4];
+        load4(g, k, w);
+        store4(o, k, v[i][0] * inv * w[0], v[i][1] * inv * w[1], v[i][2] * inv * w[2], v[i][3] * inv * w[3]);
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = from_float<To>(x[i] * inv * (float)g[i]);
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -98,3 +98,14 @@ def test_stream_k_schedule_arithmetic(U, G):
     for c in range(G):
         assert _owner(U, G, starts[c]) == c
         assert _owner(U, G, starts[c + 1] - 1) == c
+
+
+@pytest.mark.parametrize("tiles,KT", [(96, 64), (32, 64), (32, 192), (2, 2), (1, 64), (3, 5), (576, 64)])
+def test_stream_k_contributors_per_tile_bounded(tiles, KT):
+    # launcher: G = min(SMs, U / ceil(KT / 14)); every tile then has at most 16 contributors
+    U = tiles * KT
+    G = max(1, min(152, U // ((KT + 13) // 14)))
+    for t in range(tiles):
+        c_first = _owner(U, G, t * KT)
+        c_last = _owner(U, G, t * KT + KT - 1)
+        assert c_last - c_first + 1 <= 16
