@@ -96,6 +96,9 @@ WORKLOADS = {
                     "LLaDA-8B-shaped dense bf16, b16 P1024 G256 B32 tau0.9"),
     "lladamoe_long": (LLADA_MOE, RunConfig(1, 8192, 512, 64, 0.85),
                       "LLaDA-MoE-shaped bf16 long context, b1 P8192 G512 B64 tau0.85"),
+    # profiling / parity case: the LLaDA-8B shapes with 2 of the 32 layers
+    "llada8b_b1_2layer": (dataclasses.replace(LLADA_8B, n_layers=2), RunConfig(1, 512, 1024, 64, 0.9),
+                          "LLaDA-8B widths, 2 layers, b1 P512 G1024 B64 tau0.9"),
 }
 
 
