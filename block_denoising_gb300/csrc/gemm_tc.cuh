@@ -76,7 +76,7 @@ struct GemmCfg {
   static constexpr int kStage = kStageA + kStageB;
   static constexpr int kStages = (BN == 64) ? 8 : (BN == 128 ? 6 : 4);
   static constexpr int kXchgFloats = 128 * 17;
-  static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStage + kXchgFloats * 4 + 256;
+  static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStage + kXchgFloats * 4 + 512;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
 };
 
@@ -116,11 +116,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
                                                float* xchg) {
   if (a.q_out != nullptr) {
     // ---- QKV: RoPE pairs (i, i + 64) sit in rows row and row ^ 64 ----
-    float* mine = xchg + row * 17;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mine[i] = v[i];
-    named_bar_sync(1, 128);
-    const float* part = xchg + (row ^ 64) * 17;
     const int n = nt * 128 + row;
     const int d = a.d_model;
     const int which = n / d;          // 0 q, 1 k, 2 v
@@ -130,66 +125,83 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
     const int half = hd >> 1;
     const int j = i % half;
     const int base_pos = a.pos_from_state ? a.state->block_start : 0;
+    // every global load of the chunk is issued before any store
+    float cs[16], sn[16];
+    if (which < 2) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = min(m0 + c, a.M - 1);
+        const int bi = m / a.rows_per_seq;
+        const int pos = base_pos + (m - bi * a.rows_per_seq);
+        cs[c] = __ldg(a.rope_cos + pos * half + j);
+        sn[c] = __ldg(a.rope_sin + pos * half + j);
+      }
+    }
+    float* mine = xchg + row * 17;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) mine[c] = v[c];
+    named_bar_sync(1, 128);
+    const float* part = xchg + (row ^ 64) * 17;
+    float o[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float p = part[c];
+      o[c] = (which == 2) ? v[c] : ((i < half) ? (v[c] * cs[c] - p * sn[c]) : (v[c] * cs[c] + p * sn[c]));
+    }
+    named_bar_sync(1, 128);
+    __nv_bfloat16* __restrict__ dst = which == 0 ? a.q_out : (which == 1 ? a.k_cache : a.v_cache);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int m = m0 + c;
       if (m < a.M) {
         const int bi = m / a.rows_per_seq;
         const int pos = base_pos + (m - bi * a.rows_per_seq);
-        float o = v[c];
-        if (which < 2) {
-          const float cs = a.rope_cos[pos * half + j];
-          const float sn = a.rope_sin[pos * half + j];
-          const float p = part[c];
-          o = (i < half) ? (v[c] * cs - p * sn) : (v[c] * cs + p * sn);
-        }
-        const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-        if (which == 0) {
-          a.q_out[(size_t)m * d + nn] = ob;
-        } else {
-          const size_t ci = ((size_t)bi * a.seq_len + pos) * d + nn;
-          if (which == 1) a.k_cache[ci] = ob; else a.v_cache[ci] = ob;
-        }
+        const size_t off = which == 0 ? (size_t)m * d + nn : ((size_t)bi * a.seq_len + pos) * d + nn;
+        dst[off] = __float2bfloat16_rn(o[c]);
       }
     }
-    named_bar_sync(1, 128);
   } else if (a.a_mode == A_PAIR) {
     // ---- SwiGLU: gate row r (< 64) pairs with up row r + 64 ----
     float* mine = xchg + row * 17;
 #pragma unroll
     for (int i = 0; i < 16; ++i) mine[i] = v[i];
     named_bar_sync(1, 128);
-    if (row < 64) {
+    float o[16];
+    const bool act_row = row < 64;
+    if (act_row) {
       const float* up = xchg + (row + 64) * 17;
-      const int jf = nt * 64 + row;
-      if (jf < a.N) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int m = m0 + c;
-          if (m < a.M) {
-            const float g = v[c];
-            const float s = g / (1.0f + expf(-g));
-            a.out_bf16[(size_t)m * a.ldo + jf] = __float2bfloat16_rn(s * up[c]);
-          }
-        }
+      for (int c = 0; c < 16; ++c) {
+        const float g = v[c];
+        o[c] = g / (1.0f + expf(-g)) * up[c];
       }
     }
     named_bar_sync(1, 128);
+    const int jf = nt * 64 + row;
+    if (act_row && jf < a.N) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (m0 + c < a.M) a.out_bf16[(size_t)(m0 + c) * a.ldo + jf] = __float2bfloat16_rn(o[c]);
+    }
   } else {
     const int n = nt * 128 + row;
     if (n < a.N) {
+      if (a.resid) {
+        // residual add: all 16 loads in flight before the stores
+        float hv[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int m = m0 + c;
-        if (m < a.M) {
-          if (a.resid) {
-            a.resid[(size_t)m * a.N + n] += v[c];
-          } else if (a.out_bf16) {
-            a.out_bf16[(size_t)m * a.ldo + n] = __float2bfloat16_rn(v[c]);
-          } else {
-            a.out_f32[(size_t)m * a.ldo + n] = v[c];
-          }
-        }
+        for (int c = 0; c < 16; ++c) hv[c] = (m0 + c < a.M) ? a.resid[(size_t)(m0 + c) * a.N + n] : 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (m0 + c < a.M) a.resid[(size_t)(m0 + c) * a.N + n] = hv[c] + v[c];
+      } else if (a.out_bf16) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (m0 + c < a.M) a.out_bf16[(size_t)(m0 + c) * a.ldo + n] = __float2bfloat16_rn(v[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (m0 + c < a.M) a.out_f32[(size_t)(m0 + c) * a.ldo + n] = v[c];
       }
     }
   }
@@ -361,6 +373,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* misc;
   const Pipe p = setup_pipe<BN>(smem_raw, xchg, tmem_slot, misc);
   volatile int* last_flag = misc + 1;
+  int* slot_idx = const_cast<int*>(misc + 4);  // [16]: fixup contributors' slots
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -403,16 +416,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       const bool whole = (kb == 0 && ke == a.k_tiles);
-      if (whole) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          float v[16];
-          tmem_ld16(tbase + c * 16, v);
-          epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
-        }
-        tc_fence_before();
-        mbar_arrive(&p.tempty[acc]);
-      } else {
+      int nc = 0;  // > 0: this CTA reduces the tile from nc partial slots
+      if (!whole) {
         // partial tile: slot 0 holds this CTA's part of its first tile, slot 1
         // of its last; layout [row][BN] so each thread moves whole float4s
         const int which = (t == sl.tf) ? 0 : 1;
@@ -440,48 +445,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           *last_flag = is_last;
         }
         named_bar_sync(1, 128);
-        if (*last_flag) {
-          __threadfence();
-          // the contributors' slots for this tile, summed in CTA order, four
-          // contributors' float4s in flight at a time
-          const int nc = c_last - c_first + 1;
-#pragma unroll 1
-          for (int c = 0; c < BN / 16; ++c) {
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
-#pragma unroll 1
-            for (int x0 = 0; x0 < nc; x0 += 4) {
-              float4 buf[4][4];
-#pragma unroll
-              for (int x = 0; x < 4; ++x) {
-                if (x0 + x < nc) {
-                  const int cc = c_first + x0 + x;
-                  const int w = (t == (int)(sc.start(cc) / a.k_tiles)) ? 0 : 1;
-                  const float4* src = reinterpret_cast<const float4*>(a.ws + ((size_t)cc * 2 + w) * (BN * 128)) +
-                                      (size_t)row * (BN / 4) + c * 4;
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) buf[x][i] = __ldcg(src + i);
-                }
-              }
-#pragma unroll
-              for (int x = 0; x < 4; ++x) {
-                if (x0 + x < nc) {
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    v[4 * i] += buf[x][i].x;
-                    v[4 * i + 1] += buf[x][i].y;
-                    v[4 * i + 2] += buf[x][i].z;
-                    v[4 * i + 3] += buf[x][i].w;
-                  }
-                }
-              }
-            }
-            epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
-          }
+        if (!*last_flag) continue;  // uniform across the epilogue warps
+        __threadfence();
+        // the contributors' slots, summed in CTA order; slot indices are
+        // computed once (64-bit schedule arithmetic) into shared memory
+        nc = c_last - c_first + 1;
+        if (ep_tid < nc) {
+          const int cc = c_first + ep_tid;
+          slot_idx[ep_tid] = cc * 2 + ((t == (int)(sc.start(cc) / a.k_tiles)) ? 0 : 1);
         }
         named_bar_sync(1, 128);
       }
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        if (nc == 0) {
+          tmem_ld16(tbase + c * 16, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          // two contributors' float4s in flight at a time
+#pragma unroll 1
+          for (int x0 = 0; x0 < nc; x0 += 2) {
+            float4 buf[2][4];
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+              if (x0 + x < nc) {
+                const float4* src = reinterpret_cast<const float4*>(a.ws + (size_t)slot_idx[x0 + x] * (BN * 128)) +
+                                    (size_t)row * (BN / 4) + c * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) buf[x][i] = __ldcg(src + i);
+              }
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+              if (x0 + x < nc)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  v[4 * i] += buf[x][i].x;
+                  v[4 * i + 1] += buf[x][i].y;
+                  v[4 * i + 2] += buf[x][i].z;
+                  v[4 * i + 3] += buf[x][i].w;
+                }
+          }
+        }
+        epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
+      }
+      if (whole) {
+        tc_fence_before();
+        mbar_arrive(&p.tempty[acc]);
+      }
+      named_bar_sync(1, 128);
     }
   }
 

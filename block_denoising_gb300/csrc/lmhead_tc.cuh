@@ -25,7 +25,7 @@ struct LmArgs {
 template <int BN>
 struct LmCfg {
   static constexpr int kMaxM = 1024;
-  static constexpr int kSmem = GemmCfg<BN>::kSmem + kMaxM * 12 + 4 * 16 * 12 + 64;
+  static constexpr int kSmem = GemmCfg<BN>::kSmem + kMaxM * 12 + 4 * 16 * 12 + 128;
 };
 
 template <int BN>
@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const Pipe p = setup_pipe<BN>(smem_raw, xchg, tmem_slot, misc);
   volatile int* last_flag = misc + 1;
   // running softmax state per token, after the GEMM's shared memory
-  uint8_t* extra = reinterpret_cast<uint8_t*>(const_cast<int*>(misc + 4));
+  uint8_t* extra = reinterpret_cast<uint8_t*>(const_cast<int*>(misc + 24));
   float* st_m = reinterpret_cast<float*>(extra);
   float* st_s = st_m + LmCfg<BN>::kMaxM;
   int* st_a = reinterpret_cast<int*>(st_s + LmCfg<BN>::kMaxM);
