@@ -118,15 +118,19 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
   // (the fixup merges up to 16 partial slots)
   const long long min_units = (a.k_tiles + 13) / 14;
   const int grid = (int)std::max<long long>(1, std::min<long long>(num_sms(), units / min_units));
+  const int tiles = a.m_tiles * a.n_tiles;
   switch (BN) {
     case 64:
       gemm_tc_kernel<64><<<grid, kGemmThreads, GemmCfg<64>::kSmem, s>>>(maps, a);
+      splitk_fixup_kernel<64><<<tiles * 4, 128, 0, s>>>(a, grid);
       break;
     case 128:
       gemm_tc_kernel<128><<<grid, kGemmThreads, GemmCfg<128>::kSmem, s>>>(maps, a);
+      splitk_fixup_kernel<128><<<tiles * 8, 128, 0, s>>>(a, grid);
       break;
     default:
       gemm_tc_kernel<256><<<grid, kGemmThreads, GemmCfg<256>::kSmem, s>>>(maps, a);
+      splitk_fixup_kernel<256><<<tiles * 16, 128, 0, s>>>(a, grid);
       break;
   }
   return cudaGetLastError();

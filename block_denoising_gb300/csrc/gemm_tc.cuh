@@ -14,9 +14,11 @@
 //           thread = one output feature), fused output op.
 // Work is split "stream-K": the (tile, k-step) units are divided evenly over
 // the CTAs, so every SM streams the same number of weight bytes whatever the
-// tile count.  A tile shared by several CTAs is reduced by the last CTA to
-// finish it (atomic ticket), summing the fp32 partials in CTA order so that
-// results do not depend on timing.
+// tile count.  A CTA that owns a whole tile applies the fused epilogue
+// itself; a tile shared by several CTAs is left as fp32 partials, which the
+// fixup kernel below sums in CTA order (so results do not depend on timing)
+// and finishes with the same epilogue -- one CTA per 16-column chunk, so the
+// reduction is one parallel round trip instead of a serial tail.
 #pragma once
 #include "common.cuh"
 
@@ -372,8 +374,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot;
   volatile int* misc;
   const Pipe p = setup_pipe<BN>(smem_raw, xchg, tmem_slot, misc);
-  volatile int* last_flag = misc + 1;
-  int* slot_idx = const_cast<int*>(misc + 4);  // [16]: fixup contributors' slots
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -405,7 +405,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;          // output feature row inside the tile
-    const int ep_tid = threadIdx.x - 64;    // 0..127
     for (int j = 0; j < sl.nseg; ++j) {
       int t, kb, ke;
       sl.seg(j, t, kb, ke);
@@ -416,7 +415,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       const bool whole = (kb == 0 && ke == a.k_tiles);
-      int nc = 0;  // > 0: this CTA reduces the tile from nc partial slots
       if (!whole) {
         // partial tile: slot 0 holds this CTA's part of its first tile, slot 1
         // of its last; layout [row][BN] so each thread moves whole float4s
@@ -433,68 +431,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&p.tempty[acc]);
-        __threadfence();
-        named_bar_sync(1, 128);
-        const long long tu0 = (long long)t * a.k_tiles;
-        const int c_first = sc.owner(tu0);
-        const int c_last = sc.owner(tu0 + a.k_tiles - 1);
-        if (ep_tid == 0) {
-          const int prev = atomicAdd(&a.tickets[t], 1);
-          const int is_last = (prev == c_last - c_first);
-          if (is_last) a.tickets[t] = 0;
-          *last_flag = is_last;
-        }
-        named_bar_sync(1, 128);
-        if (!*last_flag) continue;  // uniform across the epilogue warps
-        __threadfence();
-        // the contributors' slots, summed in CTA order; slot indices are
-        // computed once (64-bit schedule arithmetic) into shared memory
-        nc = c_last - c_first + 1;
-        if (ep_tid < nc) {
-          const int cc = c_first + ep_tid;
-          slot_idx[ep_tid] = cc * 2 + ((t == (int)(sc.start(cc) / a.k_tiles)) ? 0 : 1);
-        }
-        named_bar_sync(1, 128);
+        continue;
       }
 #pragma unroll 1
       for (int c = 0; c < BN / 16; ++c) {
         float v[16];
-        if (nc == 0) {
-          tmem_ld16(tbase + c * 16, v);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0.f;
-          // two contributors' float4s in flight at a time
-#pragma unroll 1
-          for (int x0 = 0; x0 < nc; x0 += 2) {
-            float4 buf[2][4];
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-              if (x0 + x < nc) {
-                const float4* src = reinterpret_cast<const float4*>(a.ws + (size_t)slot_idx[x0 + x] * (BN * 128)) +
-                                    (size_t)row * (BN / 4) + c * 4;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) buf[x][i] = __ldcg(src + i);
-              }
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-              if (x0 + x < nc)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  v[4 * i] += buf[x][i].x;
-                  v[4 * i + 1] += buf[x][i].y;
-                  v[4 * i + 2] += buf[x][i].z;
-                  v[4 * i + 3] += buf[x][i].w;
-                }
-          }
-        }
+        tmem_ld16(tbase + c * 16, v);
         epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
       }
-      if (whole) {
-        tc_fence_before();
-        mbar_arrive(&p.tempty[acc]);
-      }
-      named_bar_sync(1, 128);
+      tc_fence_before();
+      mbar_arrive(&p.tempty[acc]);
     }
   }
 
@@ -504,6 +450,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
+}
+
+// Split-K fixup: block = (tile, 16-column chunk), 128 threads = the tile's
+// output rows.  Sums the partial slots of the tile's contributors (the CTAs
+// of the GEMM grid whose unit ranges overlap it) in CTA order, then applies
+// the GEMM's epilogue.  Tiles owned whole by one CTA were finished by it.
+template <int BN>
+__global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a, int gemm_grid) {
+  __shared__ float xchg[128 * 17];
+  __shared__ int slot_idx[32];
+  const int chunks = BN / 16;
+  const int t = blockIdx.x / chunks, c = blockIdx.x % chunks;
+  Sched sc;
+  sc.G = gemm_grid;
+  sc.KT = a.k_tiles;
+  sc.U = (long long)a.m_tiles * a.n_tiles * a.k_tiles;
+  const long long tu0 = (long long)t * a.k_tiles;
+  const int c_first = sc.owner(tu0);
+  const int c_last = sc.owner(tu0 + a.k_tiles - 1);
+  if (c_first == c_last) return;  // whole tile: done by the GEMM
+  const int nc = c_last - c_first + 1;
+  const int row = threadIdx.x;
+  if (row < nc && row < 32) {
+    const int cc = c_first + row;
+    slot_idx[row] = cc * 2 + ((t == (int)(sc.start(cc) / a.k_tiles)) ? 0 : 1);
+  }
+  __syncthreads();
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll 1
+  for (int x0 = 0; x0 < nc; x0 += 4) {
+    float4 buf[4][4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      if (x0 + x < nc) {
+        const float4* src = reinterpret_cast<const float4*>(a.ws + (size_t)slot_idx[x0 + x] * (BN * 128)) +
+                            (size_t)row * (BN / 4) + c * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) buf[x][i] = __ldcg(src + i);
+      }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      if (x0 + x < nc)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[4 * i] += buf[x][i].x;
+          v[4 * i + 1] += buf[x][i].y;
+          v[4 * i + 2] += buf[x][i].z;
+          v[4 * i + 3] += buf[x][i].w;
+        }
+  }
+  const int nt = t / a.m_tiles, mt = t % a.m_tiles;
+  epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
 }
 
 }  // namespace dinfer
