@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int c_begin = split * a.chunks_per_split;
   const int c_end = min(n_chunks, c_begin + a.chunks_per_split);
 
+  pdl_wait();
   load_tile_async(s_q, qg, a.d, q_valid);
   cp_async_commit();
   if (c_begin < c_end) {
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     l_r[h] += __shfl_xor_sync(0xffffffffu, l_r[h], 2);
   }
   const int r_lo = warp * 16 + g, r_hi = r_lo + 8;  // rows inside the tile
+  if (threadIdx.x == 0) pdl_trigger();
   if (a.splits == 1) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {

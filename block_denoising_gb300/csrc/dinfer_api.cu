@@ -77,6 +77,37 @@ int num_sms() {
   return g_num_sms;
 }
 
+// Launch with programmatic dependent launch (the kernel may start while the
+// previous kernel of the stream finishes; it waits with griddepcontrol.wait)
+// and an optional cluster along z.
+bool g_pdl = true;
+template <typename... ExpTypes, typename... ActTypes>
+cudaError_t launchk(void (*kernel)(ExpTypes...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_z,
+                    ActTypes&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  if (g_pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_z > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = 1;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = cluster_z;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<ActTypes>(args)...);
+}
+
 bool set_smem_attrs() {
   static bool done = false;
   if (done) return true;
@@ -106,34 +137,50 @@ bool set_smem_attrs() {
 // Stream-K fixup workspace: floats per CTA slot pair and the ticket count.
 size_t gemm_ws_floats(int grid) { return (size_t)grid * 2 * 256 * 128; }
 
-// Launch the tensor-core GEMM (templated on the token tile).
-cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s) {
+// Launch the tensor-core GEMM (templated on the token tile).  Tiles shared
+// by several CTAs are finished by the split-K fixup kernel, or -- residual
+// GEMMs with defer_resid -- by the following resid_norm_kernel.
+cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s, bool defer_resid = false) {
   a.m_tiles = (a.M + BN - 1) / BN;
   a.k_tiles = a.K / 64;
   a.stream_k = 1;
-  // every CTA must own at least one (tile, k-step) unit: the fixup counts
-  // the CTAs between a tile's first and last contributor
+  // every CTA must own at least one (tile, k-step) unit, and at least
+  // k_tiles / 14 of them so that at most 16 CTAs share a tile
   const long long units = (long long)a.m_tiles * a.n_tiles * a.k_tiles;
-  // at least k_tiles / 14 units per CTA, so that at most 16 CTAs share a tile
-  // (the fixup merges up to 16 partial slots)
   const long long min_units = (a.k_tiles + 13) / 14;
-  const int grid = (int)std::max<long long>(1, std::min<long long>(num_sms(), units / min_units));
+  a.grid = (int)std::max<long long>(1, std::min<long long>(num_sms(), units / min_units));
+  if ((unsigned long long)units * (unsigned long long)a.grid >= (1ull << 32)) return cudaErrorInvalidValue;
+  a.slot_tok_major = defer_resid ? 1 : 0;
   const int tiles = a.m_tiles * a.n_tiles;
+  cudaError_t e = cudaSuccess;
   switch (BN) {
     case 64:
-      gemm_tc_kernel<64><<<grid, kGemmThreads, GemmCfg<64>::kSmem, s>>>(maps, a);
-      splitk_fixup_kernel<64><<<tiles * 4, 128, 0, s>>>(a, grid);
+      e = launchk(gemm_tc_kernel<64>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<64>::kSmem, s, 1, maps, a);
+      if (e == cudaSuccess && !defer_resid) e = launchk(splitk_fixup_kernel<64>, dim3(tiles * 4), dim3(128), 0, s, 1, a);
       break;
     case 128:
-      gemm_tc_kernel<128><<<grid, kGemmThreads, GemmCfg<128>::kSmem, s>>>(maps, a);
-      splitk_fixup_kernel<128><<<tiles * 8, 128, 0, s>>>(a, grid);
+      e = launchk(gemm_tc_kernel<128>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<128>::kSmem, s, 1, maps, a);
+      if (e == cudaSuccess && !defer_resid) e = launchk(splitk_fixup_kernel<128>, dim3(tiles * 8), dim3(128), 0, s, 1, a);
       break;
     default:
-      gemm_tc_kernel<256><<<grid, kGemmThreads, GemmCfg<256>::kSmem, s>>>(maps, a);
-      splitk_fixup_kernel<256><<<tiles * 16, 128, 0, s>>>(a, grid);
+      e = launchk(gemm_tc_kernel<256>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<256>::kSmem, s, 1, maps, a);
+      if (e == cudaSuccess && !defer_resid) e = launchk(splitk_fixup_kernel<256>, dim3(tiles * 16), dim3(128), 0, s, 1, a);
       break;
   }
-  return cudaGetLastError();
+  return e;
+}
+
+ResidPlan resid_plan(const GemmArgs& a, int BN, const float* ws) {
+  ResidPlan p;
+  p.ws = ws;
+  p.BN = BN;
+  p.m_tiles = (a.M + BN - 1) / BN;
+  p.n_tiles = a.n_tiles;
+  p.k_tiles = a.K / 64;
+  const long long units = (long long)p.m_tiles * p.n_tiles * p.k_tiles;
+  const long long min_units = (p.k_tiles + 13) / 14;
+  p.grid = (int)std::max<long long>(1, std::min<long long>(num_sms(), units / min_units));
+  return p;
 }
 
 int lmhead_grid(int M, int V) {
@@ -150,16 +197,12 @@ cudaError_t launch_lmhead_tc(const GemmMaps& maps, GemmArgs ga, LmArgs la, int B
   la.dec.n_parts = grid;
   switch (BN) {
     case 64:
-      lmhead_tc_kernel<64><<<grid, kGemmThreads, LmCfg<64>::kSmem, s>>>(maps, ga, la);
-      break;
+      return launchk(lmhead_tc_kernel<64>, dim3(grid), dim3(kGemmThreads), LmCfg<64>::kSmem, s, 1, maps, ga, la);
     case 128:
-      lmhead_tc_kernel<128><<<grid, kGemmThreads, LmCfg<128>::kSmem, s>>>(maps, ga, la);
-      break;
+      return launchk(lmhead_tc_kernel<128>, dim3(grid), dim3(kGemmThreads), LmCfg<128>::kSmem, s, 1, maps, ga, la);
     default:
-      lmhead_tc_kernel<256><<<grid, kGemmThreads, LmCfg<256>::kSmem, s>>>(maps, ga, la);
-      break;
+      return launchk(lmhead_tc_kernel<256>, dim3(grid), dim3(kGemmThreads), LmCfg<256>::kSmem, s, 1, maps, ga, la);
   }
-  return cudaGetLastError();
 }
 
 struct AttnPlan {
@@ -181,23 +224,7 @@ AttnPlan plan_attention(int batch, int rows_per_seq, int heads, int L) {
 
 cudaError_t launch_attention(const AttnArgs& aa, int batch, cudaStream_t s) {
   dim3 g(batch * aa.q_tiles, aa.heads, aa.splits);
-  if (aa.splits == 1) {
-    attn_bf16_kernel<<<g, kAttnThreads, kAttnSmem, s>>>(aa);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = g;
-  cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = kAttnSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 1;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = aa.splits;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_bf16_kernel, aa);
+  return launchk(attn_bf16_kernel, g, dim3(kAttnThreads), kAttnSmem, s, aa.splits, aa);
 }
 
 struct GraphSet {
@@ -239,8 +266,6 @@ struct dinfer_ctx {
   DevState* st = nullptr;
   DevState* st_host = nullptr;  // pinned
   float* gemm_ws = nullptr;
-  int* tickets = nullptr;
-  size_t n_tickets = 0;
   SoftmaxState* lm_part = nullptr;
   int* lm_ticket = nullptr;
 
@@ -345,38 +370,33 @@ struct Fwd {
 
 // Enqueue one forward over f.rows rows, final norm of the block rows, LM head,
 // decode and (optionally) the commit.  Works eagerly or under stream capture.
-dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
+// bf16 layer sequence (per layer, all on the tensor-core path):
+//   [norm] -> QKV GEMM (+fixup: RoPE, q, dual-cache K/V) -> attention ->
+//   O GEMM (deferred residual) -> resid_norm (h += O; ffn norm) ->
+//   gate/up GEMM (+fixup: SwiGLU) -> down GEMM (deferred residual) ->
+//   resid_norm (h += down; next layer's attention norm, or the final norm of
+//   the block rows)
+dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   const dinfer_model_desc& d = c->desc;
   const int D = d.d_model, F = d.ffn, H = d.n_heads, hd = d.head_dim;
   const int rows = f.rows;
   RowMap rm{f.rows_per_seq, f.L, f.pos_from_state};
-  // a1: embedding
-  if (c->bf16)
-    embed_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>((const __nv_bfloat16*)c->W(0), c->ids, c->h, rows, D, d.vocab,
-                                                     rm, c->st);
-  else
-    embed_kernel<float><<<rows, 256, 0, s>>>((const float*)c->W(0), c->ids, c->h, rows, D, d.vocab, rm, c->st);
-  CK(cudaGetLastError());
-
+  CK(launchk(embed_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, 1, (const __nv_bfloat16*)c->W(0),
+             (const int32_t*)c->ids, c->h, rows, D, d.vocab, rm, c->st));
+  CK(launchk(rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(rows), dim3(256), 0, s, 1,
+             (const float*)c->h, (const __nv_bfloat16*)c->LW(0, 0), (__nv_bfloat16*)c->xn, rows, D, d.rms_eps, 0,
+             rm, (const DevState*)c->st));
   const int BN = bn_for_rows(rows);
   GemmMaps mx{}, mo{}, mact{};
-  if (c->bf16) {
-    if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BN) ||
-        !make_map(&mact.b, c->act, rows, F, BN))
-      return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
-  }
+  if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BN) ||
+      !make_map(&mact.b, c->act, rows, F, BN))
+    return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
-
+  const int nthr = D / 16;  // resid_norm threads per row
+  if (nthr > 512 || D % 128) return fail(c, DINFER_EINVAL, "d_model unsupported by the fused residual norm");
   for (int l = 0; l < d.n_layers; ++l) {
-    // a2: RMSNorm -> QKV GEMM (+RoPE, cache write)
-    if (c->bf16)
-      rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<rows, 256, 0, s>>>(
-          c->h, (const __nv_bfloat16*)c->LW(l, 0), (__nv_bfloat16*)c->xn, rows, D, d.rms_eps, 0, rm, c->st);
-    else
-      rmsnorm_kernel<float, float><<<rows, 256, 0, s>>>(c->h, (const float*)c->LW(l, 0), (float*)c->xn, rows, D,
-                                                        d.rms_eps, 0, rm, c->st);
-    CK(cudaGetLastError());
-    if (c->bf16) {
+    // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue
+    {
       GemmMaps m = mx;
       m.a[0] = c->m_wq[l];
       m.a[1] = c->m_wk[l];
@@ -391,25 +411,11 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.rope_cos = c->rope_cos; a.rope_sin = c->rope_sin;
       a.d_model = D; a.head_dim = hd;
       a.rows_per_seq = f.rows_per_seq; a.seq_len = f.L; a.pos_from_state = f.pos_from_state;
-      a.state = c->st; a.ws = c->gemm_ws; a.tickets = c->tickets; a.status = c->st;
+      a.state = c->st; a.ws = c->gemm_ws; a.status = c->st;
       CK(launch_gemm_tc(m, a, BN, s));
-    } else {
-      dim3 g1((3 * D + 63) / 64, (rows + 63) / 64);
-      // three column blocks of one [rows, 3D] output
-      for (int j = 0; j < 3; ++j) {
-        dim3 g((D + 63) / 64, (rows + 63) / 64);
-        gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 1 + j), c->qkv32 + j * D,
-                                          rows, D, D, 3 * D, 0);
-      }
-      (void)g1;
-      CK(cudaGetLastError());
-      rope_cache_f32_kernel<<<rows, 256, 0, s>>>(c->qkv32, (float*)c->q, (float*)c->kc_layer(l),
-                                                  (float*)c->vc_layer(l), c->rope_cos, c->rope_sin, rows, D, hd, rm,
-                                                  c->st);
-      CK(cudaGetLastError());
     }
     // a3: attention over the dual cache
-    if (c->bf16) {
+    {
       AttnArgs aa{};
       aa.q = (const __nv_bfloat16*)c->q;
       aa.k = (const __nv_bfloat16*)c->kc_layer(l);
@@ -419,75 +425,106 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       aa.q_tiles = ap.q_tiles; aa.splits = ap.splits; aa.chunks_per_split = ap.cps;
       aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
       CK(launch_attention(aa, f.batch, s));
-    } else {
-      AttnF32Args aa{(const float*)c->q, (const float*)c->kc_layer(l), (const float*)c->vc_layer(l),
-                     (float*)c->attn_o, D, H, hd, f.L, f.rows_per_seq, 1.f / sqrtf((float)hd)};
-      dim3 g(rows, H);
-      attn_f32_kernel<<<g, 128, (size_t)(f.L + hd) * sizeof(float), s>>>(aa);
     }
-    CK(cudaGetLastError());
-    // a4: O projection + residual
-    if (c->bf16) {
+    // a4: O projection + residual, fused with the FFN norm
+    {
       GemmMaps m = mo;
       m.a[0] = c->m_wo[l];
       GemmArgs a{};
       a.M = rows; a.N = D; a.K = D; a.n_tiles = D / 128; a.a_mode = A_SINGLE;
-      a.resid = c->h; a.ws = c->gemm_ws; a.tickets = c->tickets; a.status = c->st; a.state = c->st;
-      CK(launch_gemm_tc(m, a, BN, s));
-    } else {
-      dim3 g((D + 63) / 64, (rows + 63) / 64);
-      gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->attn_o, (const float*)c->LW(l, 4), c->h, rows, D, D, D, 1);
-      CK(cudaGetLastError());
+      a.resid = c->h; a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
+      CK(launch_gemm_tc(m, a, BN, s, true));
+      CK(launchk(resid_norm_kernel<__nv_bfloat16>, dim3(rows), dim3(nthr), 0, s, 1, c->h,
+                 (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, D, d.rms_eps, f.rows_per_seq, f.L, 0,
+                 (const DevState*)c->st, resid_plan(a, BN, c->gemm_ws)));
     }
-    // a5: RMSNorm -> SwiGLU FFN + residual
-    if (c->bf16)
-      rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<rows, 256, 0, s>>>(
-          c->h, (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, rows, D, d.rms_eps, 0, rm, c->st);
-    else
-      rmsnorm_kernel<float, float><<<rows, 256, 0, s>>>(c->h, (const float*)c->LW(l, 5), (float*)c->xn, rows, D,
-                                                        d.rms_eps, 0, rm, c->st);
-    CK(cudaGetLastError());
-    if (c->bf16) {
+    // a5: SwiGLU FFN (gate/up with the SiLU*up epilogue, down + residual)
+    {
       GemmMaps m = mx;
       m.a[0] = c->m_wg[l];
       m.a[1] = c->m_wu[l];
       GemmArgs a{};
       a.M = rows; a.N = F; a.K = D; a.n_tiles = F / 64; a.a_mode = A_PAIR;
       a.out_bf16 = (__nv_bfloat16*)c->act; a.ldo = F;
-      a.ws = c->gemm_ws; a.tickets = c->tickets; a.status = c->st; a.state = c->st;
+      a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
       CK(launch_gemm_tc(m, a, BN, s));
       GemmMaps m2 = mact;
       m2.a[0] = c->m_wd[l];
       GemmArgs b{};
       b.M = rows; b.N = D; b.K = F; b.n_tiles = D / 128; b.a_mode = A_SINGLE;
-      b.resid = c->h; b.ws = c->gemm_ws; b.tickets = c->tickets; b.status = c->st; b.state = c->st;
-      CK(launch_gemm_tc(m2, b, BN, s));
-    } else {
-      dim3 g((F + 63) / 64, (rows + 63) / 64);
-      gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 6), c->gu32, rows, F, D, 2 * F, 0);
-      gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 7), c->gu32 + F, rows, F, D, 2 * F,
-                                        0);
-      swiglu_f32_kernel<<<256, 256, 0, s>>>(c->gu32, (float*)c->act, rows, F);
-      dim3 g2((D + 63) / 64, (rows + 63) / 64);
-      gemm_f32_kernel<<<g2, 256, 0, s>>>((const float*)c->act, (const float*)c->LW(l, 8), c->h, rows, D, F, D, 1);
-      CK(cudaGetLastError());
+      b.resid = c->h; b.ws = c->gemm_ws; b.status = c->st; b.state = c->st;
+      CK(launch_gemm_tc(m2, b, BN, s, true));
+      const bool last = l + 1 == d.n_layers;
+      const void* gn = last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0);
+      // after the last layer only the block rows go on (to the LM head)
+      const int nrows = last ? f.batch * f.B : rows;
+      const int gather = last && f.refresh ? 1 : 0;
+      CK(launchk(resid_norm_kernel<__nv_bfloat16>, dim3(nrows), dim3(nthr), 0, s, 1, c->h,
+                 (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps, f.B, f.L, gather,
+                 (const DevState*)c->st, resid_plan(b, BN, c->gemm_ws)));
     }
   }
+  return DINFER_OK;
+}
 
-  // a6: final norm of the block rows (gathered from the full sequence at a refresh)
-  const int brows = f.batch * f.B;
-  RowMap rb{f.B, f.L, 1};
-  const int gather = f.refresh ? 1 : 0;
-  const void* gfin = c->W(1 + 9 * d.n_layers);
-  if (c->bf16)
-    rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<brows, 256, 0, s>>>(
-        c->h, (const __nv_bfloat16*)gfin, (__nv_bfloat16*)c->xn, brows, D, d.rms_eps, gather, rb, c->st);
-  else
-    rmsnorm_kernel<float, float><<<brows, 256, 0, s>>>(c->h, (const float*)gfin, (float*)c->xn, brows, D, d.rms_eps,
-                                                       gather, rb, c->st);
-  CK(cudaGetLastError());
+// Enqueue one forward over f.rows rows, final norm of the block rows, LM head,
+// decode and (optionally) the commit.  Works eagerly or under stream capture.
+dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
+  const dinfer_model_desc& d = c->desc;
+  const int D = d.d_model, F = d.ffn, H = d.n_heads, hd = d.head_dim;
+  const int rows = f.rows;
+  RowMap rm{f.rows_per_seq, f.L, f.pos_from_state};
+  if (c->bf16) {
+    dinfer_status st = enqueue_layers_bf16(c, f, s);
+    if (st != DINFER_OK) return st;
+  } else {
+    // fp32 models: SIMT FFMA GEMMs and separate elementwise kernels
+    embed_kernel<float><<<rows, 256, 0, s>>>((const float*)c->W(0), c->ids, c->h, rows, D, d.vocab, rm, c->st);
+    CK(cudaGetLastError());
+    for (int l = 0; l < d.n_layers; ++l) {
+      rmsnorm_kernel<float, float><<<rows, 256, 0, s>>>(c->h, (const float*)c->LW(l, 0), (float*)c->xn, rows, D,
+                                                        d.rms_eps, 0, rm, c->st);
+      for (int j = 0; j < 3; ++j) {
+        dim3 g((D + 63) / 64, (rows + 63) / 64);
+        gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 1 + j), c->qkv32 + j * D,
+                                          rows, D, D, 3 * D, 0);
+      }
+      rope_cache_f32_kernel<<<rows, 256, 0, s>>>(c->qkv32, (float*)c->q, (float*)c->kc_layer(l),
+                                                  (float*)c->vc_layer(l), c->rope_cos, c->rope_sin, rows, D, hd, rm,
+                                                  c->st);
+      AttnF32Args aa{(const float*)c->q, (const float*)c->kc_layer(l), (const float*)c->vc_layer(l),
+                     (float*)c->attn_o, D, H, hd, f.L, f.rows_per_seq, 1.f / sqrtf((float)hd)};
+      attn_f32_kernel<<<dim3(rows, H), 128, (size_t)(f.L + hd) * sizeof(float), s>>>(aa);
+      {
+        dim3 g((D + 63) / 64, (rows + 63) / 64);
+        gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->attn_o, (const float*)c->LW(l, 4), c->h, rows, D, D, D,
+                                          1);
+      }
+      rmsnorm_kernel<float, float><<<rows, 256, 0, s>>>(c->h, (const float*)c->LW(l, 5), (float*)c->xn, rows, D,
+                                                        d.rms_eps, 0, rm, c->st);
+      {
+        dim3 g((F + 63) / 64, (rows + 63) / 64);
+        gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 6), c->gu32, rows, F, D,
+                                          2 * F, 0);
+        gemm_f32_kernel<<<g, 256, 0, s>>>((const float*)c->xn, (const float*)c->LW(l, 7), c->gu32 + F, rows, F, D,
+                                          2 * F, 0);
+        swiglu_f32_kernel<<<256, 256, 0, s>>>(c->gu32, (float*)c->act, rows, F);
+        dim3 g2((D + 63) / 64, (rows + 63) / 64);
+        gemm_f32_kernel<<<g2, 256, 0, s>>>((const float*)c->act, (const float*)c->LW(l, 8), c->h, rows, D, F, D, 1);
+      }
+      CK(cudaGetLastError());
+    }
+    // a6: final norm of the block rows (gathered from the full sequence at a refresh)
+    const int brows = f.batch * f.B;
+    RowMap rb{f.B, f.L, 1};
+    rmsnorm_kernel<float, float><<<brows, 256, 0, s>>>(c->h, (const float*)c->W(1 + 9 * d.n_layers),
+                                                       (float*)c->xn, brows, D, d.rms_eps, f.refresh ? 1 : 0, rb,
+                                                       c->st);
+    CK(cudaGetLastError());
+  }
 
   // a6 + a7: LM head, online softmax, threshold commit
+  const int brows = f.batch * f.B;
   DecodeArgs dec{};
   dec.M = brows; dec.batch = f.batch; dec.L = f.L; dec.B = f.B;
   dec.threshold = f.threshold; dec.commit = f.commit;
@@ -765,14 +802,6 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
   CKC(cudaMallocHost((void**)&c->st_host, sizeof(DevState)));
   const int G = num_sms();
   AL(c->gemm_ws, gemm_ws_floats(G) * 4);
-  // tickets: the largest tile count of any GEMM (rows up to max_rows, token tile >= 64)
-  {
-    const size_t mt = (c->max_rows + 63) / 64;
-    size_t nt = std::max<size_t>(3 * D / 128, F / 64);
-    c->n_tickets = mt * nt + 1;
-    AL(c->tickets, c->n_tickets * 4);
-    CKC(cudaMemset(c->tickets, 0, c->n_tickets * 4));
-  }
   AL(c->lm_part, (size_t)G * 1024 * sizeof(SoftmaxState));
   AL(c->lm_ticket, 16);
   CKC(cudaMemset(c->lm_ticket, 0, 16));
@@ -1016,7 +1045,7 @@ dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_
   GemmArgs a{};
   a.M = M; a.N = N; a.K = K; a.n_tiles = N / 128; a.a_mode = A_SINGLE;
   a.out_f32 = Y; a.ldo = N;
-  a.ws = reinterpret_cast<float*>(o.data); a.tickets = o.tickets; a.status = o.st; a.state = o.st;
+  a.ws = reinterpret_cast<float*>(o.data); a.status = o.st; a.state = o.st;
   CK(launch_gemm_tc(m, a, BN, reinterpret_cast<cudaStream_t>(stream)));
   return DINFER_OK;
 }

@@ -63,9 +63,10 @@ struct GemmArgs {
   int seq_len;             // L (cache stride in positions)
   int pos_from_state;      // 1: position = block_start + local row; 0: local row
   const DevState* state;
-  // stream-K fixup
+  // stream-K partial tiles
   float* ws;               // [grid][2][BN * 128] fp32
-  int* tickets;            // [tiles], zero between launches
+  int grid;                // CTAs of the GEMM launch (fixes the unit ranges)
+  int slot_tok_major;      // partial slots [BN tokens][128 rows] (residual GEMMs), else [128 rows][BN]
   DevState* status;
 };
 
@@ -86,18 +87,18 @@ struct GemmCfg {
 // schedule: contiguous unit ranges per CTA
 // ---------------------------------------------------------------------------
 struct Sched {
-  long long U;  // total units
-  int KT;       // units per tile (k-steps) in stream-K mode, 1 otherwise
-  int G;
-  __device__ __forceinline__ long long start(int c) const { return (U * c) / G; }
-  __device__ __forceinline__ int owner(long long u) const { return (int)(((u + 1) * G - 1) / U); }
+  // 32-bit: the launcher guarantees U * G < 2^32
+  unsigned U;  // total units
+  unsigned KT; // units per tile (k-steps) in stream-K mode, 1 otherwise
+  unsigned G;
+  __host__ __device__ __forceinline__ unsigned start(unsigned c) const { return (U * c) / G; }
+  __host__ __device__ __forceinline__ int owner(unsigned u) const { return (int)(((u + 1) * G - 1) / U); }
 };
 
 template <int BN>
-__device__ __forceinline__ void load_stage(const GemmMaps& maps, const GemmArgs& a, uint8_t* stage, uint64_t* bar,
-                                           int nt, int mt, int k, uint64_t pol_w, uint64_t pol_x) {
+__device__ __forceinline__ void load_stage_a(const GemmMaps& maps, const GemmArgs& a, uint8_t* stage, uint64_t* bar,
+                                             int nt, int k, uint64_t pol_w) {
   uint8_t* sa = stage;
-  uint8_t* sb = stage + GemmCfg<BN>::kStageA;
   const int kx = k * 64;
   if (a.a_mode == A_PAIR) {
     tma_load_2d(sa, &maps.a[0], bar, kx, nt * 64, pol_w);
@@ -108,7 +109,11 @@ __device__ __forceinline__ void load_stage(const GemmMaps& maps, const GemmArgs&
   } else {
     tma_load_2d(sa, &maps.a[0], bar, kx, nt * 128, pol_w);
   }
-  tma_load_2d(sb, &maps.b, bar, kx, mt * BN, pol_x);
+}
+template <int BN>
+__device__ __forceinline__ void load_stage_b(const GemmMaps& maps, uint8_t* stage, uint64_t* bar, int mt, int k,
+                                             uint64_t pol_x) {
+  tma_load_2d(stage + GemmCfg<BN>::kStageA, &maps.b, bar, k * 64, mt * BN, pol_x);
 }
 
 // One 16-column chunk of the finished accumulator for output feature row
@@ -272,12 +277,31 @@ struct Pipe {
 };
 
 // TMA producer loop (one elected thread of warp 0).
+// TMA producer loop (one elected thread of warp 0).  The weight tiles of the
+// first pipeline stages do not depend on the preceding kernel, so they are
+// requested before griddepcontrol.wait; the activation tiles after it.
 template <int BN>
 __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArgs& a, const SegList& sl,
                                              const Pipe& p, int m_tiles) {
   using C = GemmCfg<BN>;
   const uint64_t pol_w = l2_policy_evict_first();
   const uint64_t pol_x = l2_policy_evict_last();
+  // phase 1: weights of the first kStages stages
+  int pre_mt[C::kStages], pre_k[C::kStages];
+  int pre = 0;
+  for (int j = 0; j < sl.nseg && pre < C::kStages; ++j) {
+    int t, kb, ke;
+    sl.seg(j, t, kb, ke);
+    for (int k = kb; k < ke && pre < C::kStages; ++k, ++pre) {
+      mbar_arrive_expect_tx(&p.full[pre], C::kStage);
+      load_stage_a<BN>(maps, a, p.stages + pre * C::kStage, &p.full[pre], t / m_tiles, k, pol_w);
+      pre_mt[pre] = t % m_tiles;
+      pre_k[pre] = k;
+    }
+  }
+  pdl_wait();
+  for (int i = 0; i < pre; ++i) load_stage_b<BN>(maps, p.stages + i * C::kStage, &p.full[i], pre_mt[i], pre_k[i], pol_x);
+  // phase 2: the rest of the pipeline
   uint32_t it = 0;
   for (int j = 0; j < sl.nseg && !*p.abort_flag; ++j) {
     int t, kb, ke;
@@ -285,11 +309,13 @@ __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArg
     const int nt = t / m_tiles, mt = t % m_tiles;
     bool ok = true;
     for (int k = kb; k < ke; ++k, ++it) {
+      if (it < (uint32_t)pre) continue;
       const int s = it % C::kStages;
       const uint32_t round = it / C::kStages;
       if (!mbar_wait(&p.empty[s], (round & 1) ^ 1, p.abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(&p.full[s], C::kStage);
-      load_stage<BN>(maps, a, p.stages + s * C::kStage, &p.full[s], nt, mt, k, pol_w, pol_x);
+      load_stage_a<BN>(maps, a, p.stages + s * C::kStage, &p.full[s], nt, k, pol_w);
+      load_stage_b<BN>(maps, p.stages + s * C::kStage, &p.full[s], mt, k, pol_x);
     }
     if (!ok) break;
   }
@@ -383,7 +409,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   sc.G = gridDim.x;
   const int tiles = a.m_tiles * a.n_tiles;
   sc.KT = a.stream_k ? a.k_tiles : 1;
-  sc.U = (long long)tiles * sc.KT;
+  sc.U = (unsigned)tiles * sc.KT;
   SegList sl;
   sl.init(a.stream_k, a.k_tiles, sc.start(blockIdx.x), sc.start(blockIdx.x + 1));
 
@@ -396,6 +422,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // one wave (<= one CTA per SM): the next kernel may start launching now
+  if (threadIdx.x == 0) pdl_trigger();
 
   if (warp == 0) {
     if (elect_one_sync()) run_producer<BN>(maps, a, sl, p, a.m_tiles);
@@ -403,6 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (elect_one_sync()) run_mma<BN>(sl, p, tmem_base);
   } else {
     // ------------------------------ epilogue ------------------------------
+    pdl_wait();  // global writes only after the preceding kernel completed
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;          // output feature row inside the tile
     for (int j = 0; j < sl.nseg; ++j) {
@@ -419,15 +448,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // partial tile: slot 0 holds this CTA's part of its first tile, slot 1
         // of its last; layout [row][BN] so each thread moves whole float4s
         const int which = (t == sl.tf) ? 0 : 1;
-        float4* slot = reinterpret_cast<float4*>(a.ws + ((size_t)blockIdx.x * 2 + which) * (BN * 128)) +
-                       (size_t)row * (BN / 4);
+        float* base = a.ws + ((size_t)blockIdx.x * 2 + which) * (BN * 128);
+        if (a.slot_tok_major) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          float v[16];
-          tmem_ld16(tbase + c * 16, v);
+          for (int c = 0; c < BN / 16; ++c) {
+            float v[16];
+            tmem_ld16(tbase + c * 16, v);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            slot[c * 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 16; ++i) base[(size_t)(c * 16 + i) * 128 + row] = v[i];
+          }
+        } else {
+          float4* slot = reinterpret_cast<float4*>(base) + (size_t)row * (BN / 4);
+#pragma unroll 1
+          for (int c = 0; c < BN / 16; ++c) {
+            float v[16];
+            tmem_ld16(tbase + c * 16, v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              slot[c * 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
         }
         tc_fence_before();
         mbar_arrive(&p.tempty[acc]);
@@ -457,19 +496,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // of the GEMM grid whose unit ranges overlap it) in CTA order, then applies
 // the GEMM's epilogue.  Tiles owned whole by one CTA were finished by it.
 template <int BN>
-__global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a, int gemm_grid) {
+__global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
   __shared__ float xchg[128 * 17];
   __shared__ int slot_idx[32];
+  pdl_wait();
   const int chunks = BN / 16;
   const int t = blockIdx.x / chunks, c = blockIdx.x % chunks;
   Sched sc;
-  sc.G = gemm_grid;
+  sc.G = a.grid;
   sc.KT = a.k_tiles;
-  sc.U = (long long)a.m_tiles * a.n_tiles * a.k_tiles;
-  const long long tu0 = (long long)t * a.k_tiles;
+  sc.U = (unsigned)(a.m_tiles * a.n_tiles) * a.k_tiles;
+  const unsigned tu0 = (unsigned)t * a.k_tiles;
   const int c_first = sc.owner(tu0);
   const int c_last = sc.owner(tu0 + a.k_tiles - 1);
-  if (c_first == c_last) return;  // whole tile: done by the GEMM
+  if (c_first == c_last) {  // whole tile: done by the GEMM
+    pdl_trigger();
+    return;
+  }
   const int nc = c_last - c_first + 1;
   const int row = threadIdx.x;
   if (row < nc && row < 32) {
@@ -504,6 +547,111 @@ __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a, int
   }
   const int nt = t / a.m_tiles, mt = t % a.m_tiles;
   epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
+  pdl_trigger();
+}
+
+// Residual GEMM finish fused with the next RMSNorm.  The O and down
+// projections leave tiles shared by several CTAs as token-major fp32 partials
+// (whole tiles were already added to h by the GEMM).  One CTA per output row r
+// (token src(r)), d / 16 threads, 16 consecutive features per thread (one
+// weight tile of 128 features per 8 threads):
+//   h[src] += sum of the partials of every shared tile, in CTA order;
+//   out[r] = bf16(h[src] / sqrt(mean(h[src]^2) + eps) * g).
+struct ResidPlan {
+  const float* ws;
+  int m_tiles, n_tiles, k_tiles, grid, BN;
+};
+
+template <typename Tg>
+__global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, const Tg* __restrict__ g,
+                                                         __nv_bfloat16* __restrict__ out, int d, float eps,
+                                                         int rows_per_seq, int L, int pos_from_state,
+                                                         const DevState* st, ResidPlan rp) {
+  __shared__ float red[32];
+  pdl_wait();
+  const int r = blockIdx.x;
+  size_t src = r;
+  if (pos_from_state) {  // gather the block rows of a full-sequence residual
+    const int bi = r / rows_per_seq;
+    src = (size_t)bi * L + st->block_start + (r - bi * rows_per_seq);
+  }
+  const int f0 = threadIdx.x * 16;
+  float* hp = h + src * d + f0;
+  float x[16];
+  {
+    const float4* h4 = reinterpret_cast<const float4*>(hp);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 t = h4[i];
+      x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
+    }
+  }
+  // partial tiles of the residual GEMM for (token src, features f0..f0+15)
+  const int m = (int)src;
+  const int mt = m / rp.BN, ml = m - mt * rp.BN;
+  const int nt = f0 / 128, fl = f0 - nt * 128;
+  const int t = nt * rp.m_tiles + mt;
+  Sched sc;
+  sc.G = rp.grid;
+  sc.KT = rp.k_tiles;
+  sc.U = (unsigned)(rp.m_tiles * rp.n_tiles) * rp.k_tiles;
+  const unsigned tu0 = (unsigned)t * rp.k_tiles;
+  const int c_first = sc.owner(tu0), c_last = sc.owner(tu0 + rp.k_tiles - 1);
+  if (c_first != c_last) {
+    for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+      float4 buf[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cc = c0 + q;
+        if (cc <= c_last) {
+          const int w = ((unsigned)t == sc.start(cc) / sc.KT) ? 0 : 1;
+          const float4* sp = reinterpret_cast<const float4*>(rp.ws + ((size_t)cc * 2 + w) * (rp.BN * 128) +
+                                                             (size_t)ml * 128 + fl);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) buf[q][i] = __ldcg(sp + i);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c0 + q <= c_last)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            x[4 * i] += buf[q][i].x;
+            x[4 * i + 1] += buf[q][i].y;
+            x[4 * i + 2] += buf[q][i].z;
+            x[4 * i + 3] += buf[q][i].w;
+          }
+    }
+    float4* h4 = reinterpret_cast<float4*>(hp);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / (float)d + eps);
+  uint4 o[2];
+  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a0 = x[2 * i] * inv * (float)g[f0 + 2 * i];
+    const float a1 = x[2 * i + 1] * inv * (float)g[f0 + 2 * i + 1];
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+    ow[i] = *reinterpret_cast<uint32_t*>(&b2);
+  }
+  uint4* op = reinterpret_cast<uint4*>(out + (size_t)r * d + f0);
+  op[0] = o[0];
+  op[1] = o[1];
+  pdl_trigger();
 }
 
 }  // namespace dinfer

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   Sched sc;
   sc.G = gridDim.x;
   sc.KT = 1;
-  sc.U = (long long)ga.m_tiles * ga.n_tiles;
+  sc.U = (unsigned)(ga.m_tiles * ga.n_tiles);
   SegList sl;
   sl.init(0, ga.k_tiles, sc.start(blockIdx.x), sc.start(blockIdx.x + 1));
 
@@ -72,12 +72,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) pdl_trigger();
 
   if (warp == 0) {
     if (elect_one_sync()) run_producer<BN>(maps, ga, sl, p, ga.m_tiles);
   } else if (warp == 1) {
     if (elect_one_sync()) run_mma<BN>(sl, p, tmem_base);
   } else {
+    pdl_wait();
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int ep_tid = threadIdx.x - 64;

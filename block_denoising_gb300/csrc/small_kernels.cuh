@@ -23,6 +23,7 @@ struct RowMap {
 template <typename T>
 __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict__ ids, float* __restrict__ h,
                              int rows, int d, int vocab, RowMap rm, DevState* st) {
+  pdl_wait();
   const int r = blockIdx.x;
   if (r >= rows) return;
   int id = ids[rm.seq_index(r, st)];
@@ -33,6 +34,7 @@ __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict_
   const T* src = E + (size_t)id * d;
   float* dst = h + (size_t)r * d;
   for (int i = threadIdx.x; i < d; i += blockDim.x) dst[i] = (float)src[i];
+  pdl_trigger();
 }
 
 template <typename T>
@@ -72,6 +74,7 @@ template <typename Tg, typename To>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ h, const Tg* __restrict__ g,
                                                       To* __restrict__ out, int rows, int d, float eps, int gather,
                                                       RowMap rm, const DevState* st) {
+  pdl_wait();
   const int r = blockIdx.x;
   if (r >= rows) return;
   const size_t src = gather ? rm.seq_index(r, st) : (size_t)r;
@@ -118,6 +121,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
   } else {
     for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = from_float<To>(x[i] * inv * (float)g[i]);
   }
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
