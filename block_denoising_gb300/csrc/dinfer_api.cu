@@ -137,34 +137,60 @@ bool set_smem_attrs() {
 // Stream-K fixup workspace: floats per CTA slot pair and the ticket count.
 size_t gemm_ws_floats(int grid) { return (size_t)grid * 2 * 256 * 128; }
 
-// Launch the tensor-core GEMM (templated on the token tile).  Tiles shared
-// by several CTAs are finished by the split-K fixup kernel, or -- residual
-// GEMMs with defer_resid -- by the following resid_norm_kernel.
+// GEMM schedule.  With enough output tiles to keep most SMs streaming
+// (a single SM pulls ~80-90 GB/s, so ~80 busy SMs saturate HBM), every CTA
+// owns whole tiles and applies the epilogue itself.  With few tiles (the
+// d_model-wide O and down projections of a block), the (tile, k-step) units
+// are split evenly over the SMs (stream-K) and shared tiles are finished by
+// the split-K fixup kernel, or -- residual GEMMs with defer_resid -- by the
+// following resid_norm_kernel.
+struct GemmSched {
+  int stream_k, grid;
+};
+GemmSched gemm_schedule(int M, int n_tiles, int K, int BN) {
+  const int m_tiles = (M + BN - 1) / BN;
+  const long long tiles = (long long)m_tiles * n_tiles;
+  const int k_tiles = K / 64;
+  const int sms = num_sms();
+  GemmSched g;
+  if (tiles * 10 >= (long long)sms * 6) {
+    const long long per = (tiles + sms - 1) / sms;
+    g.stream_k = 0;
+    g.grid = (int)((tiles + per - 1) / per);
+  } else {
+    // at least k_tiles / 14 units per CTA, so that at most 16 CTAs share a tile
+    const long long units = tiles * k_tiles;
+    const long long min_units = (k_tiles + 13) / 14;
+    g.stream_k = 1;
+    g.grid = (int)std::max<long long>(1, std::min<long long>(sms, units / min_units));
+  }
+  return g;
+}
+
 cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s, bool defer_resid = false) {
   a.m_tiles = (a.M + BN - 1) / BN;
   a.k_tiles = a.K / 64;
-  a.stream_k = 1;
-  // every CTA must own at least one (tile, k-step) unit, and at least
-  // k_tiles / 14 of them so that at most 16 CTAs share a tile
-  const long long units = (long long)a.m_tiles * a.n_tiles * a.k_tiles;
-  const long long min_units = (a.k_tiles + 13) / 14;
-  a.grid = (int)std::max<long long>(1, std::min<long long>(num_sms(), units / min_units));
+  const GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN);
+  a.stream_k = gs.stream_k;
+  a.grid = gs.grid;
+  const long long units = (long long)a.m_tiles * a.n_tiles * (a.stream_k ? a.k_tiles : 1);
   if ((unsigned long long)units * (unsigned long long)a.grid >= (1ull << 32)) return cudaErrorInvalidValue;
   a.slot_tok_major = defer_resid ? 1 : 0;
   const int tiles = a.m_tiles * a.n_tiles;
+  const bool fixup = a.stream_k && !defer_resid;
   cudaError_t e = cudaSuccess;
   switch (BN) {
     case 64:
       e = launchk(gemm_tc_kernel<64>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<64>::kSmem, s, 1, maps, a);
-      if (e == cudaSuccess && !defer_resid) e = launchk(splitk_fixup_kernel<64>, dim3(tiles * 4), dim3(128), 0, s, 1, a);
+      if (e == cudaSuccess && fixup) e = launchk(splitk_fixup_kernel<64>, dim3(tiles * 4), dim3(128), 0, s, 1, a);
       break;
     case 128:
       e = launchk(gemm_tc_kernel<128>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<128>::kSmem, s, 1, maps, a);
-      if (e == cudaSuccess && !defer_resid) e = launchk(splitk_fixup_kernel<128>, dim3(tiles * 8), dim3(128), 0, s, 1, a);
+      if (e == cudaSuccess && fixup) e = launchk(splitk_fixup_kernel<128>, dim3(tiles * 8), dim3(128), 0, s, 1, a);
       break;
     default:
       e = launchk(gemm_tc_kernel<256>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<256>::kSmem, s, 1, maps, a);
-      if (e == cudaSuccess && !defer_resid) e = launchk(splitk_fixup_kernel<256>, dim3(tiles * 16), dim3(128), 0, s, 1, a);
+      if (e == cudaSuccess && fixup) e = launchk(splitk_fixup_kernel<256>, dim3(tiles * 16), dim3(128), 0, s, 1, a);
       break;
   }
   return e;
@@ -177,9 +203,9 @@ ResidPlan resid_plan(const GemmArgs& a, int BN, const float* ws) {
   p.m_tiles = (a.M + BN - 1) / BN;
   p.n_tiles = a.n_tiles;
   p.k_tiles = a.K / 64;
-  const long long units = (long long)p.m_tiles * p.n_tiles * p.k_tiles;
-  const long long min_units = (p.k_tiles + 13) / 14;
-  p.grid = (int)std::max<long long>(1, std::min<long long>(num_sms(), units / min_units));
+  const GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN);
+  p.stream_k = gs.stream_k;
+  p.grid = gs.grid;
   return p;
 }
 

@@ -560,6 +560,7 @@ __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
 struct ResidPlan {
   const float* ws;
   int m_tiles, n_tiles, k_tiles, grid, BN;
+  int stream_k;  // 0: the GEMM owned whole tiles, nothing left to add
 };
 
 template <typename Tg>
@@ -596,7 +597,8 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
   sc.KT = rp.k_tiles;
   sc.U = (unsigned)(rp.m_tiles * rp.n_tiles) * rp.k_tiles;
   const unsigned tu0 = (unsigned)t * rp.k_tiles;
-  const int c_first = sc.owner(tu0), c_last = sc.owner(tu0 + rp.k_tiles - 1);
+  const int c_first = rp.stream_k ? sc.owner(tu0) : 0;
+  const int c_last = rp.stream_k ? sc.owner(tu0 + rp.k_tiles - 1) : 0;
   if (c_first != c_last) {
     for (int c0 = c_first; c0 <= c_last; c0 += 4) {
       float4 buf[4][4];

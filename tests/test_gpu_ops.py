@@ -53,6 +53,8 @@ GEMM_SHAPES = [
     (200, 640, 320),       # token tile 256, ragged
     (1536, 1024, 512),     # refresh-like rows: several token tiles
     (512, 4096, 4096),     # batch-16 block rows
+    (1536, 12288, 512),    # whole-tile schedule, several tiles per CTA
+    (200, 24576, 256),     # whole-tile schedule, ragged token tile
 ]
 
 
