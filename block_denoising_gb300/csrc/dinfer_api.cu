@@ -153,10 +153,14 @@ GemmSched gemm_schedule(int M, int n_tiles, int K, int BN) {
   const int k_tiles = K / 64;
   const int sms = num_sms();
   GemmSched g;
-  if (tiles * 10 >= (long long)sms * 6) {
-    const long long per = (tiles + sms - 1) / sms;
+  const long long per = (tiles + sms - 1) / sms;
+  const long long wgrid = (tiles + per - 1) / per;
+  // weight streaming (few token rows): ~80 busy SMs already saturate HBM;
+  // tensor-bound (many rows): whole tiles only if they keep >= 90% of the SMs busy
+  const bool whole = M <= 128 ? tiles * 10 >= (long long)sms * 6 : tiles * 10 >= (long long)sms * per * 9;
+  if (whole) {
     g.stream_k = 0;
-    g.grid = (int)((tiles + per - 1) / per);
+    g.grid = (int)wgrid;
   } else {
     // at least k_tiles / 14 units per CTA, so that at most 16 CTAs share a tile
     const long long units = tiles * k_tiles;
