@@ -41,7 +41,8 @@ constexpr int kHd = 128;
 constexpr int kKeyChunk = 64;
 // 64 rows x 256 B per tile, 16-byte chunks XOR-swizzled by (row & 7)
 constexpr int kAttnTileBytes = 64 * kHd * 2;
-constexpr int kAttnSmem = kAttnTileBytes * 5;  // Q + 2 x (K, V)
+constexpr int kAttnStages = 3;                                     // K/V chunks in flight
+constexpr int kAttnSmem = kAttnTileBytes * (1 + 2 * kAttnStages);  // Q + stages x (K, V): 112 KB, 2 CTAs/SM
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a 64x128 bf16 tile
   return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4));
@@ -95,8 +96,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     attn_bf16_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   const uint32_t s_q = smem_u32(sm);
-  const uint32_t s_k[2] = {s_q + kAttnTileBytes, s_q + 3 * kAttnTileBytes};
-  const uint32_t s_v[2] = {s_q + 2 * kAttnTileBytes, s_q + 4 * kAttnTileBytes};
+  // stage i: K at s_q + (1 + 2i) tiles, V at s_q + (2 + 2i) tiles
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int qt = blockIdx.x % a.q_tiles;
@@ -114,15 +114,21 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int c_end = min(n_chunks, c_begin + a.chunks_per_split);
 
   pdl_wait();
+  auto s_k = [&](int st) { return s_q + (uint32_t)(1 + 2 * st) * kAttnTileBytes; };
+  auto s_v = [&](int st) { return s_q + (uint32_t)(2 + 2 * st) * kAttnTileBytes; };
+  auto load_chunk = [&](int c, int st) {
+    const int k0 = c * kKeyChunk;
+    load_tile_async(s_k(st), kg + (size_t)k0 * a.d, a.d, min(kKeyChunk, a.L - k0));
+    load_tile_async(s_v(st), vg + (size_t)k0 * a.d, a.d, min(kKeyChunk, a.L - k0));
+  };
+  // prologue: group 0 = Q + chunk 0, groups 1 .. kAttnStages-2 = the next chunks
   load_tile_async(s_q, qg, a.d, q_valid);
-  cp_async_commit();
-  if (c_begin < c_end) {
-    const int k0 = c_begin * kKeyChunk;
-    load_tile_async(s_k[0], kg + (size_t)k0 * a.d, a.d, min(kKeyChunk, a.L - k0));
-    load_tile_async(s_v[0], vg + (size_t)k0 * a.d, a.d, min(kKeyChunk, a.L - k0));
+#pragma unroll
+  for (int i = 0; i < kAttnStages - 1; ++i) {
+    if (c_begin + i < c_end) load_chunk(c_begin + i, i);
+    cp_async_commit();
   }
-  cp_async_commit();
-  cp_async_wait<1>();
+  cp_async_wait<kAttnStages - 2>();
   __syncthreads();
 
   // Q fragments for this warp's 16 rows, all 8 k-steps of hd
@@ -141,14 +147,12 @@ __global__ void __launch_bounds__(kAttnThreads)
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
 
   for (int c = c_begin; c < c_end; ++c) {
-    const int buf = (c - c_begin) & 1;
-    if (c + 1 < c_end) {
-      const int k1 = (c + 1) * kKeyChunk;
-      load_tile_async(s_k[buf ^ 1], kg + (size_t)k1 * a.d, a.d, min(kKeyChunk, a.L - k1));
-      load_tile_async(s_v[buf ^ 1], vg + (size_t)k1 * a.d, a.d, min(kKeyChunk, a.L - k1));
-    }
+    const int buf = (c - c_begin) % kAttnStages;
+    // refill the stage consumed in the previous iteration with chunk c + kAttnStages - 1
+    const int cn = c + kAttnStages - 1;
+    if (cn < c_end) load_chunk(cn, (cn - c_begin) % kAttnStages);
     cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<kAttnStages - 1>();
     __syncthreads();
 
     // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kAttnThreads)
         const int key = kp * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int chunk = ks * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(s_k[buf] + swz(key, chunk), b0, b1, b2, b3);
+        ldsm_x4(s_k(buf) + swz(key, chunk), b0, b1, b2, b3);
         mma_bf16_16816(s[2 * kp], qf[ks], b0, b1);
         mma_bf16_16816(s[2 * kp + 1], qf[ks], b2, b3);
       }
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(kAttnThreads)
         const int key = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
         const int chunk = np * 2 + (lane >> 4);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(s_v[buf] + swz(key, chunk), b0, b1, b2, b3);
+        ldsm_x4_t(s_v(buf) + swz(key, chunk), b0, b1, b2, b3);
         mma_bf16_16816(oacc[2 * np], pf[ks], b0, b1);
         mma_bf16_16816(oacc[2 * np + 1], pf[ks], b2, b3);
       }

@@ -284,7 +284,9 @@ template <int BN>
 __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArgs& a, const SegList& sl,
                                              const Pipe& p, int m_tiles) {
   using C = GemmCfg<BN>;
-  const uint64_t pol_w = l2_policy_evict_first();
+  // weight tiles used by a single token tile stream through L2 once; with
+  // several token tiles the following tiles re-read them from L2
+  const uint64_t pol_w = m_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
   const uint64_t pol_x = l2_policy_evict_last();
   // phase 1: weights of the first kStages stages
   int pre_mt[C::kStages], pre_k[C::kStages];
