@@ -223,19 +223,26 @@ struct SegList {
   int stream_k, k_tiles;
   long long u0, u1;
   int tf, nseg, first_partial, last_partial, np;
-  __device__ __forceinline__ void init(int sk, int kt, long long b, long long e) {
+  int stride;  // whole-tile mode: tiles tf, tf + stride, ...
+  // stream-K: the unit range [b, e).  Whole tiles (sk == 0): tiles are dealt
+  // round-robin (b = CTA index, e = tile count, stride = grid), so that the
+  // CTAs running at the same time cover consecutive tiles -- the token tiles
+  // of one weight tile -- and share its weight stream through L2.
+  __device__ __forceinline__ void init(int sk, int kt, long long b, long long e, int grid = 1) {
     stream_k = sk;
     k_tiles = kt;
     u0 = b;
     u1 = e;
-    if (u1 <= u0) {
-      nseg = 0;
+    stride = 1;
+    if (!sk) {
+      tf = (int)b;
+      stride = grid;
+      nseg = b < e ? (int)((e - b + grid - 1) / grid) : 0;
+      first_partial = last_partial = np = 0;
       return;
     }
-    if (!sk) {
-      tf = (int)u0;
-      nseg = (int)(u1 - u0);
-      first_partial = last_partial = np = 0;
+    if (u1 <= u0) {
+      nseg = 0;
       return;
     }
     tf = (int)(u0 / kt);
@@ -251,13 +258,14 @@ struct SegList {
     return (first_partial ? 1 : 0) + (j - np);
   }
   __device__ __forceinline__ void seg(int j, int& t, int& kb, int& ke) const {
-    const int k = natural(j);
-    t = tf + k;
     if (!stream_k) {
+      t = tf + j * stride;
       kb = 0;
       ke = k_tiles;
       return;
     }
+    const int k = natural(j);
+    t = tf + k;
     const long long ts = (long long)t * k_tiles;
     const long long a = ts > u0 ? ts : u0;
     const long long b = (ts + k_tiles) < u1 ? (ts + k_tiles) : u1;
@@ -413,7 +421,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   sc.KT = a.stream_k ? a.k_tiles : 1;
   sc.U = (unsigned)tiles * sc.KT;
   SegList sl;
-  sl.init(a.stream_k, a.k_tiles, sc.start(blockIdx.x), sc.start(blockIdx.x + 1));
+  if (a.stream_k)
+    sl.init(1, a.k_tiles, sc.start(blockIdx.x), sc.start(blockIdx.x + 1));
+  else
+    sl.init(0, a.k_tiles, blockIdx.x, tiles, gridDim.x);
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.b);

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   sc.KT = 1;
   sc.U = (unsigned)(ga.m_tiles * ga.n_tiles);
   SegList sl;
-  sl.init(0, ga.k_tiles, sc.start(blockIdx.x), sc.start(blockIdx.x + 1));
+  sl.init(0, ga.k_tiles, blockIdx.x, ga.m_tiles * ga.n_tiles, gridDim.x);
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.b);
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const float kLog2e = 1.4426950408889634f;
     const float sl2 = la.scale * kLog2e;
     for (int j = 0; j < sl.nseg; ++j) {
-      const int t = sl.tf + j;
+      const int t = sl.tf + j * sl.stride;
       const int nt = t / ga.m_tiles, mt = t % ga.m_tiles;
       const int acc = j & 1;
       if (!mbar_wait(&p.tfull[acc], (j >> 1) & 1, p.abort_flag)) break;
