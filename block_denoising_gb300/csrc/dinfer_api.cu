@@ -25,6 +25,7 @@
 #include "attention.cuh"
 #include "gemm_tc.cuh"
 #include "lmhead_tc.cuh"
+#include "noalloc.cuh"
 #include "small_kernels.cuh"
 
 using namespace dinfer;
@@ -1129,3 +1130,67 @@ dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void*
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// allocation-free GEMM entry point (include/dinfer_ops.h)
+// ===========================================================================
+namespace {
+// Device addresses of the fixed scratch, looked up once per device.
+constexpr int kMaxDevices = 64;
+float* g_noalloc_ptr[kMaxDevices] = {};
+DevState* g_noalloc_state_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* W, float* Y, int32_t M, int32_t N,
+                                                     int32_t K, void* stream) {
+  dinfer_ctx* c = nullptr;
+  if (!X || !W || !Y) return fail(c, DINFER_EINVAL, "NULL operand");
+  if (M < 1 || M > kNoAllocMaxRows)
+    return fail(c, DINFER_EINVAL, "the allocation-free GEMM takes 1 <= M <= %d token rows (got %d)", kNoAllocMaxRows,
+                M);
+  if (N < 128 || N % 128 || K < 64 || K % 64) return fail(c, DINFER_EINVAL, "unsupported GEMM shape");
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return fail(c, DINFER_ECUDA, "no current CUDA device");
+  }
+  // set-up on the first call on this device: the host-side names of the
+  // __device__ arrays are not device addresses, so look the addresses up
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    void* q = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&q, g_noalloc_state);
+    if (e != cudaSuccess || !p || !q) {
+      cudaGetLastError();
+      return fail(c, DINFER_ECUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
+    }
+    g_noalloc_state_ptr[dev] = reinterpret_cast<DevState*>(q);
+    g_noalloc_ptr[dev] = reinterpret_cast<float*>(p);
+  }
+  if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
+  constexpr int BN = 64;  // M <= 64: one token tile
+  GemmMaps m{};
+  if (!make_map(&m.a[0], W, N, K, 128) || !make_map(&m.b, X, M, K, BN))
+    return fail(c, DINFER_EINVAL, "tensor map encoding failed (alignment?)");
+  GemmArgs a{};
+  a.M = M; a.N = N; a.K = K; a.n_tiles = N / 128; a.a_mode = A_SINGLE;
+  a.out_f32 = Y; a.ldo = N;
+  a.m_tiles = 1;
+  a.k_tiles = K / 64;
+  const GemmSched gs = gemm_schedule(M, a.n_tiles, K, BN);
+  a.stream_k = gs.stream_k;
+  a.grid = std::min(gs.grid, kNoAllocMaxCtas);  // the scratch holds two partial tiles per CTA
+  if ((unsigned long long)a.n_tiles * (a.stream_k ? a.k_tiles : 1) * a.grid >= (1ull << 32))
+    return fail(c, DINFER_EINVAL, "GEMM too large for the allocation-free entry point");
+  a.slot_tok_major = 0;
+  a.ws = g_noalloc_ptr[dev];
+  a.status = g_noalloc_state_ptr[dev];
+  a.state = g_noalloc_state_ptr[dev];
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // No partial tile must start at zero: every slot the fixup reads is written
+  // by the GEMM launch of the same call.
+  CK(launchk(gemm_tc_kernel<BN>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<BN>::kSmem, s, 1, m, a));
+  if (a.stream_k) CK(launchk(splitk_fixup_kernel<BN>, dim3(a.n_tiles * 4), dim3(128), 0, s, 1, a));
+  return DINFER_OK;
+}

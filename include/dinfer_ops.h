@@ -52,6 +52,22 @@ dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void*
                                        int32_t rows_per_seq, int32_t L, int32_t heads, void* workspace,
                                        size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of dinfer_op_gemm_bf16 (no counterpart in the
+ * method itself: it exists for callers that cannot allocate device memory
+ * when they run a projection -- code inside another framework's memory pool,
+ * real-time paths, plug-ins that must not grow their footprint).  Same
+ * operands and result as dinfer_op_gemm_bf16 for M <= 64 token rows; no
+ * workspace argument and no allocation: the split-K partial tiles go to a
+ * fixed 9.5 MiB array in the library's module, present on every GPU that
+ * loads the library until the process exits.  The first call on a device
+ * looks the array's device address up (cudaGetSymbolAddress); make that first
+ * call before any stream capture.  All calls share the array, so calls that
+ * overlap on the GPU race and must be serialised by the caller.
+ * Errors: DINFER_EINVAL for M > 64 or an unsupported shape, DINFER_ECUDA if
+ * the set-up or a launch fails. */
+dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* W, float* Y, int32_t M, int32_t N, int32_t K,
+                                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif
