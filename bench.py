@@ -49,25 +49,41 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # algorithmic work (per unit) of the hot path
 # ---------------------------------------------------------------------------
+def _ffn_params(cfg, touched=True):
+    """FFN weights per layer: dense SwiGLU, or router + experts (all experts: a
+    block of 64 rows touches every one of 64 experts with probability ~1)."""
+    d = cfg.d_model
+    if cfg.n_experts:
+        return cfg.n_experts * d + cfg.n_experts * 3 * cfg.expert_ffn * d
+    return 3 * d * cfg.ffn
+
+
+def _ffn_flops_per_row(cfg):
+    d = cfg.d_model
+    if cfg.n_experts:
+        return 2 * (cfg.n_experts * d + cfg.top_k * 3 * cfg.expert_ffn * d)
+    return 2 * 3 * d * cfg.ffn
+
+
 def iteration_bytes(cfg, b, L, B):
     """Bytes one cached denoising iteration must move: every weight read once
     (embedding rows aside) plus the cached K/V of the L - B non-block positions."""
-    d, f, nl, V = cfg.d_model, cfg.ffn, cfg.n_layers, cfg.vocab
-    w = nl * (4 * d * d + 3 * d * f) + V * d
+    d, nl, V = cfg.d_model, cfg.n_layers, cfg.vocab
+    w = nl * (4 * d * d + _ffn_params(cfg)) + V * d
     kv = b * (L - B) * 2 * d * nl
     return 2 * (w + kv)
 
 
 def iteration_flops(cfg, b, L, B):
-    d, f, nl, V = cfg.d_model, cfg.ffn, cfg.n_layers, cfg.vocab
+    d, nl, V = cfg.d_model, cfg.n_layers, cfg.vocab
     M = b * B
-    return 2 * M * (nl * (4 * d * d + 3 * d * f) + V * d) + 4 * M * L * d * nl
+    return M * (nl * (8 * d * d + _ffn_flops_per_row(cfg)) + 2 * V * d) + 4 * M * L * d * nl
 
 
 def refresh_flops(cfg, b, L, B):
-    d, f, nl, V = cfg.d_model, cfg.ffn, cfg.n_layers, cfg.vocab
+    d, nl, V = cfg.d_model, cfg.n_layers, cfg.vocab
     M = b * L
-    return 2 * M * nl * (4 * d * d + 3 * d * f) + 4 * b * L * L * d * nl + 2 * b * B * V * d
+    return M * nl * (8 * d * d + _ffn_flops_per_row(cfg)) + 4 * b * L * L * d * nl + 2 * b * B * V * d
 
 
 class ClockSampler:
@@ -362,7 +378,8 @@ def launches_per_generation(cfg, ipb):
     """Kernels of ours launched by one generation: per forward embed + 7 per
     layer (2 norms, 4 GEMMs, attention) + final norm + LM head; per block
     begin/inner-condition/advance; one init."""
-    per_fwd = 1 + 7 * cfg.n_layers + 2
+    per_layer = 7 if not cfg.n_experts else 12
+    per_fwd = 1 + per_layer * cfg.n_layers + 2
     return 1 + len(ipb) * 3 + sum(ipb) * per_fwd
 
 
@@ -372,7 +389,7 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
     import torch
     from block_denoising_gb300 import inputs
     M = run.batch * run.seq_len
-    N, K = 2 * cfg.ffn, cfg.d_model
+    N, K = (2 * cfg.ffn if cfg.ffn else 3 * cfg.d_model), cfg.d_model
     X = inputs.normal_tensor(1, (M, K), 1.0, 9, device="cuda")
     Wt = inputs.normal_tensor(2, (N, K), 0.02, 9, device="cuda")
     Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
@@ -390,7 +407,7 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
     dt = e0.elapsed_time(e1) / 1000.0 / n
     flops = 2.0 * M * N * K
     ach = flops / dt / 1e12
-    return {"bound": "tensor", "kernel": "gemm_tc_kernel<256> (refresh gate/up GEMM, fp32 out)",
+    return {"bound": "tensor", "kernel": f"gemm_tc_kernel<256> (refresh GEMM {M}x{N}x{K}, fp32 out)",
             "achieved": ach, "peak": peak_tflops, "unit": "TFLOP/s", "frac": ach / peak_tflops,
             "traffic": None, "us_per_launch": dt * 1e6, "flops_per_launch": flops}
 

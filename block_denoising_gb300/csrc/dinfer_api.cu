@@ -25,6 +25,7 @@
 #include "attention.cuh"
 #include "gemm_tc.cuh"
 #include "lmhead_tc.cuh"
+#include "moe.cuh"
 #include "noalloc.cuh"
 #include "small_kernels.cuh"
 
@@ -201,6 +202,94 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
   return e;
 }
 
+// Grouped (MoE expert) GEMM: persistent grid, tiles from the device tables.
+cudaError_t launch_gemm_grouped(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s) {
+  a.grouped = 1;
+  a.stream_k = 0;
+  a.m_tiles = 1;
+  a.k_tiles = a.K / 64;
+  a.grid = num_sms();
+  switch (BN) {
+    case 64:
+      return launchk(gemm_tc_kernel<64>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<64>::kSmem, s, 1, maps, a);
+    case 128:
+      return launchk(gemm_tc_kernel<128>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<128>::kSmem, s, 1, maps, a);
+    default:
+      return launchk(gemm_tc_kernel<256>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<256>::kSmem, s, 1, maps, a);
+  }
+}
+
+// The routed FFN of one layer for `rows` rows of xn (bf16 [rows, d]):
+// router GEMM -> top-k -> counting-sort permutation -> grouped gate/up
+// (SwiGLU) and down GEMMs.  Leaves y [pairs, d] (fp32, permuted order),
+// topk weights and inverse positions for the combine kernel.
+struct MoeBufs {
+  float* logits;
+  int* topk_id;
+  float* topk_w;
+  int* rank;
+  int* chunk_cnt;
+  int* chunk_base;
+  int* tables;
+  int* inv;
+  void* x;
+  void* act;
+  float* y;
+  float* ws;
+  DevState* st;
+};
+cudaError_t enqueue_moe_ffn(const MoeBufs& b, const void* xn, int rows, int D, int E, int K, int FE,
+                            const CUtensorMap& m_router, const CUtensorMap& m_w13, const CUtensorMap& m_w2,
+                            cudaStream_t s) {
+  const int BN = bn_for_rows(rows);
+  GemmMaps mr{};
+  mr.a[0] = m_router;
+  if (!make_map(&mr.b, xn, rows, D, BN)) return cudaErrorInvalidValue;
+  GemmArgs ra{};
+  ra.M = rows; ra.N = E; ra.K = D; ra.n_tiles = (E + 127) / 128; ra.a_mode = A_SINGLE;
+  ra.out_f32 = b.logits; ra.ldo = E; ra.ws = b.ws; ra.status = b.st; ra.state = b.st;
+  cudaError_t e = launch_gemm_tc(mr, ra, BN, s);
+  if (e != cudaSuccess) return e;
+  e = launchk(moe_topk_kernel, dim3((rows * 32 + 255) / 256), dim3(256), 0, s, 1, (const float*)b.logits, rows, E, K,
+              b.topk_id, b.topk_w);
+  if (e != cudaSuccess) return e;
+  const int chunks = (rows + kMoeChunk - 1) / kMoeChunk;
+  e = launchk(moe_count_kernel, dim3(chunks), dim3(kMoeChunk), 0, s, 1, (const int*)b.topk_id, rows, E, K, b.rank,
+              b.chunk_cnt);
+  if (e != cudaSuccess) return e;
+  const int pairs = rows * K;
+  const int bng = bn_for_rows(std::max(1, (pairs + E - 1) / E));  // token tile of the expert GEMMs
+  int* row_off = b.tables;
+  int* cum_gu = b.tables + (E + 1);
+  int* cum_dn = b.tables + 2 * (E + 1);
+  e = launchk(moe_scan_kernel, dim3(1), dim3(64), 0, s, 1, (const int*)b.chunk_cnt, chunks, E, b.chunk_base, row_off,
+              cum_gu, cum_dn, bng, FE / 64, bng, D / 128);
+  if (e != cudaSuccess) return e;
+  e = launchk(moe_scatter_kernel, dim3(pairs), dim3(256), 0, s, 1, (const __nv_bfloat16*)xn, D, rows, E, K,
+              (const int*)b.topk_id, (const int*)b.rank, (const int*)b.chunk_base, (const int*)row_off, b.inv,
+              (__nv_bfloat16*)b.x);
+  if (e != cudaSuccess) return e;
+  // gate/up: SwiGLU into act [pairs, FE]
+  GemmMaps mg{};
+  mg.a[0] = m_w13;
+  if (!make_map(&mg.b, b.x, pairs, D, bng)) return cudaErrorInvalidValue;
+  GemmArgs ga{};
+  ga.M = pairs; ga.N = FE; ga.K = D; ga.a_mode = A_PAIR;
+  ga.groups = E; ga.g_tile_cum = cum_gu; ga.g_row_off = row_off; ga.g_wrows = 2 * FE; ga.g_a_half = FE;
+  ga.out_bf16 = (__nv_bfloat16*)b.act; ga.ldo = FE; ga.status = b.st; ga.state = b.st;
+  e = launch_gemm_grouped(mg, ga, bng, s);
+  if (e != cudaSuccess) return e;
+  // down: y [pairs, D]
+  GemmMaps md{};
+  md.a[0] = m_w2;
+  if (!make_map(&md.b, b.act, pairs, FE, bng)) return cudaErrorInvalidValue;
+  GemmArgs da{};
+  da.M = pairs; da.N = D; da.K = FE; da.a_mode = A_SINGLE;
+  da.groups = E; da.g_tile_cum = cum_dn; da.g_row_off = row_off; da.g_wrows = D;
+  da.out_f32 = b.y; da.ldo = D; da.status = b.st; da.state = b.st;
+  return launch_gemm_grouped(md, da, bng, s);
+}
+
 ResidPlan resid_plan(const GemmArgs& a, int BN, const float* ws) {
   ResidPlan p;
   p.ws = ws;
@@ -302,6 +391,19 @@ struct dinfer_ctx {
 
   // weight maps (bf16)
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
+  std::vector<CUtensorMap> m_router, m_w13, m_w2;
+  // MoE routing / permutation buffers (rows = max_rows * top_k pairs)
+  float* moe_logits = nullptr;
+  int* moe_topk_id = nullptr;
+  float* moe_topk_w = nullptr;
+  int* moe_rank = nullptr;
+  int* moe_chunk_cnt = nullptr;
+  int* moe_chunk_base = nullptr;
+  int* moe_tables = nullptr;  // row_off | tile_cum_gu | tile_cum_dn, each [E + 1]
+  int* moe_inv = nullptr;
+  void* moe_x = nullptr;      // bf16 [pairs, d]
+  void* moe_act = nullptr;    // bf16 [pairs, fe]
+  float* moe_y = nullptr;     // fp32 [pairs, d]
   CUtensorMap m_lm{};
 
   float* dbg_logits = nullptr;
@@ -362,19 +464,24 @@ const char* validate_desc(const dinfer_model_desc* d) {
   if (d->head_dim % 2) return "head_dim must be even";
   if (d->mask_id < 0 || d->mask_id >= d->vocab) return "mask_id outside [0, vocab)";
   if (d->dtype != DINFER_FP32 && d->dtype != DINFER_BF16) return "dtype must be DINFER_FP32 or DINFER_BF16";
-  if (d->n_experts != 0 || d->top_k != 0 || d->expert_ffn != 0) {
+  const bool moe = d->n_experts != 0 || d->top_k != 0 || d->expert_ffn != 0;
+  if (moe) {
     if (d->n_experts < 1 || d->top_k < 1 || d->top_k > d->n_experts || d->expert_ffn < 1)
       return "inconsistent MoE fields";
-    return "mixture-of-experts models are not supported by this build";
+    if (d->dtype != DINFER_BF16) return "MoE models must be bf16";
+    if (d->n_experts > 64) return "MoE models take at most 64 experts";
+    if (d->top_k > kMoeMaxK) return "MoE top_k must be <= 8";
+    if (d->expert_ffn % 64) return "MoE expert_ffn must be a multiple of 64";
+  } else if (d->ffn < 1) {
+    return "ffn must be positive";
   }
-  if (d->ffn < 1) return "ffn must be positive";
   if (d->max_batch < 1 || d->max_batch > kMaxBatch) return "max_batch must be in [1, 64]";
   if (d->max_seq < 1) return "max_seq must be positive";
   if (!(d->rms_eps >= 0.f) || !(d->rope_theta > 0.f) || !std::isfinite(d->logit_scale)) return "bad float field";
   if (d->dtype == DINFER_BF16) {
     if (d->head_dim != 128) return "bf16 models need head_dim 128";
     if (d->d_model % 128) return "bf16 models need d_model % 128 == 0";
-    if (d->ffn % 64) return "bf16 models need ffn % 64 == 0";
+    if (!moe && d->ffn % 64) return "bf16 models need ffn % 64 == 0";
     if (d->vocab % 8) return "bf16 models need vocab % 8 == 0";
   } else {
     if ((size_t)d->d_model * 4 * 64 > 192 * 1024) return "fp32 models need d_model <= 768";
@@ -420,7 +527,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   const int BN = bn_for_rows(rows);
   GemmMaps mx{}, mo{}, mact{};
   if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BN) ||
-      !make_map(&mact.b, c->act, rows, F, BN))
+      (!d.n_experts && !make_map(&mact.b, c->act, rows, F, BN)))
     return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
   const int nthr = D / 16;  // resid_norm threads per row
@@ -469,6 +576,23 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
                  (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, D, d.rms_eps, f.rows_per_seq, f.L, 0,
                  (const DevState*)c->st, resid_plan(a, BN, c->gemm_ws)));
     }
+    const bool last = l + 1 == d.n_layers;
+    const void* gn = last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0);
+    // after the last layer only the block rows go on (to the LM head)
+    const int nrows = last ? f.batch * f.B : rows;
+    const int gather = last && f.refresh ? 1 : 0;
+    if (d.n_experts) {
+      // a5': routed experts, then the weighted combine + residual + next norm
+      MoeBufs mb{c->moe_logits, c->moe_topk_id, c->moe_topk_w, c->moe_rank, c->moe_chunk_cnt, c->moe_chunk_base,
+                 c->moe_tables, c->moe_inv, c->moe_x, c->moe_act, c->moe_y, c->gemm_ws, c->st};
+      CK(enqueue_moe_ffn(mb, c->xn, rows, D, d.n_experts, d.top_k, d.expert_ffn, c->m_router[l], c->m_w13[l],
+                         c->m_w2[l], s));
+      CK(launchk(moe_combine_norm_kernel<__nv_bfloat16>, dim3(nrows), dim3(nthr), 0, s, 1, c->h,
+                 (const float*)c->moe_y, (const float*)c->moe_topk_w, (const int*)c->moe_inv, d.top_k,
+                 (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps, f.B, f.L, gather,
+                 (const DevState*)c->st));
+      continue;
+    }
     // a5: SwiGLU FFN (gate/up with the SiLU*up epilogue, down + residual)
     {
       GemmMaps m = mx;
@@ -485,11 +609,6 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       b.M = rows; b.N = D; b.K = F; b.n_tiles = D / 128; b.a_mode = A_SINGLE;
       b.resid = c->h; b.ws = c->gemm_ws; b.status = c->st; b.state = c->st;
       CK(launch_gemm_tc(m2, b, BN, s, true));
-      const bool last = l + 1 == d.n_layers;
-      const void* gn = last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0);
-      // after the last layer only the block rows go on (to the LM head)
-      const int nrows = last ? f.batch * f.B : rows;
-      const int gather = last && f.refresh ? 1 : 0;
       CK(launchk(resid_norm_kernel<__nv_bfloat16>, dim3(nrows), dim3(nthr), 0, s, 1, c->h,
                  (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps, f.B, f.L, gather,
                  (const DevState*)c->st, resid_plan(b, BN, c->gemm_ws)));
@@ -802,6 +921,21 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
   AL(c->q, c->max_rows * D * es);
   AL(c->attn_o, c->max_rows * D * es);
   AL(c->act, c->max_rows * F * es);
+  if (desc->n_experts) {
+    const size_t E = desc->n_experts, K = desc->top_k, FE = desc->expert_ffn;
+    const size_t pairs = c->max_rows * K, chunks = (c->max_rows + kMoeChunk - 1) / kMoeChunk;
+    AL(c->moe_logits, c->max_rows * E * 4);
+    AL(c->moe_topk_id, pairs * 4);
+    AL(c->moe_topk_w, pairs * 4);
+    AL(c->moe_rank, pairs * 4);
+    AL(c->moe_chunk_cnt, chunks * E * 4);
+    AL(c->moe_chunk_base, chunks * E * 4);
+    AL(c->moe_tables, 3 * (E + 1) * 4);
+    AL(c->moe_inv, pairs * 4);
+    AL(c->moe_x, pairs * D * 2);
+    AL(c->moe_act, pairs * FE * 2);
+    AL(c->moe_y, pairs * D * 4);
+  }
   if (!c->bf16) {
     AL(c->qkv32, c->max_rows * 3 * D * 4);
     AL(c->gu32, c->max_rows * 2 * F * 4);
@@ -841,15 +975,23 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
     const int nl = desc->n_layers;
     c->m_wq.resize(nl); c->m_wk.resize(nl); c->m_wv.resize(nl); c->m_wo.resize(nl);
     c->m_wg.resize(nl); c->m_wu.resize(nl); c->m_wd.resize(nl);
+    c->m_router.resize(nl); c->m_w13.resize(nl); c->m_w2.resize(nl);
     bool ok = true;
+    const size_t E = desc->n_experts, FE = desc->expert_ffn;
     for (int l = 0; l < nl; ++l) {
       ok &= make_map(&c->m_wq[l], c->LW(l, 1), D, D, 128);
       ok &= make_map(&c->m_wk[l], c->LW(l, 2), D, D, 128);
       ok &= make_map(&c->m_wv[l], c->LW(l, 3), D, D, 128);
       ok &= make_map(&c->m_wo[l], c->LW(l, 4), D, D, 128);
-      ok &= make_map(&c->m_wg[l], c->LW(l, 6), F, D, 64);
-      ok &= make_map(&c->m_wu[l], c->LW(l, 7), F, D, 64);
-      ok &= make_map(&c->m_wd[l], c->LW(l, 8), D, F, 128);
+      if (E) {
+        ok &= make_map(&c->m_router[l], c->LW(l, 6), E, D, 128);
+        ok &= make_map(&c->m_w13[l], c->LW(l, 7), E * 2 * FE, D, 64);
+        ok &= make_map(&c->m_w2[l], c->LW(l, 8), E * D, FE, 128);
+      } else {
+        ok &= make_map(&c->m_wg[l], c->LW(l, 6), F, D, 64);
+        ok &= make_map(&c->m_wu[l], c->LW(l, 7), F, D, 64);
+        ok &= make_map(&c->m_wd[l], c->LW(l, 8), D, F, 128);
+      }
     }
     ok &= make_map(&c->m_lm, c->W(2 + 9 * nl), desc->vocab, D, 128);
     if (!ok) {
@@ -1130,6 +1272,56 @@ dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void*
 }
 
 }  // extern "C"
+
+extern "C" dinfer_status dinfer_op_moe_ffn_bf16(const void* X, const void* router, const void* w13, const void* w2,
+                                                int32_t M, int32_t d, int32_t E, int32_t K, int32_t fe, float* out,
+                                                int32_t* topk_id, float* topk_w, void* workspace,
+                                                size_t workspace_bytes, void* stream) {
+  dinfer_ctx* c = nullptr;
+  if (!X || !router || !w13 || !w2 || !out) return fail(c, DINFER_EINVAL, "NULL operand");
+  if (M < 1 || d < 128 || d % 128 || d / 16 > 512 || E < 1 || E > 64 || K < 1 || K > kMoeMaxK || K > E || fe < 64 ||
+      fe % 64)
+    return fail(c, DINFER_EINVAL, "unsupported MoE shape");
+  OpWs o;
+  if (!op_ws(workspace, workspace_bytes, o)) return fail(c, DINFER_EINVAL, "workspace too small");
+  if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
+  // carve the data region
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    void* p = o.data + off;
+    off += (bytes + 255) & ~size_t(255);
+    return p;
+  };
+  const size_t pairs = (size_t)M * K, chunks = (M + kMoeChunk - 1) / kMoeChunk;
+  MoeBufs b;
+  b.ws = (float*)take(gemm_ws_floats(num_sms()) * 4);
+  b.logits = (float*)take((size_t)M * E * 4);
+  b.topk_id = (int*)take(pairs * 4);
+  b.topk_w = (float*)take(pairs * 4);
+  b.rank = (int*)take(pairs * 4);
+  b.chunk_cnt = (int*)take(chunks * E * 4);
+  b.chunk_base = (int*)take(chunks * E * 4);
+  b.tables = (int*)take(3 * ((size_t)E + 1) * 4);
+  b.inv = (int*)take(pairs * 4);
+  b.x = take(pairs * d * 2);
+  b.act = take(pairs * fe * 2);
+  b.y = (float*)take(pairs * d * 4);
+  b.st = o.st;
+  if (off > o.data_bytes) return fail(c, DINFER_EINVAL, "workspace too small for this MoE shape");
+  CUtensorMap mr, m13, m2;
+  if (!make_map(&mr, router, E, d, 128) || !make_map(&m13, w13, (size_t)E * 2 * fe, d, 64) ||
+      !make_map(&m2, w2, (size_t)E * d, fe, 128))
+    return fail(c, DINFER_EINVAL, "tensor map encoding failed (alignment?)");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CK(enqueue_moe_ffn(b, X, M, d, E, K, fe, mr, m13, m2, s));
+  CK(cudaMemsetAsync(out, 0, (size_t)M * d * 4, s));
+  CK(launchk(moe_combine_norm_kernel<__nv_bfloat16>, dim3(M), dim3(d / 16), 0, s, 1, out, (const float*)b.y,
+             (const float*)b.topk_w, (const int*)b.inv, K, (const __nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr,
+             d, 0.f, M, M, 0, (const DevState*)o.st));
+  if (topk_id) CK(cudaMemcpyAsync(topk_id, b.topk_id, pairs * 4, cudaMemcpyDeviceToDevice, s));
+  if (topk_w) CK(cudaMemcpyAsync(topk_w, b.topk_w, pairs * 4, cudaMemcpyDeviceToDevice, s));
+  return DINFER_OK;
+}
 
 // ===========================================================================
 // allocation-free GEMM entry point (include/dinfer_ops.h)

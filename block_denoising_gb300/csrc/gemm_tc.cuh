@@ -68,7 +68,58 @@ struct GemmArgs {
   int grid;                // CTAs of the GEMM launch (fixes the unit ranges)
   int slot_tok_major;      // partial slots [BN tokens][128 rows] (residual GEMMs), else [128 rows][BN]
   DevState* status;
+  // grouped mode (mixture-of-experts): the tiles of `groups` independent
+  // GEMMs that share the maps.  Group e owns rows [g_row_off[e], g_row_off[e+1])
+  // of the token operand and weight rows [e * g_wrows, (e+1) * g_wrows) of the
+  // weight map; its tiles are [g_tile_cum[e], g_tile_cum[e+1]) (device tables
+  // written by the routing kernels), n-tile major.
+  int grouped;
+  int groups;
+  const int* g_tile_cum;   // [groups + 1]
+  const int* g_row_off;    // [groups + 1]
+  int g_wrows;             // weight rows per group
+  int g_a_half;            // A_PAIR: offset of the up rows inside a group
 };
+
+// Where a tile's operands and outputs are.  Token columns are local to the
+// tile's group: local row m = mt * BN + c is valid when m < m_lim and lands on
+// output row out_base + m.
+struct TileRef {
+  int nt, mt;
+  int a_base;    // first weight row of the group in the weight map (0 when dense)
+  int b_row;     // first token row of the token tile
+  int m_lim;
+  int out_base;
+};
+
+template <int BN>
+__device__ __forceinline__ TileRef decode_tile(const GemmArgs& a, int t) {
+  TileRef r;
+  if (!a.grouped) {
+    r.nt = t / a.m_tiles;
+    r.mt = t - r.nt * a.m_tiles;
+    r.a_base = 0;
+    r.b_row = r.mt * BN;
+    r.m_lim = a.M;
+    r.out_base = 0;
+    return r;
+  }
+  int lo = 0, hi = a.groups;  // e with g_tile_cum[e] <= t < g_tile_cum[e + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a.g_tile_cum + mid) <= t) lo = mid; else hi = mid;
+  }
+  const int row0 = __ldg(a.g_row_off + lo), rows = __ldg(a.g_row_off + lo + 1) - row0;
+  const int mtiles = (rows + BN - 1) / BN;
+  const int li = t - __ldg(a.g_tile_cum + lo);
+  r.nt = li / mtiles;
+  r.mt = li - r.nt * mtiles;
+  r.a_base = lo * a.g_wrows;
+  r.b_row = row0 + r.mt * BN;
+  r.m_lim = rows;
+  r.out_base = row0;
+  return r;
+}
 
 constexpr int kGemmThreads = 192;
 
@@ -97,10 +148,18 @@ struct Sched {
 
 template <int BN>
 __device__ __forceinline__ void load_stage_a(const GemmMaps& maps, const GemmArgs& a, uint8_t* stage, uint64_t* bar,
-                                             int nt, int k, uint64_t pol_w) {
+                                             const TileRef& tr, int k, uint64_t pol_w) {
   uint8_t* sa = stage;
   const int kx = k * 64;
-  if (a.a_mode == A_PAIR) {
+  const int nt = tr.nt;
+  if (a.grouped) {
+    if (a.a_mode == A_PAIR) {
+      tma_load_2d(sa, &maps.a[0], bar, kx, tr.a_base + nt * 64, pol_w);
+      tma_load_2d(sa + 64 * 128, &maps.a[0], bar, kx, tr.a_base + a.g_a_half + nt * 64, pol_w);
+    } else {
+      tma_load_2d(sa, &maps.a[0], bar, kx, tr.a_base + nt * 128, pol_w);
+    }
+  } else if (a.a_mode == A_PAIR) {
     tma_load_2d(sa, &maps.a[0], bar, kx, nt * 64, pol_w);
     tma_load_2d(sa + 64 * 128, &maps.a[1], bar, kx, nt * 64, pol_w);
   } else if (a.a_mode == A_THREE) {
@@ -111,16 +170,16 @@ __device__ __forceinline__ void load_stage_a(const GemmMaps& maps, const GemmArg
   }
 }
 template <int BN>
-__device__ __forceinline__ void load_stage_b(const GemmMaps& maps, uint8_t* stage, uint64_t* bar, int mt, int k,
+__device__ __forceinline__ void load_stage_b(const GemmMaps& maps, uint8_t* stage, uint64_t* bar, int b_row, int k,
                                              uint64_t pol_x) {
-  tma_load_2d(stage + GemmCfg<BN>::kStageA, &maps.b, bar, k * 64, mt * BN, pol_x);
+  tma_load_2d(stage + GemmCfg<BN>::kStageA, &maps.b, bar, k * 64, b_row, pol_x);
 }
 
 // One 16-column chunk of the finished accumulator for output feature row
 // `row` (0..127 inside the tile) and tokens m0 .. m0+15.
 template <int BN>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16], int row, int nt, int m0,
-                                               float* xchg) {
+                                               float* xchg, int m_lim, int out_base) {
   if (a.q_out != nullptr) {
     // ---- QKV: RoPE pairs (i, i + 64) sit in rows row and row ^ 64 ----
     const int n = nt * 128 + row;
@@ -188,7 +247,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
     if (act_row && jf < a.N) {
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        if (m0 + c < a.M) a.out_bf16[(size_t)(m0 + c) * a.ldo + jf] = __float2bfloat16_rn(o[c]);
+        if (m0 + c < m_lim) a.out_bf16[(size_t)(out_base + m0 + c) * a.ldo + jf] = __float2bfloat16_rn(o[c]);
     }
   } else {
     const int n = nt * 128 + row;
@@ -204,11 +263,11 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
       } else if (a.out_bf16) {
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          if (m0 + c < a.M) a.out_bf16[(size_t)(m0 + c) * a.ldo + n] = __float2bfloat16_rn(v[c]);
+          if (m0 + c < m_lim) a.out_bf16[(size_t)(out_base + m0 + c) * a.ldo + n] = __float2bfloat16_rn(v[c]);
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          if (m0 + c < a.M) a.out_f32[(size_t)(m0 + c) * a.ldo + n] = v[c];
+          if (m0 + c < m_lim) a.out_f32[(size_t)(out_base + m0 + c) * a.ldo + n] = v[c];
       }
     }
   }
@@ -294,29 +353,32 @@ __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArg
   using C = GemmCfg<BN>;
   // weight tiles used by a single token tile stream through L2 once; with
   // several token tiles the following tiles re-read them from L2
-  const uint64_t pol_w = m_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
+  const uint64_t pol_w = (m_tiles == 1 && !a.grouped) ? l2_policy_evict_first() : l2_policy_evict_normal();
   const uint64_t pol_x = l2_policy_evict_last();
-  // phase 1: weights of the first kStages stages
-  int pre_mt[C::kStages], pre_k[C::kStages];
+  // phase 1: weights of the first kStages stages (dense: before the wait)
+  int pre_b[C::kStages], pre_k[C::kStages];
   int pre = 0;
-  for (int j = 0; j < sl.nseg && pre < C::kStages; ++j) {
-    int t, kb, ke;
-    sl.seg(j, t, kb, ke);
-    for (int k = kb; k < ke && pre < C::kStages; ++k, ++pre) {
-      mbar_arrive_expect_tx(&p.full[pre], C::kStage);
-      load_stage_a<BN>(maps, a, p.stages + pre * C::kStage, &p.full[pre], t / m_tiles, k, pol_w);
-      pre_mt[pre] = t % m_tiles;
-      pre_k[pre] = k;
+  if (!a.grouped) {
+    for (int j = 0; j < sl.nseg && pre < C::kStages; ++j) {
+      int t, kb, ke;
+      sl.seg(j, t, kb, ke);
+      const TileRef tr = decode_tile<BN>(a, t);
+      for (int k = kb; k < ke && pre < C::kStages; ++k, ++pre) {
+        mbar_arrive_expect_tx(&p.full[pre], C::kStage);
+        load_stage_a<BN>(maps, a, p.stages + pre * C::kStage, &p.full[pre], tr, k, pol_w);
+        pre_b[pre] = tr.b_row;
+        pre_k[pre] = k;
+      }
     }
   }
   pdl_wait();
-  for (int i = 0; i < pre; ++i) load_stage_b<BN>(maps, p.stages + i * C::kStage, &p.full[i], pre_mt[i], pre_k[i], pol_x);
+  for (int i = 0; i < pre; ++i) load_stage_b<BN>(maps, p.stages + i * C::kStage, &p.full[i], pre_b[i], pre_k[i], pol_x);
   // phase 2: the rest of the pipeline
   uint32_t it = 0;
   for (int j = 0; j < sl.nseg && !*p.abort_flag; ++j) {
     int t, kb, ke;
     sl.seg(j, t, kb, ke);
-    const int nt = t / m_tiles, mt = t % m_tiles;
+    const TileRef tr = decode_tile<BN>(a, t);
     bool ok = true;
     for (int k = kb; k < ke; ++k, ++it) {
       if (it < (uint32_t)pre) continue;
@@ -324,8 +386,8 @@ __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArg
       const uint32_t round = it / C::kStages;
       if (!mbar_wait(&p.empty[s], (round & 1) ^ 1, p.abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(&p.full[s], C::kStage);
-      load_stage_a<BN>(maps, a, p.stages + s * C::kStage, &p.full[s], nt, k, pol_w);
-      load_stage_b<BN>(maps, p.stages + s * C::kStage, &p.full[s], mt, k, pol_x);
+      load_stage_a<BN>(maps, a, p.stages + s * C::kStage, &p.full[s], tr, k, pol_w);
+      load_stage_b<BN>(maps, p.stages + s * C::kStage, &p.full[s], tr.b_row, k, pol_x);
     }
     if (!ok) break;
   }
@@ -417,7 +479,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   Sched sc;
   sc.G = gridDim.x;
-  const int tiles = a.m_tiles * a.n_tiles;
+  // grouped: the tile count is written by the routing kernels that precede
+  // this launch, so it is read after the dependency wait
+  if (a.grouped) pdl_wait();
+  const int tiles = a.grouped ? __ldg(a.g_tile_cum + a.groups) : a.m_tiles * a.n_tiles;
   sc.KT = a.stream_k ? a.k_tiles : 1;
   sc.U = (unsigned)tiles * sc.KT;
   SegList sl;
@@ -450,7 +515,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int j = 0; j < sl.nseg; ++j) {
       int t, kb, ke;
       sl.seg(j, t, kb, ke);
-      const int nt = t / a.m_tiles, mt = t % a.m_tiles;
+      const TileRef tr = decode_tile<BN>(a, t);
       const int acc = j & 1;
       const uint32_t use = j >> 1;
       if (!mbar_wait(&p.tfull[acc], use & 1, p.abort_flag)) break;
@@ -489,7 +554,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int c = 0; c < BN / 16; ++c) {
         float v[16];
         tmem_ld16(tbase + c * 16, v);
-        epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
+        epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg, tr.m_lim, tr.out_base);
       }
       tc_fence_before();
       mbar_arrive(&p.tempty[acc]);
@@ -559,7 +624,7 @@ __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
         }
   }
   const int nt = t / a.m_tiles, mt = t % a.m_tiles;
-  epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg);
+  epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg, a.M, 0);
   pdl_trigger();
 }
 

@@ -1,0 +1,221 @@
+// Mixture-of-experts FFN (OLMoE-style routing, LLaDA-MoE shapes).
+//
+//   p = softmax(x_hat W_r^T) over the E experts; the top-k experts of each row
+//   by p (ties to the lower expert index), weights not renormalised;
+//   h += sum over the row's experts of p_e * (silu(x_hat W_g,e^T) * x_hat W_u,e^T) W_d,e^T
+//
+// Device pipeline: router logits (tcgen05 GEMM, fp32 out) -> moe_topk_kernel
+// (one warp per row) -> moe_count_kernel + moe_scan_kernel + moe_scatter_kernel
+// (a counting sort of the (row, expert) pairs by expert, rows in ascending
+// order inside an expert, so the permutation does not depend on timing) ->
+// grouped gate/up and down GEMMs over the permuted rows (gemm_tc_kernel in
+// grouped mode, tile tables written here) -> moe_combine_norm_kernel
+// (weighted sum of the row's k expert outputs in slot order, residual add,
+// next RMSNorm).
+#pragma once
+#include "common.cuh"
+
+namespace dinfer {
+
+constexpr int kMoeMaxK = 8;
+constexpr int kMoeMaxE = 256;
+constexpr int kMoeChunk = 256;  // rows per counting chunk
+
+// top-k of softmax(logits) per row; one warp per row, E <= 64 (2 per lane)
+__global__ void moe_topk_kernel(const float* __restrict__ logits, int M, int E, int K, int* __restrict__ topk_id,
+                                float* __restrict__ topk_w) {
+  pdl_wait();
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp < M) {
+    const float* l = logits + (size_t)warp * E;
+    float v0 = lane < E ? l[lane] : -INFINITY;
+    float v1 = lane + 32 < E ? l[lane + 32] : -INFINITY;
+    const float mx = warp_max(fmaxf(v0, v1));
+    const float e0 = lane < E ? expf(v0 - mx) : 0.f, e1 = lane + 32 < E ? expf(v1 - mx) : 0.f;
+    const float inv = 1.f / warp_sum(e0 + e1);
+    // selection by logit (monotone in p), ties to the lower expert
+    float c0 = v0, c1 = v1;
+    for (int k = 0; k < K; ++k) {
+      float bv = c0;
+      int bi = lane;
+      if (c1 > bv) { bv = c1; bi = lane + 32; }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) {
+        topk_id[(size_t)warp * K + k] = bi;
+        topk_w[(size_t)warp * K + k] = expf(bv - mx) * inv;
+      }
+      if (bi == lane) c0 = -INFINITY;
+      if (bi == lane + 32) c1 = -INFINITY;
+    }
+  }
+  pdl_trigger();
+}
+
+// Per chunk of 256 rows: for every expert, the rank of each selecting row
+// among the chunk's selecting rows (row order) and the chunk's count.
+__global__ void __launch_bounds__(kMoeChunk) moe_count_kernel(const int* __restrict__ topk_id, int M, int E, int K,
+                                                             int* __restrict__ local_rank, int* __restrict__ chunk_cnt) {
+  __shared__ int warp_tot[kMoeChunk / 32];
+  pdl_wait();
+  const int r = blockIdx.x * kMoeChunk + threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ids[kMoeMaxK];
+#pragma unroll
+  for (int k = 0; k < kMoeMaxK; ++k) ids[k] = (r < M && k < K) ? topk_id[(size_t)r * K + k] : -1;
+  for (int e = 0; e < E; ++e) {
+    int slot = -1;
+#pragma unroll
+    for (int k = 0; k < kMoeMaxK; ++k)
+      if (ids[k] == e) slot = k;
+    const unsigned bal = __ballot_sync(0xffffffffu, slot >= 0);
+    if (lane == 0) warp_tot[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kMoeChunk / 32; ++w) {
+      const int c = warp_tot[w];
+      before += w < warp ? c : 0;
+      total += c;
+    }
+    if (slot >= 0) local_rank[(size_t)r * K + slot] = before + __popc(bal & ((1u << lane) - 1u));
+    if (threadIdx.x == 0) chunk_cnt[(size_t)blockIdx.x * E + e] = total;
+    __syncthreads();
+  }
+  pdl_trigger();
+}
+
+// One CTA: chunk bases per expert, expert row offsets, and the tile tables of
+// the two grouped GEMMs (n-tiles per expert x token tiles of that expert).
+__global__ void moe_scan_kernel(const int* __restrict__ chunk_cnt, int n_chunks, int E, int* __restrict__ chunk_base,
+                                int* __restrict__ row_off, int* __restrict__ tile_cum_gu, int* __restrict__ tile_cum_dn,
+                                int bn_gu, int nt_gu, int bn_dn, int nt_dn) {
+  __shared__ int tot[kMoeMaxE];
+  pdl_wait();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int acc = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      chunk_base[(size_t)c * E + e] = acc;
+      acc += chunk_cnt[(size_t)c * E + e];
+    }
+    tot[e] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ro = 0, tg = 0, td = 0;
+    for (int e = 0; e < E; ++e) {
+      row_off[e] = ro;
+      tile_cum_gu[e] = tg;
+      tile_cum_dn[e] = td;
+      ro += tot[e];
+      tg += ((tot[e] + bn_gu - 1) / bn_gu) * nt_gu;
+      td += ((tot[e] + bn_dn - 1) / bn_dn) * nt_dn;
+    }
+    row_off[E] = ro;
+    tile_cum_gu[E] = tg;
+    tile_cum_dn[E] = td;
+  }
+  pdl_trigger();
+}
+
+// One CTA per (row, slot): its permuted position, and a copy of the row's
+// normed input into the permuted operand of the gate/up GEMM.
+__global__ void moe_scatter_kernel(const __nv_bfloat16* __restrict__ xn, int d, int M, int E, int K,
+                                   const int* __restrict__ topk_id, const int* __restrict__ local_rank,
+                                   const int* __restrict__ chunk_base, const int* __restrict__ row_off,
+                                   int* __restrict__ inv, __nv_bfloat16* __restrict__ x_perm) {
+  pdl_wait();
+  const int pair = blockIdx.x;
+  const int r = pair / K;
+  const int e = topk_id[pair];
+  const int dst = row_off[e] + chunk_base[(size_t)(r / kMoeChunk) * E + e] + local_rank[pair];
+  if (threadIdx.x == 0) inv[pair] = dst;
+  const uint4* src = reinterpret_cast<const uint4*>(xn + (size_t)r * d);
+  uint4* out = reinterpret_cast<uint4*>(x_perm + (size_t)dst * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) out[i] = src[i];
+  pdl_trigger();
+}
+
+// h[src] += sum_k w[r, k] * y[inv[r, k]] (slot order); then, if out != NULL,
+// out[r] = bf16(RMSNorm(h[src]) * g).  One CTA per output row, d / 16 threads.
+template <typename Tg>
+__global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict__ h, const float* __restrict__ y,
+                                                               const float* __restrict__ topk_w,
+                                                               const int* __restrict__ inv, int K,
+                                                               const Tg* __restrict__ g,
+                                                               __nv_bfloat16* __restrict__ out, int d, float eps,
+                                                               int rows_per_seq, int L, int gather,
+                                                               const DevState* st) {
+  __shared__ float red[32];
+  pdl_wait();
+  const int r = blockIdx.x;
+  size_t src = r;
+  if (gather) {
+    const int bi = r / rows_per_seq;
+    src = (size_t)bi * L + st->block_start + (r - bi * rows_per_seq);
+  }
+  const int f0 = threadIdx.x * 16;
+  float* hp = h + src * d + f0;
+  float x[16];
+  {
+    const float4* h4 = reinterpret_cast<const float4*>(hp);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 t = h4[i];
+      x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
+    }
+  }
+  for (int k = 0; k < K; ++k) {
+    const float w = topk_w[src * K + k];
+    const float4* yp = reinterpret_cast<const float4*>(y + (size_t)inv[src * K + k] * d + f0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 t = __ldcg(yp + i);
+      x[4 * i] = fmaf(w, t.x, x[4 * i]);
+      x[4 * i + 1] = fmaf(w, t.y, x[4 * i + 1]);
+      x[4 * i + 2] = fmaf(w, t.z, x[4 * i + 2]);
+      x[4 * i + 3] = fmaf(w, t.w, x[4 * i + 3]);
+    }
+  }
+  {
+    float4* h4 = reinterpret_cast<float4*>(hp);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+  }
+  if (out == nullptr) {
+    pdl_trigger();
+    return;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv_rms = rsqrtf(red[0] / (float)d + eps);
+  uint4 o[2];
+  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a0 = x[2 * i] * inv_rms * (float)g[f0 + 2 * i];
+    const float a1 = x[2 * i + 1] * inv_rms * (float)g[f0 + 2 * i + 1];
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+    ow[i] = *reinterpret_cast<uint32_t*>(&b2);
+  }
+  uint4* op = reinterpret_cast<uint4*>(out + (size_t)r * d + f0);
+  op[0] = o[0];
+  op[1] = o[1];
+  pdl_trigger();
+}
+
+}  // namespace dinfer

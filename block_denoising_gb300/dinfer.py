@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
     L.dinfer_op_lmhead_bf16.restype = i32
     L.dinfer_op_attention_bf16.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, sz, vp]
     L.dinfer_op_attention_bf16.restype = i32
+    L.dinfer_op_moe_ffn_bf16.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    L.dinfer_op_moe_ffn_bf16.restype = i32
     _lib = L
     return L
 
@@ -204,3 +206,16 @@ def op_attention_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rows_pe
     _check(lib().dinfer_op_attention_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), b, rows_per_seq, L, heads,
                                           _ptr(ws.buf), ws.nbytes, _stream_ptr()))
     return out
+
+
+def op_moe_ffn_bf16(X: torch.Tensor, router: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, top_k: int,
+                    ws: OpWorkspace):
+    """Routed expert FFN output [M, d] fp32 and the routing (ids [M, k], weights [M, k])."""
+    M, d = X.shape
+    E, two_fe, _ = w13.shape
+    out = torch.empty((M, d), dtype=torch.float32, device=X.device)
+    ids = torch.empty((M, top_k), dtype=torch.int32, device=X.device)
+    w = torch.empty((M, top_k), dtype=torch.float32, device=X.device)
+    _check(lib().dinfer_op_moe_ffn_bf16(_ptr(X), _ptr(router), _ptr(w13), _ptr(w2), M, d, E, top_k, two_fe // 2,
+                                        _ptr(out), _ptr(ids), _ptr(w), _ptr(ws.buf), ws.nbytes, _stream_ptr()))
+    return out, ids, w

@@ -52,6 +52,19 @@ dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void*
                                        int32_t rows_per_seq, int32_t L, int32_t heads, void* workspace,
                                        size_t workspace_bytes, void* stream);
 
+/* Routed expert FFN of a mixture-of-experts layer (LLaDA-MoE / OLMoE-style
+ * routing), the a5' step of the denoising iteration:
+ *   p = softmax(X router^T) over E experts; the K experts of highest p (ties
+ *   to the lower index); out[m] = sum over them of p_e * SwiGLU_e(X[m]) with
+ *   SwiGLU_e(x) = (silu(x W_g,e^T) * x W_u,e^T) W_d,e^T  (weights not renormalised).
+ * X [M, d] bf16 (the normed FFN input); router [E, d]; w13 [E, 2 fe, d] (gate
+ * rows then up rows); w2 [E, d, fe]; all bf16 row-major.  out [M, d] fp32.
+ * topk_id [M, K] int32 / topk_w [M, K] fp32 optional (the routing decision).
+ * d % 128 == 0, d <= 8192, E <= 64, K <= 8, fe % 64 == 0. */
+dinfer_status dinfer_op_moe_ffn_bf16(const void* X, const void* router, const void* w13, const void* w2, int32_t M,
+                                     int32_t d, int32_t E, int32_t K, int32_t fe, float* out, int32_t* topk_id,
+                                     float* topk_w, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Allocation-free variant of dinfer_op_gemm_bf16 (no counterpart in the
  * method itself: it exists for callers that cannot allocate device memory
  * when they run a projection -- code inside another framework's memory pool,

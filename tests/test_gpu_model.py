@@ -68,10 +68,30 @@ def flags_for(rec, tau, tol, B, s0):
     return fl
 
 
-def teacher_forced(D, cfg, W, prompt, G, B, tau, tol, max_blocks=None):
-    """Run every oracle iteration on the GPU from the oracle's state; return error statistics."""
+def teacher_forced(D, cfg, W, prompt, G, B, tau, tol, max_blocks=None, route_margin=None):
+    """Run every oracle iteration on the GPU from the oracle's state; return error statistics.
+
+    route_margin (MoE models): block rows whose router top-k margin (k-th minus
+    (k+1)-th router logit, any layer) is below it are flagged too -- a routing
+    decision inside the bf16 noise can send the row to another expert.
+    """
     m = O.Model(O.Desc.from_config(cfg), [w.float().numpy() for w in W])
-    x, trace = O.generate(m, prompt, G, B, tau, keep_logits=True, max_blocks=max_blocks)
+    margins = []
+    if route_margin is not None:
+        orig_route = O.route
+
+        def recording_route(a, router, top_k):
+            lg = O.linear(a, router)
+            srt = np.sort(lg, axis=-1)[:, ::-1]
+            margins.append(srt[:, top_k - 1] - srt[:, top_k])
+            return orig_route(a, router, top_k)
+
+        O.route = recording_route
+    try:
+        x, trace = O.generate(m, prompt, G, B, tau, keep_logits=True, max_blocks=max_blocks)
+    finally:
+        if route_margin is not None:
+            O.route = orig_route
     b, P = prompt.shape
     L = P + G
     dec = D.Decoder(cfg, [w.to(dev) for w in W], max_batch=b, max_seq=L)
@@ -80,8 +100,23 @@ def teacher_forced(D, cfg, W, prompt, G, B, tau, tol, max_blocks=None):
     cf = torch.empty(b * B, dtype=torch.float32, device=dev)
     dec.set_debug_outputs(lg, tk, cf)
     out = dict(max_err=0.0, sum_err=0.0, n=0, conf_err=0.0, conf_outside=0, tok_mismatch=0, commit_mismatch=0, flagged=0,
-               unflagged_mismatch=0, iterations=len(trace))
-    for rec in trace:
+               unflagged_mismatch=0, iterations=len(trace), route_flagged_rows=0)
+    # routing margins per iteration: each forward calls route once per layer
+    per_iter = []
+    if route_margin is not None:
+        nl = cfg.n_layers
+        b_ = prompt.shape[0]
+        k = 0
+        for rec in trace:
+            rows_fwd = b_ * (P + G) if rec.iteration == 1 else b_ * B
+            ms = []
+            for _ in range(nl):
+                mm = []
+                for _s in range(b_):
+                    mm.append(margins[k]); k += 1
+                ms.append(mm)
+            per_iter.append(ms)
+    for it_i, rec in enumerate(trace):
         s0 = P + rec.block * B
         ids = torch.tensor(rec.x_before, dtype=torch.int32, device=dev)
         mask = torch.tensor(rec.mask_before.astype(np.uint8), device=dev)
@@ -93,6 +128,16 @@ def teacher_forced(D, cfg, W, prompt, G, B, tau, tol, max_blocks=None):
         g_lg = lg.cpu().numpy().reshape(b, B, -1)
         fin = np.isfinite(rec.logits)
         assert np.array_equal(fin, np.isfinite(g_lg))
+        if route_margin is not None:  # rows routed differently may differ beyond delta
+            rows_ok = np.ones((b, B), bool)
+            for si in range(b):
+                mins = np.full(B, np.inf)
+                for lm in per_iter[it_i]:
+                    mg = lm[si]
+                    mg = mg[s0:s0 + B] if len(mg) > B else mg
+                    mins = np.minimum(mins, mg)
+                rows_ok[si] = mins >= route_margin
+            fin = fin & rows_ok[:, :, None]
         e = np.abs(g_lg[fin] - rec.logits[fin])
         out["max_err"] = max(out["max_err"], float(e.max()))
         out["sum_err"] += float(e.sum())
@@ -105,6 +150,16 @@ def teacher_forced(D, cfg, W, prompt, G, B, tau, tol, max_blocks=None):
         g_mask = mask.cpu().numpy().astype(bool)
         g_commit = rec.mask_before[:, s0:s0 + B] & ~g_mask[:, s0:s0 + B]
         fl = flags_for(rec, tau, tol, B, s0)
+        if route_margin is not None:
+            for si in range(b):
+                mins = np.full(B, np.inf)
+                for lm in per_iter[it_i]:
+                    mg = lm[si]
+                    mg = mg[s0:s0 + B] if len(mg) > B else mg  # refresh: all rows; iteration: block rows
+                    mins = np.minimum(mins, mg)
+                rf = mins < route_margin
+                out["route_flagged_rows"] += int(rf.sum())
+                fl[si] |= rf
         out["flagged"] += int(fl.sum())
         tm = g_tok != rec.tok
         cm = g_commit != rec.commit
@@ -272,4 +327,33 @@ def test_errors_are_reported_not_raised_on_device(D):
     with pytest.raises(D.DinferError) as e:
         dec.generate(bad, 32, 32, 0.9)
     assert e.value.status == D.EDEVICE
+    dec.close()
+
+
+# ---------------------------------------------------------------------------
+# small mixture-of-experts model (OLMoE-style routing) on the tensor-core path
+# ---------------------------------------------------------------------------
+SMALL_MOE = inputs.shrink(inputs.LLADA_MOE, n_layers=2, d_model=256, n_heads=2, vocab=2048, mask_id=2047,
+                          n_experts=8, top_k=2, expert_ffn=128)
+
+
+def test_small_moe_teacher_forced(D):
+    W = inputs.make_weights(SMALL_MOE, 0)
+    prompt = inputs.make_prompt(SMALL_MOE, 1, 64).numpy()
+    st, _, _ = teacher_forced(D, SMALL_MOE, W, prompt, 64, 32, 0.9, BF16_SMALL, route_margin=0.02)
+    print(st)
+    assert st["max_err"] < BF16_SMALL["delta"]
+    assert st["mean_err"] < BF16_SMALL["logit_mean"]
+    assert st["unflagged_mismatch"] == 0
+
+
+def test_small_moe_generate_invariants(D):
+    W = [w.to(dev) for w in inputs.make_weights(SMALL_MOE, 0)]
+    P, G, B = 40, 64, 32
+    prompt = inputs.make_prompt(SMALL_MOE, 2, P, device=dev)
+    dec = D.Decoder(SMALL_MOE, W, max_batch=2, max_seq=P + G)
+    a, sa = dec.generate(prompt, G, B, 0.9)
+    b, sb = dec.generate(prompt, G, B, 0.9)
+    check_generation_invariants(a.cpu().numpy(), prompt.cpu().numpy(), G, B, SMALL_MOE.mask_id, sa)
+    assert torch.equal(a, b)
     dec.close()

@@ -164,3 +164,39 @@ def test_attention_key_order_invariance(D, ws):
     b = D.op_attention_bf16(q, k[:, perm].contiguous(), v[:, perm].contiguous(), rows, ws).float()
     torch.cuda.synchronize()
     assert torch.max(torch.abs(a - b)).item() < 2e-2
+
+
+# ---------------------------------------------------------------------------
+# routed expert FFN (router + top-k + permutation + grouped GEMMs + combine)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,d,E,K,fe", [
+    (64, 2048, 64, 8, 1024),   # LLaDA-MoE layer shape, one block of 64 rows
+    (50, 256, 8, 2, 128),      # ragged rows
+    (300, 512, 16, 4, 256),    # several token tiles per expert
+])
+def test_moe_ffn_matches_oracle(D, ws, M, d, E, K, fe):
+    X = inputs.normal_tensor(11, (M, d), 1.0, 7, device=dev)
+    router = inputs.normal_tensor(12, (E, d), 1.0 / np.sqrt(d), 7, device=dev)
+    w13 = inputs.normal_tensor(13, (E, 2 * fe, d), 0.02, 7, device=dev)
+    w2 = inputs.normal_tensor(14, (E, d, fe), 0.02, 7, device=dev)
+    out, ids, w = D.op_moe_ffn_bf16(X, router, w13, w2, K, ws)
+    torch.cuda.synchronize()
+    Xc = X.float().cpu().numpy().astype(np.float64)
+    lw = {"router": router.float().cpu().numpy(), "w13": w13.float().cpu().numpy(), "w2": w2.float().cpu().numpy()}
+    desc = O.Desc(n_layers=1, d_model=d, n_heads=d // 128, head_dim=128, ffn=0, vocab=8, mask_id=7,
+                  n_experts=E, top_k=K, expert_ffn=fe, dtype="bf16")
+    ref = O.moe_ffn(Xc, lw, desc, O.Precision("bf16"))
+    p, idx = O.route(Xc, lw["router"], K)
+    # routing decisions: exact except rows whose k-th and (k+1)-th router logits are within 1e-4
+    logits = Xc @ lw["router"].astype(np.float64).T
+    srt = np.sort(logits, axis=-1)[:, ::-1]
+    near = (srt[:, K - 1] - srt[:, K]) < 1e-4 if K < E else np.zeros(M, bool)
+    g_ids = ids.cpu().numpy()
+    same = (np.sort(g_ids, -1) == np.sort(idx, -1)).all(-1)
+    assert np.all(same | near), int((~same & ~near).sum())
+    np.testing.assert_allclose(w.cpu().numpy()[same], np.take_along_axis(p, g_ids.astype(np.int64), -1)[same],
+                               rtol=1e-5, atol=1e-7)
+    got = out.cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)[same]
+    # expert outputs differ only by rare bf16 roundings of SiLU(g)*u and fp32 accumulation
+    assert np.all(err <= 1e-3 + 1e-2 * np.abs(ref[same])), float(err.max())
