@@ -530,7 +530,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       (!d.n_experts && !make_map(&mact.b, c->act, rows, F, BN)))
     return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
-  const int nthr = D / 16;  // resid_norm threads per row
+  const int nthr = ((D / 16 + 31) / 32) * 32;  // fused-norm threads per row: whole warps
   if (nthr > 512 || D % 128) return fail(c, DINFER_EINVAL, "d_model unsupported by the fused residual norm");
   for (int l = 0; l < d.n_layers; ++l) {
     // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue
@@ -1315,7 +1315,8 @@ extern "C" dinfer_status dinfer_op_moe_ffn_bf16(const void* X, const void* route
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   CK(enqueue_moe_ffn(b, X, M, d, E, K, fe, mr, m13, m2, s));
   CK(cudaMemsetAsync(out, 0, (size_t)M * d * 4, s));
-  CK(launchk(moe_combine_norm_kernel<__nv_bfloat16>, dim3(M), dim3(d / 16), 0, s, 1, out, (const float*)b.y,
+  CK(launchk(moe_combine_norm_kernel<__nv_bfloat16>, dim3(M), dim3(((d / 16 + 31) / 32) * 32), 0, s, 1, out,
+             (const float*)b.y,
              (const float*)b.topk_w, (const int*)b.inv, K, (const __nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr,
              d, 0.f, M, M, 0, (const DevState*)o.st));
   if (topk_id) CK(cudaMemcpyAsync(topk_id, b.topk_id, pairs * 4, cudaMemcpyDeviceToDevice, s));

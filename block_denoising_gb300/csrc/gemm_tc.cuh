@@ -654,10 +654,14 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
     const int bi = r / rows_per_seq;
     src = (size_t)bi * L + st->block_start + (r - bi * rows_per_seq);
   }
-  const int f0 = threadIdx.x * 16;
+  // blockDim is a whole number of warps; threads past d / 16 hold zeros
+  const bool active = threadIdx.x * 16 < d;
+  const int f0 = active ? threadIdx.x * 16 : 0;
   float* hp = h + src * d + f0;
   float x[16];
-  {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = 0.f;
+  if (active) {
     const float4* h4 = reinterpret_cast<const float4*>(hp);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -677,7 +681,7 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
   const unsigned tu0 = (unsigned)t * rp.k_tiles;
   const int c_first = rp.stream_k ? sc.owner(tu0) : 0;
   const int c_last = rp.stream_k ? sc.owner(tu0 + rp.k_tiles - 1) : 0;
-  if (c_first != c_last) {
+  if (active && c_first != c_last) {
     for (int c0 = c_first; c0 <= c_last; c0 += 4) {
       float4 buf[4][4];
 #pragma unroll
@@ -728,9 +732,11 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
     __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
     ow[i] = *reinterpret_cast<uint32_t*>(&b2);
   }
-  uint4* op = reinterpret_cast<uint4*>(out + (size_t)r * d + f0);
-  op[0] = o[0];
-  op[1] = o[1];
+  if (active) {
+    uint4* op = reinterpret_cast<uint4*>(out + (size_t)r * d + f0);
+    op[0] = o[0];
+    op[1] = o[1];
+  }
   pdl_trigger();
 }
 

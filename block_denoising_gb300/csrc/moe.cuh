@@ -141,7 +141,8 @@ __global__ void moe_scatter_kernel(const __nv_bfloat16* __restrict__ xn, int d, 
 }
 
 // h[src] += sum_k w[r, k] * y[inv[r, k]] (slot order); then, if out != NULL,
-// out[r] = bf16(RMSNorm(h[src]) * g).  One CTA per output row, d / 16 threads.
+// out[r] = bf16(RMSNorm(h[src]) * g).  One CTA per output row, whole warps
+// covering d / 16 threads (16 features each).
 template <typename Tg>
 __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict__ h, const float* __restrict__ y,
                                                                const float* __restrict__ topk_w,
@@ -158,10 +159,14 @@ __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict
     const int bi = r / rows_per_seq;
     src = (size_t)bi * L + st->block_start + (r - bi * rows_per_seq);
   }
-  const int f0 = threadIdx.x * 16;
+  // blockDim is a whole number of warps; threads past d / 16 hold zeros
+  const bool active = threadIdx.x * 16 < d;
+  const int f0 = active ? threadIdx.x * 16 : 0;
   float* hp = h + src * d + f0;
   float x[16];
-  {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = 0.f;
+  if (active) {
     const float4* h4 = reinterpret_cast<const float4*>(hp);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict
       x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
     }
   }
-  for (int k = 0; k < K; ++k) {
+  for (int k = 0; k < K && active; ++k) {
     const float w = topk_w[src * K + k];
     const float4* yp = reinterpret_cast<const float4*>(y + (size_t)inv[src * K + k] * d + f0);
 #pragma unroll
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict
       x[4 * i + 3] = fmaf(w, t.w, x[4 * i + 3]);
     }
   }
-  {
+  if (active) {
     float4* h4 = reinterpret_cast<float4*>(hp);
 #pragma unroll
     for (int i = 0; i < 4; ++i) h4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
@@ -212,9 +217,11 @@ __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict
     __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
     ow[i] = *reinterpret_cast<uint32_t*>(&b2);
   }
-  uint4* op = reinterpret_cast<uint4*>(out + (size_t)r * d + f0);
-  op[0] = o[0];
-  op[1] = o[1];
+  if (active) {
+    uint4* op = reinterpret_cast<uint4*>(out + (size_t)r * d + f0);
+    op[0] = o[0];
+    op[1] = o[1];
+  }
   pdl_trigger();
 }
 
