@@ -239,6 +239,10 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def progress(msg):
+    print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -265,8 +269,10 @@ def run_ours(args):
     out_d = torch.empty((b, L), dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
     # warm-up (also captures and instantiates the graphs)
-    for _ in range(args.warmup):
+    progress(f"{args.workload}: weights and context ready; warm-up")
+    for i in range(args.warmup):
         dec.generate(prompt_d, G, B, run.threshold, out=out_d)
+        progress(f"warm-up generation {i + 1} done")
     # ---- device-timed region: inputs resident in HBM -------------------------
     # the 15 GB of weights streamed every iteration exceed the 129 MB L2, so no
     # flush is needed between steps
@@ -287,6 +293,7 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
     t_dev = ev0.elapsed_time(ev1) / 1000.0
+    progress(f"timed generations done ({t_dev:.3f} s)")
     # ---- end to end: host prompt in, host ids out, through the public API ----
     prompt_h = inputs.make_prompt(cfg, b, P).pin_memory()
     out_h = torch.empty((b, L), dtype=torch.int32).pin_memory()
@@ -320,6 +327,7 @@ def run_ours(args):
         us_refresh = 1000.0 * e0.elapsed_time(e1) / 3
     dec.sync()
 
+    progress(f"iteration {us_iter:.1f} us, refresh {us_refresh:.1f} us")
     # ---- dominant kernel: the refresh GEMMs (tensor-bound) --------------------
     hbm, tf_burst, tf_sus, peak_src = load_peaks()
     dom = gemm_roofline(cfg, run, dinfer, stream, tf_sus)

@@ -1,0 +1,480 @@
+// Bidirectional attention of query rows against the dual KV cache on the
+// tcgen05 tensor cores (head_dim 128).
+//
+// Every query row attends over ALL L cached positions of its sequence (the
+// prefix, the block slot just written with the block's fresh K/V, and the
+// suffix) with no mask: o = softmax(q k^T / sqrt(128)) v.
+//
+// One CTA = 128 query rows x one head x one range of 128-key chunks,
+// 192 threads:
+//   warp 0     TMA: Q once, then K and V chunks (2-stage ring, 3-D tensor maps
+//              so that keys past L and rows past the sequence read as zeros);
+//   warp 1     TMEM allocation and the single-thread MMA issue:
+//              S_j = Q K_j^T into one of two TMEM buffers, then O += P_{j-1} V_{j-1}
+//              (V is the MN-major operand, P comes from shared memory);
+//   warps 2-5  one thread per query row: tcgen05.ld of the row of S, online
+//              softmax in the log2 domain, P = bf16(2^(s - m)) written to one of
+//              two shared-memory buffers in the 128-byte-swizzled K-major
+//              layout (so the softmax of chunk j overlaps P_{j-1} V_{j-1}),
+//              final O / l.  Warps whose 32 rows all lie past the sequence's
+//              rows (a 64-row block) only keep the barrier counts.
+// The running max used for the exponent is raised only when a chunk's max
+// exceeds it by more than 8 (P stays <= 2^8); then O (in TMEM) and l are
+// rescaled once.  O / l is exact whatever max was used.
+// Small grids (a batch-1 block) split the keys over up to 8 CTAs of a cluster;
+// partials (m, l, O) are merged through distributed shared memory.
+#pragma once
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace dinfer {
+
+struct AttnTcMaps {
+  CUtensorMap q;  // [batch][rows_per_seq][d], box {64, 128, 1}
+  CUtensorMap k;  // [batch][L][d], box {64, 128, 1}
+  CUtensorMap v;
+};
+
+struct AttnTcArgs {
+  __nv_bfloat16* o;  // [batch * rows_per_seq, d]
+  int d, heads, L, rows_per_seq, q_tiles;
+  int splits, chunks_per_split;
+  float scale_log2;  // log2(e) / sqrt(128)
+  DevState* status;
+};
+
+constexpr int kHd = 128;                // head dimension of the bf16 path
+constexpr int kAtcThreads = 192;
+constexpr int kAtcKeys = 128;           // keys per chunk
+constexpr int kAtcTile = 128 * 128 * 2; // one 128 x 128 bf16 operand (two 64-column swizzle slabs)
+constexpr int kAtcSlab = 128 * 128;     // bytes of one 64-column slab of 128 rows
+constexpr int kAtcStages = 2;
+constexpr int kAtcMaxSplits = 8;
+// Q | K[stages] | V[stages] | P[2] | barriers
+constexpr int kAtcOffK = kAtcTile;
+constexpr int kAtcOffV = kAtcOffK + kAtcStages * kAtcTile;
+constexpr int kAtcOffP = kAtcOffV + kAtcStages * kAtcTile;
+constexpr int kAtcOffBar = kAtcOffP + 2 * kAtcTile;
+constexpr int kAtcSmem = 1024 + kAtcOffBar + 256;
+constexpr int kAtcTmemCols = 512;       // S0 | S1 | O | unused
+constexpr float kAtcLazy = 8.0f;        // log2 growth of the max tolerated before rescaling O
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory descriptor of an MN-major operand with the 128-byte swizzle:
+// 64 MN elements (128 B) per row, one row per K index, 8-row groups 1024 B
+// apart (stride byte offset), MN slabs of 64 elements `lbo` bytes apart
+// (leading byte offset).
+__device__ __forceinline__ uint64_t make_sw128_desc_mn(uint32_t smem_addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+#define ATC_O4(x, b) "=r"(x[(b)]), "=r"(x[(b) + 1]), "=r"(x[(b) + 2]), "=r"(x[(b) + 3])
+#define ATC_O32(x, b)                                                                                      \
+  ATC_O4(x, b), ATC_O4(x, (b) + 4), ATC_O4(x, (b) + 8), ATC_O4(x, (b) + 12), ATC_O4(x, (b) + 16),          \
+      ATC_O4(x, (b) + 20), ATC_O4(x, (b) + 24), ATC_O4(x, (b) + 28)
+#define ATC_I4(x, b) "+r"(x[(b)]), "+r"(x[(b) + 1]), "+r"(x[(b) + 2]), "+r"(x[(b) + 3])
+#define ATC_I32(x, b)                                                                                      \
+  ATC_I4(x, b), ATC_I4(x, (b) + 4), ATC_I4(x, (b) + 8), ATC_I4(x, (b) + 12), ATC_I4(x, (b) + 16),          \
+      ATC_I4(x, (b) + 20), ATC_I4(x, (b) + 24), ATC_I4(x, (b) + 28)
+
+// 128 consecutive TMEM columns of this warp's 32 lanes, one wait for all four
+// loads.  The empty statements after the wait carry the registers, so no use
+// of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 0) : "r"(taddr));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 32) : "r"(taddr + 32));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 64) : "r"(taddr + 64));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 96) : "r"(taddr + 96));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : ATC_I32(x, 0)::"memory");
+  asm volatile("" : ATC_I32(x, 32));
+  asm volatile("" : ATC_I32(x, 64));
+  asm volatile("" : ATC_I32(x, 96));
+}
+
+// 2^x with the PTX approximate base-2 exponential (2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b2);
+}
+
+__global__ void __launch_bounds__(kAtcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ AttnTcMaps maps, const AttnTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kAtcOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;                 // [2]
+  uint64_t* kv_empty = kv_full + kAtcStages;    // [2]
+  uint64_t* s_full = kv_empty + kAtcStages;     // [2]
+  uint64_t* s_empty = s_full + 2;               // [2]
+  uint64_t* p_full = s_empty + 2;               // [2]
+  uint64_t* pv_done = p_full + 2;               // [2]
+  uint64_t* drain = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x % a.q_tiles;
+  const int bi = blockIdx.x / a.q_tiles;
+  const int head = blockIdx.y;
+  const int split = blockIdx.z;
+  const int row0 = qt * 128;
+  const int q_valid = min(128, a.rows_per_seq - row0);
+  const int n_chunks = (a.L + kAtcKeys - 1) / kAtcKeys;
+  const int c_begin = split * a.chunks_per_split;
+  const int nck = max(0, min(n_chunks, c_begin + a.chunks_per_split) - c_begin);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kAtcStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], 128);
+      mbar_init(&p_full[s], 128);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.q);
+    prefetch_tmap(&maps.k);
+    prefetch_tmap(&maps.v);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kAtcTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s[2] = {tmem, tmem + 128};
+  const uint32_t t_o = tmem + 256;
+  const int hc = head * 128;  // first column of this head
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (elect_one_sync()) {
+      pdl_wait();
+      mbar_arrive_expect_tx(q_full, kAtcTile);
+      tma_load_3d(sm, &maps.q, q_full, hc, row0, bi);
+      tma_load_3d(sm + kAtcSlab, &maps.q, q_full, hc + 64, row0, bi);
+      int issued = 0;
+      for (int j = 0; j < nck && !*abort_flag; ++j) {
+        const int st = j % kAtcStages;
+        if (!mbar_wait_diag(&kv_empty[st], ((j / kAtcStages) & 1) ^ 1, abort_flag, a.status, kDiagAttn, 1, j)) break;
+        issued = j + 1;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kAtcTile);
+        const int key0 = (c_begin + j) * kAtcKeys;
+        uint8_t* kb = sm + kAtcOffK + st * kAtcTile;
+        uint8_t* vb = sm + kAtcOffV + st * kAtcTile;
+        tma_load_3d(kb, &maps.k, &kv_full[st], hc, key0, bi);
+        tma_load_3d(kb + kAtcSlab, &maps.k, &kv_full[st], hc + 64, key0, bi);
+        tma_load_3d(vb, &maps.v, &kv_full[st], hc, key0, bi);
+        tma_load_3d(vb + kAtcSlab, &maps.v, &kv_full[st], hc + 64, key0, bi);
+      }
+      if (*abort_flag) {  // let the copies in flight land before the CTA exits
+        mbar_wait_drain(q_full, 0);
+        for (int j = max(0, issued - kAtcStages); j < issued; ++j)
+          mbar_wait_drain(&kv_full[j % kAtcStages], (j / kAtcStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (elect_one_sync()) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 128);
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128) | (1u << 16);  // B (V) MN-major
+      const uint32_t q_addr = smem_u32(sm), p_addr = smem_u32(sm + kAtcOffP);
+      // O += P_i V_i; P_i sits in buffer i & 1
+      auto issue_pv = [&](int i) -> bool {
+        const int st = i % kAtcStages, pb = i & 1;
+        if (!mbar_wait_diag(&p_full[pb], (i >> 1) & 1, abort_flag, a.status, kDiagAttn, 2, i)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sm + kAtcOffV + st * kAtcTile);
+        const uint32_t pa = p_addr + pb * kAtcTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
+          const uint64_t ad = make_sw128_desc(pa + (kk >> 2) * kAtcSlab + (kk & 3) * 32);
+          const uint64_t bd = make_sw128_desc_mn(v_addr + kk * 2048, kAtcSlab);
+          tc_mma_bf16(t_o, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&kv_empty[st]);
+        tc_commit(&pv_done[pb]);
+        return true;
+      };
+      bool ok = mbar_wait_diag(q_full, 0, abort_flag, a.status, kDiagAttn, 3, 0);
+      for (int j = 0; j < nck && ok; ++j) {
+        const int st = j % kAtcStages, sb = j & 1;
+        if (!mbar_wait_diag(&kv_full[st], (j / kAtcStages) & 1, abort_flag, a.status, kDiagAttn, 4, j)) { ok = false; break; }
+        if (!mbar_wait_diag(&s_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag, a.status, kDiagAttn, 5, j)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sm + kAtcOffK + st * kAtcTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // 16 head dims per step
+          const uint64_t ad = make_sw128_desc(q_addr + (kk >> 2) * kAtcSlab + (kk & 3) * 32);
+          const uint64_t bd = make_sw128_desc(k_addr + (kk >> 2) * kAtcSlab + (kk & 3) * 32);
+          tc_mma_bf16(t_s[sb], ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[sb]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && nck > 0) issue_pv(nck - 1);
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------ softmax / output ------------------------------
+    // Every wait's outcome is made warp-uniform: the TMEM accesses are warp-collective.
+    const int q = warp & 3;
+    const int r = q * 32 + lane;            // query row inside the tile (TMEM lane)
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const bool live = q * 32 < q_valid;     // warp-uniform
+    const float sc = a.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nck; ++j) {
+      const int sb = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_diag(&s_full[sb], (j >> 1) & 1, abort_flag, a.status, kDiagAttn, 6, j))) {
+        ok = false;
+        break;
+      }
+      if (!live) {  // rows past the sequence: keep the counts only
+        mbar_arrive(&s_empty[sb]);
+        mbar_arrive(&p_full[sb]);
+        continue;
+      }
+      tc_fence_after();
+      uint32_t sv[128];
+      tmem_ld128(t_s[sb] + lane_off, sv);
+      tc_fence_before();
+      mbar_arrive(&s_empty[sb]);
+      const int nvalid = a.L - (c_begin + j) * kAtcKeys;  // >= 1
+      if (nvalid < kAtcKeys) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= nvalid) sv[i] = 0xff800000u;  // -inf: no key
+      }
+      float mx0 = __uint_as_float(sv[0]), mx1 = __uint_as_float(sv[1]);
+      float mx2 = __uint_as_float(sv[2]), mx3 = __uint_as_float(sv[3]);
+#pragma unroll
+      for (int i = 4; i < 128; i += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sv[i]));
+        mx1 = fmaxf(mx1, __uint_as_float(sv[i + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sv[i + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sv[i + 3]));
+      }
+      const float mj = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;
+      if (j == 0) {
+        m_used = mj;
+      } else {
+        const bool grow = mj > m_used + kAtcLazy;
+        if (__any_sync(0xffffffffu, grow)) {
+          // rescale O: it must hold every product issued so far (P_{j-1} V_{j-1})
+          if (!__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag,
+                                                      a.status, kDiagAttn, 7, j))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = grow ? ex2_approx(m_used - mj) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            float o16[16];
+            tmem_ld16(t_o + lane_off + c * 16, o16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o16[i] *= alpha;
+            tmem_st16(t_o + lane_off + c * 16, o16);
+          }
+          tc_fence_before();
+          l *= alpha;
+          if (grow) m_used = mj;
+        }
+      }
+      // buffer sb is free once P_{j-2} V_{j-2} completed
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[sb], ((j >> 1) & 1) ^ 1, abort_flag, a.status,
+                                                             kDiagAttn, 8, j))) {
+        ok = false;
+        break;
+      }
+      const float nm = -m_used;
+      uint8_t* prow = sm + kAtcOffP + sb * kAtcTile + r * 128;
+      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+#pragma unroll
+      for (int kc = 0; kc < 2; ++kc) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = kc * 64 + u * 8;
+          float p[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) p[e] = ex2_approx(fmaf(__uint_as_float(sv[i + e]), sc, nm));
+          const uint4 w = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                                     pack_bf16x2(p[6], p[7]));
+          // l sums the bf16 values the tensor cores multiply, so that O / l
+          // weights the keys exactly in proportion (one dominant key keeps
+          // weight 1 whatever its rounding)
+          rs0 += __uint_as_float(w.x << 16) + __uint_as_float(w.x & 0xffff0000u);
+          rs1 += __uint_as_float(w.y << 16) + __uint_as_float(w.y & 0xffff0000u);
+          rs2 += __uint_as_float(w.z << 16) + __uint_as_float(w.z & 0xffff0000u);
+          rs3 += __uint_as_float(w.w << 16) + __uint_as_float(w.w & 0xffff0000u);
+          *reinterpret_cast<uint4*>(prow + kc * kAtcSlab + ((u ^ (r & 7)) << 4)) = w;
+        }
+      }
+      l += (rs0 + rs1) + (rs2 + rs3);
+      fence_async_shared();  // the P rows become visible to the tensor cores
+      tc_fence_before();
+      mbar_arrive(&p_full[sb]);
+    }
+    if (live) {
+      if (ok && nck > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[(nck - 1) & 1], ((nck - 1) >> 1) & 1, abort_flag,
+                                                  a.status, kDiagAttn, 9, nck)))
+        ok = false;
+      tc_fence_after();
+      uint32_t ov[128];
+      tmem_ld128(t_o + lane_off, ov);
+      tc_fence_before();
+      if (!ok) l = 1.f;
+      pdl_wait();
+      if (a.splits == 1) {
+        if (r < q_valid) {
+          const float inv = 1.f / l;
+          uint4* og = reinterpret_cast<uint4*>(a.o + ((size_t)bi * a.rows_per_seq + row0 + r) * a.d + hc);
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int i = u * 8;
+            og[u] = make_uint4(pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv),
+                               pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv),
+                               pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv),
+                               pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv));
+          }
+        }
+      } else {
+        // partial (unnormalised O, m, l) in this CTA's shared memory, over the
+        // K ring and the P buffers, merged below
+        float4* po = reinterpret_cast<float4*>(sm + kAtcOffK) + r * 32;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          po[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                              __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+        float* pml = reinterpret_cast<float*>(sm + kAtcOffP) + r * 2;
+        pml[0] = m_used;
+        pml[1] = l;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (a.splits > 1) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (warp >= 2) {
+      // This CTA merges rows [ra, rb) of the tile over all splits.  Every
+      // remote load of a step is issued before any of its values is used.
+      const int t = threadIdx.x - 64;  // 0..127
+      const int rank = (int)cluster.block_rank();
+      const int per = (q_valid + a.splits - 1) / a.splits;
+      const int ra = rank * per, nr = max(0, min(q_valid, ra + per) - ra);
+      const float* pml = reinterpret_cast<const float*>(sm + kAtcOffP);
+      const float* po = reinterpret_cast<const float*>(sm + kAtcOffK);
+      float* coef = reinterpret_cast<float*>(sm);  // [per][8], over this CTA's Q tile
+      if (t < nr) {
+        const int rr = ra + t;
+        float mv[kAtcMaxSplits], lv[kAtcMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kAtcMaxSplits; ++sp) {
+          mv[sp] = -INFINITY;
+          lv[sp] = 0.f;
+          if (sp < a.splits) {
+            const float* rp = cluster.map_shared_rank(pml, sp);
+            mv[sp] = rp[rr * 2];
+            lv[sp] = rp[rr * 2 + 1];
+          }
+        }
+        float mmax = mv[0];
+#pragma unroll
+        for (int sp = 1; sp < kAtcMaxSplits; ++sp) mmax = fmaxf(mmax, mv[sp]);
+        float lsum = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kAtcMaxSplits; ++sp) {
+          mv[sp] = ex2_approx(mv[sp] - mmax);
+          lsum = fmaf(mv[sp], lv[sp], lsum);
+        }
+        const float inv = 1.f / lsum;
+#pragma unroll
+        for (int sp = 0; sp < kAtcMaxSplits; ++sp) coef[t * kAtcMaxSplits + sp] = mv[sp] * inv;
+      }
+      named_bar_sync(1, 128);
+      for (int idx = t; idx < nr * 32; idx += 128) {
+        const int row = idx >> 5, c4 = (idx & 31) * 4;
+        const int rr = ra + row;
+        float4 o[kAtcMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kAtcMaxSplits; ++sp)
+          if (sp < a.splits) o[sp] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(po, sp) + rr * 128 + c4);
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kAtcMaxSplits; ++sp) {
+          if (sp < a.splits) {
+            const float w = coef[row * kAtcMaxSplits + sp];
+            acc0 = fmaf(w, o[sp].x, acc0);
+            acc1 = fmaf(w, o[sp].y, acc1);
+            acc2 = fmaf(w, o[sp].z, acc2);
+            acc3 = fmaf(w, o[sp].w, acc3);
+          }
+        }
+        __nv_bfloat16* og = a.o + ((size_t)bi * a.rows_per_seq + row0 + rr) * a.d + hc + c4;
+        *reinterpret_cast<uint2*>(og) = make_uint2(pack_bf16x2(acc0, acc1), pack_bf16x2(acc2, acc3));
+      }
+    }
+    cluster.sync();  // keep this CTA's shared memory alive until every peer has read it
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) pdl_trigger();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kAtcTmemCols);
+  }
+}
+
+#undef ATC_O4
+#undef ATC_O32
+#undef ATC_I4
+#undef ATC_I32
+
+}  // namespace dinfer

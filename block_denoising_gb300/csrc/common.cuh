@@ -35,12 +35,26 @@ struct DevState {
   int32_t refreshes;
   uint32_t status;
   int32_t any_masked;    // 1 while some sequence of the batch has masks in the block
+  uint32_t diag[4];      // first timed-out wait: (kernel << 8 | site) + 1, block x | y << 16, block z | step << 16, thread
   int32_t committed[kMaxBatch];    // commits of the last iteration, per sequence
   int32_t iters_per_block[kMaxBlocks];
 };
 
 __device__ __forceinline__ void set_status(DevState* st, uint32_t bit) {
   if (st) atomicOr(&st->status, bit);
+}
+
+// Record the first wait that timed out (kernel and site codes are the
+// kernel's own) together with the CTA, the pipeline step and the thread.
+constexpr uint32_t kDiagGemm = 1, kDiagLmHead = 2, kDiagAttn = 3;
+__device__ __forceinline__ void record_timeout(DevState* st, uint32_t kernel, uint32_t site, uint32_t step) {
+  if (!st) return;
+  atomicOr(&st->status, ST_WAIT_TIMEOUT);
+  if (atomicCAS(&st->diag[0], 0u, ((kernel << 8) | site) + 1u) == 0u) {
+    st->diag[1] = blockIdx.x | (blockIdx.y << 16);
+    st->diag[2] = blockIdx.z | (step << 16);
+    st->diag[3] = threadIdx.x;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -138,6 +152,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       return false;
     }
   }
+}
+
+// mbar_wait that records where it gave up when its own bound ran out.
+__device__ __forceinline__ bool mbar_wait_diag(uint64_t* bar, uint32_t parity, volatile int* abort, DevState* st,
+                                               uint32_t kernel, uint32_t site, uint32_t step) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      record_timeout(st, kernel, site, step);
+      return false;
+    }
+  }
+}
+
+// Wait for a phase whatever the abort flag says (operations already issued
+// by this CTA: copies in flight, committed MMAs), bounded by kWaitCycles / 4.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles / 4) return false;
+  return true;
 }
 
 // ---------------------------------------------------------------------------

@@ -135,7 +135,8 @@ __device__ __forceinline__ void finalize_and_commit(const DecodeArgs& d, int tid
       if (st->iteration > d.B) set_status(st, ST_ITER_OVERFLOW);
     }
     st->any_masked = any_left_sh;
-    if (d.use_cond) cudaGraphSetConditional(d.cond, any_left_sh ? 1u : 0u);
+    // a device-side error ends the block loop (and, through advance_block, the sequence)
+    if (d.use_cond) cudaGraphSetConditional(d.cond, (any_left_sh && st->status == 0u) ? 1u : 0u);
   }
 }
 

@@ -23,6 +23,7 @@
 #include "../../include/dinfer.h"
 #include "../../include/dinfer_ops.h"
 #include "attention.cuh"
+#include "attention_tc.cuh"
 #include "gemm_tc.cuh"
 #include "lmhead_tc.cuh"
 #include "moe.cuh"
@@ -62,6 +63,23 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// bf16 tensor [batch][rows][cols] (row-major, packed), boxes of 128 rows x 64
+// columns of one batch entry with the 128-byte swizzle; rows past `rows` read
+// as zeros.
+bool make_map3(CUtensorMap* m, const void* base, uint64_t batch, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0) return false;
+  cuuint64_t dims[3] = {cols, rows, batch};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -126,7 +144,7 @@ bool set_smem_attrs() {
                              LmCfg<128>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(lmhead_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              LmCfg<256>::kSmem) == cudaSuccess;
-  ok &= cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem) ==
+  ok &= cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtcSmem) ==
         cudaSuccess;
   ok &= cudaFuncSetAttribute(lmhead_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
         cudaSuccess;
@@ -328,23 +346,37 @@ cudaError_t launch_lmhead_tc(const GemmMaps& maps, GemmArgs ga, LmArgs la, int B
 struct AttnPlan {
   int q_tiles, splits, cps;
 };
-// Split the keys of small grids (a batch-1 block: heads x 1 query tile) over
-// up to 8 CTAs of a cluster so that about two CTAs run per SM.
+// One CTA per SM (about 198 KB of shared memory each).  Grids smaller than
+// the SM count (a batch-1 block: heads x 1 query tile) split the keys over up
+// to 8 CTAs of a cluster so that the grid fills the SMs once.
 AttnPlan plan_attention(int batch, int rows_per_seq, int heads, int L) {
   AttnPlan p;
-  p.q_tiles = (rows_per_seq + 63) / 64;
-  const int n_chunks = (L + kKeyChunk - 1) / kKeyChunk;
+  p.q_tiles = (rows_per_seq + 127) / 128;
+  const int n_chunks = (L + kAtcKeys - 1) / kAtcKeys;
   const int base = batch * p.q_tiles * heads;
-  int want = (2 * num_sms() + base - 1) / base;
-  want = std::max(1, std::min(std::min(want, n_chunks), kMaxAttnSplits));
+  int want = num_sms() / base;
+  want = std::max(1, std::min(std::min(want, n_chunks), 8));
   p.cps = (n_chunks + want - 1) / want;
   p.splits = (n_chunks + p.cps - 1) / p.cps;
   return p;
 }
 
-cudaError_t launch_attention(const AttnArgs& aa, int batch, cudaStream_t s) {
-  dim3 g(batch * aa.q_tiles, aa.heads, aa.splits);
-  return launchk(attn_bf16_kernel, g, dim3(kAttnThreads), kAttnSmem, s, aa.splits, aa);
+// q [batch * rows_per_seq, heads * 128], k/v [batch, L, heads * 128] -> o
+cudaError_t launch_attention(const void* q, const void* k, const void* v, void* o, int batch, int rows_per_seq,
+                             int heads, int L, const AttnPlan& ap, DevState* status, cudaStream_t s) {
+  const int d = heads * kHd;
+  AttnTcMaps maps;
+  if (!make_map3(&maps.q, q, batch, rows_per_seq, d) || !make_map3(&maps.k, k, batch, L, d) ||
+      !make_map3(&maps.v, v, batch, L, d))
+    return cudaErrorInvalidValue;
+  AttnTcArgs aa{};
+  aa.o = (__nv_bfloat16*)o;
+  aa.d = d; aa.heads = heads; aa.L = L; aa.rows_per_seq = rows_per_seq;
+  aa.q_tiles = ap.q_tiles; aa.splits = ap.splits; aa.chunks_per_split = ap.cps;
+  aa.scale_log2 = 1.4426950408889634f / sqrtf((float)kHd);
+  aa.status = status;
+  dim3 g(batch * ap.q_tiles, heads, ap.splits);
+  return launchk(attn_tc_kernel, g, dim3(kAtcThreads), kAtcSmem, s, ap.splits, maps, aa);
 }
 
 struct GraphSet {
@@ -553,17 +585,8 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       CK(launch_gemm_tc(m, a, BN, s));
     }
     // a3: attention over the dual cache
-    {
-      AttnArgs aa{};
-      aa.q = (const __nv_bfloat16*)c->q;
-      aa.k = (const __nv_bfloat16*)c->kc_layer(l);
-      aa.v = (const __nv_bfloat16*)c->vc_layer(l);
-      aa.o = (__nv_bfloat16*)c->attn_o;
-      aa.d = D; aa.heads = H; aa.L = f.L; aa.rows_per_seq = f.rows_per_seq;
-      aa.q_tiles = ap.q_tiles; aa.splits = ap.splits; aa.chunks_per_split = ap.cps;
-      aa.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-      CK(launch_attention(aa, f.batch, s));
-    }
+    CK(launch_attention(c->q, c->kc_layer(l), c->vc_layer(l), c->attn_o, f.batch, f.rows_per_seq, H, f.L, ap,
+                        c->st, s));
     // a4: O projection + residual, fused with the FFN norm
     {
       GemmMaps m = mo;
@@ -720,8 +743,11 @@ dinfer_status read_status(dinfer_ctx* c) {
   CK(cudaMemcpyAsync(c->st_host, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
   CK(cudaStreamSynchronize(c->stream));
   if (c->st_host->status)
-    return fail(c, DINFER_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad token, 4 NaN confidence, 8 "
-                "iteration overflow)", c->st_host->status);
+    return fail(c, DINFER_EDEVICE,
+                "device status word 0x%x (1 wait timeout, 2 bad token, 4 NaN confidence, 8 iteration overflow); "
+                "first timeout: site 0x%x block 0x%x z/step 0x%x thread %u",
+                c->st_host->status, c->st_host->diag[0], c->st_host->diag[1], c->st_host->diag[2],
+                c->st_host->diag[3]);
   return DINFER_OK;
 }
 
@@ -1256,17 +1282,13 @@ dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void*
   dinfer_ctx* c = nullptr;
   if (!q || !k || !v || !out) return fail(c, DINFER_EINVAL, "NULL operand");
   if (batch < 1 || rows_per_seq < 1 || L < 1 || heads < 1) return fail(c, DINFER_EINVAL, "unsupported shape");
-  (void)workspace;
-  (void)workspace_bytes;
+  OpWs o{};
+  if (workspace && !op_ws(workspace, workspace_bytes, o)) return fail(c, DINFER_EINVAL, "workspace too small");
   if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
   const AttnPlan ap = plan_attention(batch, rows_per_seq, heads, L);
-  AttnArgs aa{};
-  aa.q = (const __nv_bfloat16*)q; aa.k = (const __nv_bfloat16*)k; aa.v = (const __nv_bfloat16*)v;
-  aa.o = (__nv_bfloat16*)out;
-  aa.d = heads * kHd; aa.heads = heads; aa.L = L; aa.rows_per_seq = rows_per_seq;
-  aa.q_tiles = ap.q_tiles; aa.splits = ap.splits; aa.chunks_per_split = ap.cps;
-  aa.scale_log2 = 1.4426950408889634f / sqrtf((float)kHd);
-  CK(launch_attention(aa, batch, reinterpret_cast<cudaStream_t>(stream)));
+  if (launch_attention(q, k, v, out, batch, rows_per_seq, heads, L, ap, o.st,
+                       reinterpret_cast<cudaStream_t>(stream)) == cudaErrorInvalidValue)
+    return fail(c, DINFER_EINVAL, "tensor map encoding failed (alignment?)");
   CK(cudaGetLastError());
   return DINFER_OK;
 }

@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncthreads();
-  if (*p.abort_flag && threadIdx.x == 0) set_status(a.status, ST_WAIT_TIMEOUT);
+  if (*p.abort_flag && threadIdx.x == 0) record_timeout(a.status, kDiagGemm, 0, 0);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);

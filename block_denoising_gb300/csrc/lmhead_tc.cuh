@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncthreads();
-  if (*p.abort_flag && threadIdx.x == 0) set_status(ga.status, ST_WAIT_TIMEOUT);
+  if (*p.abort_flag && threadIdx.x == 0) record_timeout(ga.status, kDiagLmHead, 0, 0);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);

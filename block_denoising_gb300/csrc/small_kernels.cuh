@@ -302,6 +302,7 @@ __global__ void init_sequence_kernel(const int32_t* __restrict__ prompt, int32_t
     st->total_iterations = 0;
     st->refreshes = 0;
     st->status = 0;
+    st->diag[0] = 0;
     st->any_masked = 1;
   }
 }
@@ -314,14 +315,14 @@ __global__ void begin_block_kernel(DevState* st) {
 
 // inner loop condition after the refresh: iterate while masks remain
 __global__ void set_inner_cond_kernel(DevState* st, cudaGraphConditionalHandle h) {
-  cudaGraphSetConditional(h, st->any_masked ? 1u : 0u);
+  cudaGraphSetConditional(h, (st->any_masked && st->status == 0u) ? 1u : 0u);
 }
 
 // end of a block: move to the next one; outer loop continues while blocks remain
 __global__ void advance_block_kernel(DevState* st, int B, cudaGraphConditionalHandle h, int use_cond) {
   st->block_index += 1;
   st->block_start += B;
-  if (use_cond) cudaGraphSetConditional(h, st->block_index < st->n_blocks ? 1u : 0u);
+  if (use_cond) cudaGraphSetConditional(h, (st->block_index < st->n_blocks && st->status == 0u) ? 1u : 0u);
 }
 
 // geometry of a stand-alone prefill / block step
@@ -330,6 +331,7 @@ __global__ void set_block_kernel(DevState* st, int block_start, int reset) {
   if (reset) {
     st->iteration = 0;
     st->status = 0;
+    st->diag[0] = 0;
     st->block_index = 0;
   }
 }

@@ -171,6 +171,13 @@ class OpWorkspace:
         self.buf = torch.zeros(n, dtype=torch.uint8, device=device)
         self.nbytes = n
 
+    def check(self):
+        """Raise if a kernel run on this workspace reported a device-side error
+        (the status word of the device state at the head of the workspace)."""
+        st = int(self.buf[:32].view(torch.int32)[6].item())
+        if st:
+            raise DinferError(EDEVICE, f"device status 0x{st:x}")
+
 
 def _stream_ptr():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)

@@ -46,8 +46,11 @@ dinfer_status dinfer_op_lmhead_bf16(const void* X, const void* W, int32_t M, int
  *   o[r, h, :] = sum_j softmax_j(q[r, h, :] . k[b, j, h, :] / sqrt(128)) v[b, j, h, :]
  * over all j < L of sequence b = r / rows_per_seq, no mask.  q, o
  * [batch * rows_per_seq, heads * 128] bf16; k, v [batch, L, heads * 128] bf16.
- * Keys are split over up to 8 CTAs of a thread-block cluster when the grid
- * would be small; the workspace is not used (may be NULL). */
+ * One CTA per 128 query rows x head on the tcgen05 tensor cores; when that
+ * grid has fewer CTAs than the GPU has SMs, the keys are split over up to 8
+ * CTAs of a thread-block cluster.  All pointers 16-byte aligned.  The
+ * workspace may be NULL; when given, a wait that timed out sets its status
+ * word. */
 dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void* v, void* o, int32_t batch,
                                        int32_t rows_per_seq, int32_t L, int32_t heads, void* workspace,
                                        size_t workspace_bytes, void* stream);

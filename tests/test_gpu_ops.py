@@ -133,6 +133,9 @@ def test_lmhead_never_picks_the_mask_token(D, ws):
     (1, 16, 96, 2),       # tiny, ragged key chunk
     (2, 100, 100, 2),     # refresh-like: every position queries, ragged query tile
     (2, 32, 1280, 4),     # batch of sequences
+    (1, 300, 700, 2),     # three query tiles and five key chunks, both ragged
+    (1, 64, 4160, 16),    # LLaDA-MoE block over a long cache (7 key splits)
+    (1, 1536, 1536, 32),  # LLaDA-8B refresh: every position queries (rows sampled)
 ])
 def test_attention_matches_oracle(D, ws, batch, rows, L, heads):
     d = heads * 128
@@ -141,13 +144,41 @@ def test_attention_matches_oracle(D, ws, batch, rows, L, heads):
     v = inputs.normal_tensor(9, (batch, L, d), 1.0, 5, device=dev)
     o = D.op_attention_bf16(q, k, v, rows, ws)
     torch.cuda.synchronize()
+    ws.check()
+    # every row of small cases; at the refresh size rows spanning all query tiles
+    sel = np.arange(rows) if rows * heads <= 4096 else np.unique(np.linspace(0, rows - 1, 40).astype(int))
+    got = o.float().cpu().numpy().reshape(batch, rows, heads, 128)[:, sel]
+    qc = q.float().cpu().numpy().reshape(batch, rows, heads, 128)[:, sel]
+    kc = k.float().cpu().numpy().reshape(batch, L, heads, 128)
+    vc = v.float().cpu().numpy().reshape(batch, L, heads, 128)
+    for b in range(batch):
+        ref = O.attention(qc[b], kc[b], vc[b])
+        # bf16 output rounding (2^-9 relative) plus bf16 probabilities in P.V
+        err = np.abs(got[b] - ref)
+        assert np.all(err <= 4e-3 * np.abs(ref) + 4e-3), float(err.max())
+
+
+@pytest.mark.parametrize("batch,rows,L,heads", [(1, 64, 1536, 4), (1, 256, 900, 2)])
+def test_attention_growing_scores(D, ws, batch, rows, L, heads):
+    # Key norms ramp up along the cache, so the running max of a query row keeps
+    # growing from chunk to chunk (the rescaling of the accumulated output);
+    # every other query row is damped, so within one warp some rows rescale and
+    # their neighbours do not.
+    d = heads * 128
+    ramp = torch.linspace(0.25, 6.0, L, device=dev).view(1, L, 1)
+    damp = torch.where(torch.arange(rows, device=dev) % 2 == 1, 0.05, 1.0).repeat(batch).view(-1, 1)
+    q = (inputs.normal_tensor(7, (batch * rows, d), 1.0, 8, device=dev).float() * damp).bfloat16()
+    k = (inputs.normal_tensor(8, (batch, L, d), 1.0, 8, device=dev).float() * ramp).bfloat16()
+    v = inputs.normal_tensor(9, (batch, L, d), 1.0, 8, device=dev)
+    o = D.op_attention_bf16(q, k, v, rows, ws)
+    torch.cuda.synchronize()
+    ws.check()
     got = o.float().cpu().numpy().reshape(batch, rows, heads, 128)
     qc = q.float().cpu().numpy().reshape(batch, rows, heads, 128)
     kc = k.float().cpu().numpy().reshape(batch, L, heads, 128)
     vc = v.float().cpu().numpy().reshape(batch, L, heads, 128)
     for b in range(batch):
         ref = O.attention(qc[b], kc[b], vc[b])
-        # bf16 output rounding (2^-9 relative) plus bf16 probabilities in P.V
         err = np.abs(got[b] - ref)
         assert np.all(err <= 4e-3 * np.abs(ref) + 4e-3), float(err.max())
 
