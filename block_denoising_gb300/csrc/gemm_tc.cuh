@@ -175,33 +175,48 @@ __device__ __forceinline__ void load_stage_b(const GemmMaps& maps, uint8_t* stag
   tma_load_2d(stage + GemmCfg<BN>::kStageA, &maps.b, bar, k * 64, b_row, pol_x);
 }
 
-// One 16-column chunk of the finished accumulator for output feature row
-// `row` (0..127 inside the tile) and tokens m0 .. m0+15.
+// RoPE factors of output row `row` of tile nt for the 16 tokens m0..m0+15
+// (q and k rows; v rows need none).  base_pos: absolute position of token 0
+// of a sequence's rows (the block start for block rows, 0 for a refresh).
+// bf16 models have head_dim 128, so a 128-row tile is one head of q, k or v
+// and row is the feature inside the head; its rotation frequency is row % 64.
+// Token -> (sequence, row) steps along the chunk: one division per chunk.
+__device__ __forceinline__ void qkv_rope_fetch(const GemmArgs& a, int base_pos, int row, int nt, int m0,
+                                               float (&cs)[16], float (&sn)[16]) {
+  if (nt * 128 >= 2 * a.d_model) return;
+  const int j = row & 63;
+  int r = m0 - (m0 / a.rows_per_seq) * a.rows_per_seq;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const int pos = base_pos + r;
+    cs[c] = __ldg(a.rope_cos + pos * 64 + j);
+    sn[c] = __ldg(a.rope_sin + pos * 64 + j);
+    if (++r == a.rows_per_seq) r = 0;
+  }
+}
+
+// Epilogue of 16 tokens (m0..m0+15) of output row `row` of tile nt.  QKV
+// tiles take their RoPE factors from `rope` (cos then sin, fetched ahead by
+// the caller) or, when it is NULL, load them here.
 template <int BN>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16], int row, int nt, int m0,
-                                               float* xchg, int m_lim, int out_base) {
+                                               float* xchg, int m_lim, int out_base,
+                                               const float (*rope)[16] = nullptr, int base_pos_in = -1) {
   if (a.q_out != nullptr) {
     // ---- QKV: RoPE pairs (i, i + 64) sit in rows row and row ^ 64 ----
-    const int n = nt * 128 + row;
     const int d = a.d_model;
-    const int which = n / d;          // 0 q, 1 k, 2 v
-    const int nn = n - which * d;     // feature inside q/k/v
-    const int hd = a.head_dim;
-    const int i = nn % hd;
-    const int half = hd >> 1;
-    const int j = i % half;
-    const int base_pos = a.pos_from_state ? a.state->block_start : 0;
-    // every global load of the chunk is issued before any store
+    const int which = (nt * 128) / d;           // 0 q, 1 k, 2 v
+    const int nn = nt * 128 - which * d + row;  // feature inside q/k/v
+    const int base_pos = base_pos_in >= 0 ? base_pos_in : (a.pos_from_state ? a.state->block_start : 0);
     float cs[16], sn[16];
-    if (which < 2) {
+    if (rope) {
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const int m = min(m0 + c, a.M - 1);
-        const int bi = m / a.rows_per_seq;
-        const int pos = base_pos + (m - bi * a.rows_per_seq);
-        cs[c] = __ldg(a.rope_cos + pos * half + j);
-        sn[c] = __ldg(a.rope_sin + pos * half + j);
+        cs[c] = rope[0][c];
+        sn[c] = rope[1][c];
       }
+    } else {
+      qkv_rope_fetch(a, base_pos, row, nt, m0, cs, sn);
     }
     float* mine = xchg + row * 17;
 #pragma unroll
@@ -209,21 +224,23 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
     named_bar_sync(1, 128);
     const float* part = xchg + (row ^ 64) * 17;
     float o[16];
+    const float sgn = row < 64 ? -1.f : 1.f;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float p = part[c];
-      o[c] = (which == 2) ? v[c] : ((i < half) ? (v[c] * cs[c] - p * sn[c]) : (v[c] * cs[c] + p * sn[c]));
-    }
+    for (int c = 0; c < 16; ++c) o[c] = (which == 2) ? v[c] : fmaf(sgn * part[c], sn[c], v[c] * cs[c]);
     named_bar_sync(1, 128);
-    __nv_bfloat16* __restrict__ dst = which == 0 ? a.q_out : (which == 1 ? a.k_cache : a.v_cache);
+    __nv_bfloat16* __restrict__ dst = (which == 0 ? a.q_out : (which == 1 ? a.k_cache : a.v_cache)) + nn;
+    int bi = m0 / a.rows_per_seq;
+    int r = m0 - bi * a.rows_per_seq;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int m = m0 + c;
       if (m < a.M) {
-        const int bi = m / a.rows_per_seq;
-        const int pos = base_pos + (m - bi * a.rows_per_seq);
-        const size_t off = which == 0 ? (size_t)m * d + nn : ((size_t)bi * a.seq_len + pos) * d + nn;
-        dst[off] = __float2bfloat16_rn(o[c]);
+        const size_t orow = which == 0 ? (size_t)m : (size_t)bi * a.seq_len + base_pos + r;
+        dst[orow * d] = __float2bfloat16_rn(o[c]);
+      }
+      if (++r == a.rows_per_seq) {
+        r = 0;
+        ++bi;
       }
     }
   } else if (a.a_mode == A_PAIR) {
@@ -239,7 +256,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const float g = v[c];
-        o[c] = g / (1.0f + expf(-g)) * up[c];
+        o[c] = __fdividef(g, 1.0f + __expf(-g)) * up[c];  // rounded to bf16 next
       }
     }
     named_bar_sync(1, 128);
@@ -510,18 +527,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------ epilogue ------------------------------
     pdl_wait();  // global writes only after the preceding kernel completed
+    const int base_pos = (a.q_out != nullptr && a.pos_from_state) ? a.state->block_start : 0;
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;          // output feature row inside the tile
+    float rope[2][16];  // QKV: RoPE factors of the next chunk to finish
     for (int j = 0; j < sl.nseg; ++j) {
       int t, kb, ke;
       sl.seg(j, t, kb, ke);
       const TileRef tr = decode_tile<BN>(a, t);
       const int acc = j & 1;
       const uint32_t use = j >> 1;
+      const bool whole = (kb == 0 && ke == a.k_tiles);
+      // loads of the tile's first RoPE factors overlap its main loop
+      if (a.q_out != nullptr && whole) qkv_rope_fetch(a, base_pos, row, tr.nt, tr.mt * BN, rope[0], rope[1]);
       if (!mbar_wait(&p.tfull[acc], use & 1, p.abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      const bool whole = (kb == 0 && ke == a.k_tiles);
       if (!whole) {
         // partial tile: slot 0 holds this CTA's part of its first tile, slot 1
         // of its last; layout [row][BN] so each thread moves whole float4s
@@ -550,11 +571,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_arrive(&p.tempty[acc]);
         continue;
       }
+      if (a.q_out != nullptr) {
+        // QKV: the RoPE factors of chunk c + 1 load while chunk c is finished
+        float next[2][16];
 #pragma unroll 1
-      for (int c = 0; c < BN / 16; ++c) {
-        float v[16];
-        tmem_ld16(tbase + c * 16, v);
-        epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg, tr.m_lim, tr.out_base);
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+          tmem_ld16(tbase + c * 16, v);
+          if (c + 1 < BN / 16) qkv_rope_fetch(a, base_pos, row, tr.nt, tr.mt * BN + (c + 1) * 16, next[0], next[1]);
+          epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg, tr.m_lim, tr.out_base, rope, base_pos);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            rope[0][i] = next[0][i];
+            rope[1][i] = next[1][i];
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+          tmem_ld16(tbase + c * 16, v);
+          epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg, tr.m_lim, tr.out_base);
+        }
       }
       tc_fence_before();
       mbar_arrive(&p.tempty[acc]);
