@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s[2] = {tmem, tmem + 128};
+  // S buffer b at columns 128 b (computed, not an indexed array: local memory
+  // would live in L2 on an SM whose memory is carved out as shared memory)
   const uint32_t t_o = tmem + 256;
   const int hc = head * 128;  // first column of this head
 
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
         for (int kk = 0; kk < 8; ++kk) {  // 16 head dims per step
           const uint64_t ad = make_sw128_desc(q_addr + (kk >> 2) * kAtcSlab + (kk & 3) * 32);
           const uint64_t bd = make_sw128_desc(k_addr + (kk >> 2) * kAtcSlab + (kk & 3) * 32);
-          tc_mma_bf16(t_s[sb], ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16((tmem + sb * 128), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[sb]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
       }
       tc_fence_after();
       uint32_t sv[128];
-      tmem_ld128(t_s[sb] + lane_off, sv);
+      tmem_ld128((tmem + sb * 128) + lane_off, sv);
       tc_fence_before();
       mbar_arrive(&s_empty[sb]);
       const int nvalid = a.L - (c_begin + j) * kAtcKeys;  // >= 1

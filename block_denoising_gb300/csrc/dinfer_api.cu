@@ -25,6 +25,7 @@
 #include "attention.cuh"
 #include "attention_tc.cuh"
 #include "gemm_tc.cuh"
+#include "layer_chain.cuh"
 #include "lmhead_tc.cuh"
 #include "moe.cuh"
 #include "noalloc.cuh"
@@ -145,6 +146,8 @@ bool set_smem_attrs() {
   ok &= cudaFuncSetAttribute(lmhead_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              LmCfg<256>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtcSmem) ==
+        cudaSuccess;
+  ok &= cudaFuncSetAttribute(layer_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem) ==
         cudaSuccess;
   ok &= cudaFuncSetAttribute(lmhead_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
         cudaSuccess;
@@ -418,6 +421,8 @@ struct dinfer_ctx {
   DevState* st = nullptr;
   DevState* st_host = nullptr;  // pinned
   float* gemm_ws = nullptr;
+  uint32_t* chain_sync = nullptr;  // layer-chain counters (zero between launches)
+  int use_chain = 0;               // 1: persistent layer chain for cached iterations (DINFER_LAYER_CHAIN=1)
   SoftmaxState* lm_part = nullptr;
   int* lm_ticket = nullptr;
 
@@ -538,6 +543,98 @@ struct Fwd {
   float threshold;
 };
 
+// The persistent layer chain serves cached iterations of dense bf16 models
+// whose block rows fit one token tile, when its segment table and norm
+// layout cover the shapes.
+bool chain_fits(const dinfer_ctx* c, const Fwd& f) {
+  const dinfer_model_desc& d = c->desc;
+  if (!c->bf16 || !c->use_chain || d.n_experts || f.refresh || f.rows > 64) return false;
+  const int G = num_sms();
+  const int D = d.d_model, F = d.ffn;
+  if (f.rows > G || D % 128 || F % 64 || F / 64 > kChainMaxGuTiles)
+    return false;
+  if (3 * D / 128 > kChainMaxQkvTiles) return false;
+  // segments of one CTA: a stream-K range spans at most ceil(range / k) + 1 tiles
+  auto sk = [&](long long tiles, long long kt) {
+    const long long per = (tiles * kt + G - 1) / G;
+    return (per + kt - 1) / kt + 1;
+  };
+  auto whole = [&](long long tiles) { return (tiles + G - 1) / G; };
+  const long long n = sk(D / 128, D / 64) + whole(F / 64) + sk(D / 128, F / 64) + whole(3 * D / 128);
+  return n <= kChainMaxSegs;
+}
+
+// Layer l from the O projection to the next layer's QKV (see layer_chain.cuh).
+cudaError_t launch_chain(dinfer_ctx* c, const Fwd& f, int l, const GemmMaps& mx, const GemmMaps& mo,
+                         const GemmMaps& mact, cudaStream_t s) {
+  const dinfer_model_desc& d = c->desc;
+  const int D = d.d_model, F = d.ffn, rows = f.rows, G = num_sms();
+  const bool last = l + 1 == d.n_layers;
+  ChainMaps cm{};
+  ChainArgs ca{};
+  cm.m[CH_O] = mo;
+  cm.m[CH_O].a[0] = c->m_wo[l];
+  cm.m[CH_GU] = mx;
+  cm.m[CH_GU].a[0] = c->m_wg[l];
+  cm.m[CH_GU].a[1] = c->m_wu[l];
+  cm.m[CH_DN] = mact;
+  cm.m[CH_DN].a[0] = c->m_wd[l];
+  GemmArgs& o = ca.g[CH_O];
+  o.M = rows; o.N = D; o.K = D; o.m_tiles = 1; o.n_tiles = D / 128; o.k_tiles = D / 64; o.stream_k = 1;
+  // the partial slots of the four phases: [G][2][64 * 128] fp32 each
+  float* ws[CH_PHASES];
+  for (int ph = 0; ph < CH_PHASES; ++ph) ws[ph] = c->gemm_ws + (size_t)ph * G * 2 * 64 * 128;
+  o.a_mode = A_SINGLE; o.resid = c->h; o.ws = ws[CH_O]; o.grid = std::min(G, (D / 128) * (D / 64));
+  o.slot_tok_major = 1;
+  o.status = c->st; o.state = c->st;
+  GemmArgs& gu = ca.g[CH_GU];
+  gu.M = rows; gu.N = F; gu.K = D; gu.m_tiles = 1; gu.n_tiles = F / 64; gu.k_tiles = D / 64;
+  // gate/up and QKV: whole tiles dealt over the last CTAs (the first ones
+  // run the row norms), as many tiles per CTA as whole-tile GEMMs take
+  auto whole_grid = [&](int tiles) {
+    const int per = (tiles + G - 1) / G;
+    return (tiles + per - 1) / per;
+  };
+  gu.a_mode = A_PAIR; gu.out_bf16 = (__nv_bfloat16*)c->act; gu.ldo = F; gu.stream_k = 0;
+  gu.ws = ws[CH_GU]; gu.grid = whole_grid(F / 64);
+  ca.cta0[CH_GU] = G - gu.grid;
+  gu.status = c->st; gu.state = c->st;
+  GemmArgs& dn = ca.g[CH_DN];
+  dn.M = rows; dn.N = D; dn.K = F; dn.m_tiles = 1; dn.n_tiles = D / 128; dn.k_tiles = F / 64; dn.stream_k = 1;
+  dn.a_mode = A_SINGLE; dn.resid = c->h; dn.ws = ws[CH_DN];
+  dn.grid = std::min(G, (D / 128) * (F / 64));
+  dn.slot_tok_major = 1; dn.status = c->st; dn.state = c->st;
+  if (!last) {
+    cm.m[CH_QKV] = mx;
+    cm.m[CH_QKV].a[0] = c->m_wq[l + 1];
+    cm.m[CH_QKV].a[1] = c->m_wk[l + 1];
+    cm.m[CH_QKV].a[2] = c->m_wv[l + 1];
+    GemmArgs& qk = ca.g[CH_QKV];
+    qk.M = rows; qk.N = 3 * D; qk.K = D; qk.m_tiles = 1; qk.n_tiles = 3 * D / 128; qk.k_tiles = D / 64;
+    qk.a_mode = A_THREE; qk.a_rows = D;
+    qk.q_out = (__nv_bfloat16*)c->q;
+    qk.k_cache = (__nv_bfloat16*)c->kc_layer(l + 1);
+    qk.v_cache = (__nv_bfloat16*)c->vc_layer(l + 1);
+    qk.rope_cos = c->rope_cos; qk.rope_sin = c->rope_sin;
+    qk.d_model = D; qk.head_dim = d.head_dim;
+    qk.rows_per_seq = f.rows_per_seq; qk.seq_len = f.L; qk.pos_from_state = f.pos_from_state;
+    qk.state = c->st; qk.status = c->st; qk.stream_k = 0;
+    qk.ws = ws[CH_QKV]; qk.grid = whole_grid(3 * D / 128);
+    ca.cta0[CH_QKV] = G - qk.grid;
+  }
+  ca.has_qkv = last ? 0 : 1;
+  ca.M = rows;
+  ca.d = D;
+  ca.eps = d.rms_eps;
+  ca.g_ffn = (const __nv_bfloat16*)c->LW(l, 5);
+  ca.g_next = (const __nv_bfloat16*)(last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0));
+  ca.h = c->h;
+  ca.xn = (__nv_bfloat16*)c->xn;
+  ca.sync = c->chain_sync;
+  ca.status = c->st;
+  return launchk(layer_chain_kernel, dim3(G), dim3(kGemmThreads), kChainSmem, s, 1, cm, ca);
+}
+
 // Enqueue one forward over f.rows rows, final norm of the block rows, LM head,
 // decode and (optionally) the commit.  Works eagerly or under stream capture.
 // bf16 layer sequence (per layer, all on the tensor-core path):
@@ -564,9 +661,11 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
   const int nthr = ((D / 16 + 31) / 32) * 32;  // fused-norm threads per row: whole warps
   if (nthr > 512 || D % 128) return fail(c, DINFER_EINVAL, "d_model unsupported by the fused residual norm");
+  const bool chain = chain_fits(c, f);
   for (int l = 0; l < d.n_layers; ++l) {
-    // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue
-    {
+    // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue (inside the
+    // previous layer's chain after layer 0 when the chain runs)
+    if (!chain || l == 0) {
       GemmMaps m = mx;
       m.a[0] = c->m_wq[l];
       m.a[1] = c->m_wk[l];
@@ -587,6 +686,10 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
     // a3: attention over the dual cache
     CK(launch_attention(c->q, c->kc_layer(l), c->vc_layer(l), c->attn_o, f.batch, f.rows_per_seq, H, f.L, ap,
                         c->st, s));
+    if (chain) {  // a4 - a5 and the next a2 in one persistent launch
+      CK(launch_chain(c, f, l, mx, mo, mact, s));
+      continue;
+    }
     // a4: O projection + residual, fused with the FFN norm
     {
       GemmMaps m = mo;
@@ -914,6 +1017,13 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
   dinfer_ctx* c = new dinfer_ctx();
   c->desc = *desc;
   c->bf16 = desc->dtype == DINFER_BF16;
+  {
+    // the per-operation kernels are the default path: the chain is measured
+    // slower on the LLaDA-8B batch-1 iteration (its row norms and the
+    // cross-CTA signals cost more than the kernel boundaries they remove)
+    const char* e = getenv("DINFER_LAYER_CHAIN");
+    c->use_chain = (e && e[0] == '1') ? 1 : 0;
+  }
   c->w.assign(weights, weights + nw);
   auto bail = [&](dinfer_status s) {
     g_create_error = c->err;
@@ -993,6 +1103,8 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
   CKC(cudaMallocHost((void**)&c->st_host, sizeof(DevState)));
   const int G = num_sms();
   AL(c->gemm_ws, gemm_ws_floats(G) * 4);
+  AL(c->chain_sync, kChainSyncWords * 4);
+  CKC(cudaMemset(c->chain_sync, 0, kChainSyncWords * 4));
   AL(c->lm_part, (size_t)G * 1024 * sizeof(SoftmaxState));
   AL(c->lm_ticket, 16);
   CKC(cudaMemset(c->lm_ticket, 0, 16));

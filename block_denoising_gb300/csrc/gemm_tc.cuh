@@ -169,6 +169,19 @@ __device__ __forceinline__ void load_stage_a(const GemmMaps& maps, const GemmArg
     tma_load_2d(sa, &maps.a[0], bar, kx, nt * 128, pol_w);
   }
 }
+// L2 prefetch of the weight tile load_stage_a would load (dense modes).
+__device__ __forceinline__ void prefetch_stage_a(const GemmMaps& maps, const GemmArgs& a, int nt, int k) {
+  const int kx = k * 64;
+  if (a.a_mode == A_PAIR) {
+    tma_prefetch_2d(&maps.a[0], kx, nt * 64);
+    tma_prefetch_2d(&maps.a[1], kx, nt * 64);
+  } else if (a.a_mode == A_THREE) {
+    const int per = a.a_rows / 128;
+    tma_prefetch_2d(&maps.a[nt / per], kx, (nt % per) * 128);
+  } else {
+    tma_prefetch_2d(&maps.a[0], kx, nt * 128);
+  }
+}
 template <int BN>
 __device__ __forceinline__ void load_stage_b(const GemmMaps& maps, uint8_t* stage, uint64_t* bar, int b_row, int k,
                                              uint64_t pol_x) {
@@ -358,6 +371,7 @@ struct Pipe {
   uint64_t* tempty;
   uint64_t* drain;
   volatile int* abort_flag;
+  int* rec;  // producer stage records [2 * kStages] (shared memory, not thread-local)
 };
 
 // TMA producer loop (one elected thread of warp 0).
@@ -372,8 +386,11 @@ __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArg
   // several token tiles the following tiles re-read them from L2
   const uint64_t pol_w = (m_tiles == 1 && !a.grouped) ? l2_policy_evict_first() : l2_policy_evict_normal();
   const uint64_t pol_x = l2_policy_evict_last();
-  // phase 1: weights of the first kStages stages (dense: before the wait)
-  int pre_b[C::kStages], pre_k[C::kStages];
+  // phase 1: weights of the first kStages stages (dense: before the wait);
+  // the stage records stay in shared memory (thread-local arrays would live
+  // in L2 on an SM whose memory is carved out as shared memory)
+  int* pre_b = p.rec;
+  int* pre_k = p.rec + C::kStages;
   int pre = 0;
   if (!a.grouped) {
     for (int j = 0; j < sl.nseg && pre < C::kStages; ++j) {
@@ -464,6 +481,7 @@ __device__ __forceinline__ Pipe setup_pipe(uint8_t* smem_raw, float*& xchg, uint
   tmem_slot = reinterpret_cast<uint32_t*>(p.drain + 1);
   misc = reinterpret_cast<volatile int*>(tmem_slot + 1);
   p.abort_flag = misc;
+  p.rec = const_cast<int*>(misc + 2);  // misc[2 .. 2 + 2 * kStages)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&p.full[s], 1);
@@ -679,6 +697,78 @@ struct ResidPlan {
   int stream_k;  // 0: the GEMM owned whole tiles, nothing left to add
 };
 
+// x = h[src, f0 .. f0+15] plus the stream-K partials of the residual GEMM
+// that cover those features (the tile's contributors, summed in CTA order so
+// the result does not depend on timing); h is written back when partials
+// were added (a tile owned whole by one CTA was already added by it).
+__device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src, int f0, int d, const ResidPlan& rp,
+                                               float (&x)[16]) {
+  float* hp = h + src * d + f0;
+  const float4* h4 = reinterpret_cast<const float4*>(hp);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 t = h4[i];
+    x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
+  }
+  const int m = (int)src;
+  const int mt = m / rp.BN, ml = m - mt * rp.BN;
+  const int nt = f0 / 128, fl = f0 - nt * 128;
+  const int t = nt * rp.m_tiles + mt;
+  Sched sc;
+  sc.G = rp.grid;
+  sc.KT = rp.k_tiles;
+  sc.U = (unsigned)(rp.m_tiles * rp.n_tiles) * rp.k_tiles;
+  const unsigned tu0 = (unsigned)t * rp.k_tiles;
+  const int c_first = rp.stream_k ? sc.owner(tu0) : 0;
+  const int c_last = rp.stream_k ? sc.owner(tu0 + rp.k_tiles - 1) : 0;
+  if (c_first == c_last) return;
+  for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+    float4 buf[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int cc = c0 + q;
+      if (cc <= c_last) {
+        const int w = ((unsigned)t == sc.start(cc) / sc.KT) ? 0 : 1;
+        const float4* sp = reinterpret_cast<const float4*>(rp.ws + ((size_t)cc * 2 + w) * (rp.BN * 128) +
+                                                           (size_t)ml * 128 + fl);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) buf[q][i] = __ldcg(sp + i);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (c0 + q <= c_last)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[4 * i] += buf[q][i].x;
+          x[4 * i + 1] += buf[q][i].y;
+          x[4 * i + 2] += buf[q][i].z;
+          x[4 * i + 3] += buf[q][i].w;
+        }
+  }
+  float4* ho = reinterpret_cast<float4*>(hp);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ho[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+}
+
+// out[16] = bf16(x * inv_rms * g[f0 .. f0+15])
+template <typename Tg>
+__device__ __forceinline__ void norm_store16(const float (&x)[16], float inv, const Tg* __restrict__ g, int f0,
+                                             __nv_bfloat16* __restrict__ out) {
+  uint4 o[2];
+  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a0 = x[2 * i] * inv * (float)g[f0 + 2 * i];
+    const float a1 = x[2 * i + 1] * inv * (float)g[f0 + 2 * i + 1];
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+    ow[i] = *reinterpret_cast<uint32_t*>(&b2);
+  }
+  uint4* op = reinterpret_cast<uint4*>(out + f0);
+  op[0] = o[0];
+  op[1] = o[1];
+}
+
 template <typename Tg>
 __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, const Tg* __restrict__ g,
                                                          __nv_bfloat16* __restrict__ out, int d, float eps,
@@ -695,59 +785,10 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
   // blockDim is a whole number of warps; threads past d / 16 hold zeros
   const bool active = threadIdx.x * 16 < d;
   const int f0 = active ? threadIdx.x * 16 : 0;
-  float* hp = h + src * d + f0;
   float x[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = 0.f;
-  if (active) {
-    const float4* h4 = reinterpret_cast<const float4*>(hp);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 t = h4[i];
-      x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
-    }
-  }
-  // partial tiles of the residual GEMM for (token src, features f0..f0+15)
-  const int m = (int)src;
-  const int mt = m / rp.BN, ml = m - mt * rp.BN;
-  const int nt = f0 / 128, fl = f0 - nt * 128;
-  const int t = nt * rp.m_tiles + mt;
-  Sched sc;
-  sc.G = rp.grid;
-  sc.KT = rp.k_tiles;
-  sc.U = (unsigned)(rp.m_tiles * rp.n_tiles) * rp.k_tiles;
-  const unsigned tu0 = (unsigned)t * rp.k_tiles;
-  const int c_first = rp.stream_k ? sc.owner(tu0) : 0;
-  const int c_last = rp.stream_k ? sc.owner(tu0 + rp.k_tiles - 1) : 0;
-  if (active && c_first != c_last) {
-    for (int c0 = c_first; c0 <= c_last; c0 += 4) {
-      float4 buf[4][4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int cc = c0 + q;
-        if (cc <= c_last) {
-          const int w = ((unsigned)t == sc.start(cc) / sc.KT) ? 0 : 1;
-          const float4* sp = reinterpret_cast<const float4*>(rp.ws + ((size_t)cc * 2 + w) * (rp.BN * 128) +
-                                                             (size_t)ml * 128 + fl);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) buf[q][i] = __ldcg(sp + i);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (c0 + q <= c_last)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            x[4 * i] += buf[q][i].x;
-            x[4 * i + 1] += buf[q][i].y;
-            x[4 * i + 2] += buf[q][i].z;
-            x[4 * i + 3] += buf[q][i].w;
-          }
-    }
-    float4* h4 = reinterpret_cast<float4*>(hp);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
-  }
+  if (active) resid_gather16(h, src, f0, d, rp, x);
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
@@ -761,20 +802,7 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
   }
   __syncthreads();
   const float inv = rsqrtf(red[0] / (float)d + eps);
-  uint4 o[2];
-  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a0 = x[2 * i] * inv * (float)g[f0 + 2 * i];
-    const float a1 = x[2 * i + 1] * inv * (float)g[f0 + 2 * i + 1];
-    __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
-    ow[i] = *reinterpret_cast<uint32_t*>(&b2);
-  }
-  if (active) {
-    uint4* op = reinterpret_cast<uint4*>(out + (size_t)r * d + f0);
-    op[0] = o[0];
-    op[1] = o[1];
-  }
+  if (active) norm_store16(x, inv, g, f0, out + (size_t)r * d);
   pdl_trigger();
 }
 
