@@ -396,6 +396,10 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
     at the launch configuration the step uses, timed with CUDA events."""
     import torch
     from block_denoising_gb300 import inputs
+    if cfg.dtype == "fp32":  # the fp32 parity model runs SIMT kernels, not the tensor-core GEMM
+        return {"bound": "alu", "kernel": "gemm_f32_kernel (fp32 parity model)", "achieved": None, "peak": None,
+                "unit": "TFLOP/s", "frac": None, "traffic": None,
+                "note": "fp32 model: a parity case, not a performance configuration"}
     M = run.batch * run.seq_len
     N, K = (2 * cfg.ffn if cfg.ffn else 3 * cfg.d_model), cfg.d_model
     X = inputs.normal_tensor(1, (M, K), 1.0, 9, device="cuda")

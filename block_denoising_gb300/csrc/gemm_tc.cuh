@@ -751,6 +751,28 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
   for (int i = 0; i < 4; ++i) ho[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
 }
 
+// gain[16] = g[f0 .. f0+15] (loaded early, off the reduction's critical path)
+template <typename Tg>
+__device__ __forceinline__ void load_gain16(const Tg* __restrict__ g, int f0, float (&gain)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) gain[i] = (float)g[f0 + i];
+}
+
+// out[16] = bf16(x * inv_rms * gain)
+__device__ __forceinline__ void norm_store16g(const float (&x)[16], float inv, const float (&gain)[16], int f0,
+                                              __nv_bfloat16* __restrict__ out) {
+  uint4 o[2];
+  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * i] * inv * gain[2 * i], x[2 * i + 1] * inv * gain[2 * i + 1]);
+    ow[i] = *reinterpret_cast<uint32_t*>(&b2);
+  }
+  uint4* op = reinterpret_cast<uint4*>(out + f0);
+  op[0] = o[0];
+  op[1] = o[1];
+}
+
 // out[16] = bf16(x * inv_rms * g[f0 .. f0+15])
 template <typename Tg>
 __device__ __forceinline__ void norm_store16(const float (&x)[16], float inv, const Tg* __restrict__ g, int f0,
@@ -785,10 +807,13 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
   // blockDim is a whole number of warps; threads past d / 16 hold zeros
   const bool active = threadIdx.x * 16 < d;
   const int f0 = active ? threadIdx.x * 16 : 0;
-  float x[16];
+  float x[16], gain[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = 0.f;
-  if (active) resid_gather16(h, src, f0, d, rp, x);
+  if (active) {
+    load_gain16(g, f0, gain);
+    resid_gather16(h, src, f0, d, rp, x);
+  }
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
@@ -802,7 +827,7 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
   }
   __syncthreads();
   const float inv = rsqrtf(red[0] / (float)d + eps);
-  if (active) norm_store16(x, inv, g, f0, out + (size_t)r * d);
+  if (active) norm_store16g(x, inv, gain, f0, out + (size_t)r * d);
   pdl_trigger();
 }
 
