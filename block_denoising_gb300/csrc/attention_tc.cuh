@@ -183,6 +183,10 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the next kernel (the O projection) may become resident on the SMs this
+  // grid leaves and request its first weight tiles; it reads this grid's
+  // output only after griddepcontrol.wait (the whole grid complete)
+  if (threadIdx.x == 0) pdl_trigger();
   // S buffer b at columns 128 b (computed, not an indexed array: local memory
   // would live in L2 on an SM whose memory is carved out as shared memory)
   const uint32_t t_o = tmem + 256;
@@ -466,7 +470,6 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
     cluster.sync();  // keep this CTA's shared memory alive until every peer has read it
   }
   __syncthreads();
-  if (threadIdx.x == 0) pdl_trigger();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kAtcTmemCols);

@@ -700,7 +700,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       CK(launch_gemm_tc(m, a, BN, s, true));
       CK(launchk(resid_norm_kernel<__nv_bfloat16>, dim3(rows), dim3(nthr), 0, s, 1, c->h,
                  (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, D, d.rms_eps, f.rows_per_seq, f.L, 0,
-                 (const DevState*)c->st, resid_plan(a, BN, c->gemm_ws)));
+                 (const DevState*)c->st, resid_plan(a, BN, c->gemm_ws), rows <= num_sms() ? 1 : 0));
     }
     const bool last = l + 1 == d.n_layers;
     const void* gn = last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0);
@@ -737,7 +737,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       CK(launch_gemm_tc(m2, b, BN, s, true));
       CK(launchk(resid_norm_kernel<__nv_bfloat16>, dim3(nrows), dim3(nthr), 0, s, 1, c->h,
                  (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps, f.B, f.L, gather,
-                 (const DevState*)c->st, resid_plan(b, BN, c->gemm_ws)));
+                 (const DevState*)c->st, resid_plan(b, BN, c->gemm_ws), nrows <= num_sms() ? 1 : 0));
     }
   }
   return DINFER_OK;

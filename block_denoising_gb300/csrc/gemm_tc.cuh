@@ -795,8 +795,12 @@ template <typename Tg>
 __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, const Tg* __restrict__ g,
                                                          __nv_bfloat16* __restrict__ out, int d, float eps,
                                                          int rows_per_seq, int L, int pos_from_state,
-                                                         const DevState* st, ResidPlan rp) {
+                                                         const DevState* st, ResidPlan rp, int trigger_early) {
   __shared__ float red[32];
+  // a grid of at most one CTA per SM lets the next GEMM become resident on
+  // the other SMs and request its first weight tiles meanwhile (with more
+  // CTAs, early dependents would take the SMs this grid still needs)
+  if (trigger_early) pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
   size_t src = r;
@@ -828,7 +832,7 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
   __syncthreads();
   const float inv = rsqrtf(red[0] / (float)d + eps);
   if (active) norm_store16g(x, inv, gain, f0, out + (size_t)r * d);
-  pdl_trigger();
+  if (!trigger_early) pdl_trigger();
 }
 
 }  // namespace dinfer

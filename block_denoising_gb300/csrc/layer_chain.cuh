@@ -271,6 +271,11 @@ __device__ __forceinline__ void chain_producer(const ChainLoad* plan, const Chai
   const uint64_t pol_x = l2_policy_evict_last();
   uint32_t it = 0;  // ring position
   bool ok = true;
+  // Everything another kernel writes -- the attention output and this
+  // grid's counters, which the previous layer's chain resets at its end --
+  // is read after the dependency wait (the kernel may start before the
+  // attention, and with it the previous chain, has completed).
+  pdl_wait();
   // bounded poll of a dependency; false when the wait gave up
   auto wait_until = [&](auto cond, uint32_t site) -> bool {
     const long long t0 = clock64();
@@ -299,7 +304,6 @@ __device__ __forceinline__ void chain_producer(const ChainLoad* plan, const Chai
       tma_load_2d(p.stages + s * C::kStage + C::kStageA, L.b, &p.full[s], k * 64, 0, pol_x);
     };
     ChainStages st(seg, begin[ph], begin[ph + 1]);
-    if (ph == CH_O) pdl_wait();  // the attention output
     bool gate = ph == CH_O || ready(st.k);
     if (!gate) {
       // the phase waits for other CTAs: its first weight tiles go into the
