@@ -419,9 +419,13 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
     dt = e0.elapsed_time(e1) / 1000.0 / n
     flops = 2.0 * M * N * K
     ach = flops / dt / 1e12
+    # DRAM bytes of one launch of this kernel at the LLaDA-8B shape, from one ncu
+    # capture (profiles/gemm_tc_kernel_llada8b_refresh_gateup.md)
+    traffic = 214110208 + 115611648 if (M, N, K) == (1536, 24576, 4096) else None
     return {"bound": "tensor", "kernel": f"gemm_tc_kernel<256> (refresh GEMM {M}x{N}x{K}, fp32 out)",
             "achieved": ach, "peak": peak_tflops, "unit": "TFLOP/s", "frac": ach / peak_tflops,
-            "traffic": None, "us_per_launch": dt * 1e6, "flops_per_launch": flops}
+            "traffic": traffic, "traffic_unit": "bytes per launch", "us_per_launch": dt * 1e6,
+            "flops_per_launch": flops}
 
 
 def run_profile(args):
@@ -433,6 +437,29 @@ def run_profile(args):
     cfg, run, _ = inputs.WORKLOADS[args.workload]
     b, P, G, B = run.batch, run.prompt_len, run.gen_length, run.block_length
     L = P + G
+    if args.profile in ("lmhead", "attention"):
+        # one kernel of the workload's cached iteration through the op API
+        ws = dinfer.OpWorkspace()
+        rows = b * B
+        if args.profile == "lmhead":
+            X = inputs.normal_tensor(5, (rows, cfg.d_model), 1.0, 3, device="cuda")
+            Wl = inputs.normal_tensor(6, (cfg.vocab, cfg.d_model), 0.02, 3, device="cuda")
+            call = lambda: dinfer.op_lmhead_bf16(X, Wl, cfg.mask_id, cfg.logit_scale, ws)
+        else:
+            d = cfg.d_model
+            q = inputs.normal_tensor(7, (rows, d), 1.0, 5, device="cuda")
+            k = inputs.normal_tensor(8, (b, L, d), 1.0, 5, device="cuda")
+            v = inputs.normal_tensor(9, (b, L, d), 1.0, 5, device="cuda")
+            call = lambda: dinfer.op_attention_bf16(q, k, v, B, ws)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        call()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        ws.check()
+        return
     if args.profile == "gemm":
         M, N, K = args.gemm
         X = inputs.normal_tensor(1, (M, K), 1.0, 9, device="cuda")
@@ -472,7 +499,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llada8b_b1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["iteration", "refresh", "gemm"], default=None)
+    ap.add_argument("--profile", choices=["iteration", "refresh", "gemm", "lmhead", "attention"], default=None)
     ap.add_argument("--gemm", type=int, nargs=3, default=[64, 24576, 4096], metavar=("M", "N", "K"))
     args = ap.parse_args()
     if args.profile:
