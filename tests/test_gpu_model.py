@@ -407,3 +407,44 @@ def test_small_moe_generate_invariants(D):
     check_generation_invariants(a.cpu().numpy(), prompt.cpu().numpy(), G, B, SMALL_MOE.mask_id, sa)
     assert torch.equal(a, b)
     dec.close()
+
+
+# ---------------------------------------------------------------------------
+# full-size models (the workloads' shapes and launch configuration): properties
+# that hold at any size -- the fp64 oracle cannot run 32 LLaDA-8B layers
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("workload,G", [("llada8b_b1", 128), ("lladamoe_b1", 128)])
+def test_full_size_generation_invariants(D, workload, G):
+    cfg, run, _ = inputs.WORKLOADS[workload]
+    P, B = run.prompt_len, run.block_length
+    W = inputs.make_weights(cfg, 0, device=dev)
+    prompt = inputs.make_prompt(cfg, 1, P, device=dev)
+    dec = D.Decoder(cfg, W, max_batch=1, max_seq=P + G)
+    a, sa = dec.generate(prompt, G, B, run.threshold)
+    b, sb = dec.generate(prompt, G, B, run.threshold)
+    out = a.cpu().numpy()
+    check_generation_invariants(out, prompt.cpu().numpy(), G, B, cfg.mask_id, sa)
+    assert ((out >= 0) & (out < cfg.vocab)).all()
+    # deterministic: the same generation twice (CTA-order split-K sums, fixed routing order)
+    assert torch.equal(a, b) and sa["iters_per_block"] == sb["iters_per_block"]
+    # every cached iteration of the block decodes finite logits with confidences in (0, 1]
+    ids = torch.full((1, P + G), cfg.mask_id, dtype=torch.int32, device=dev)
+    ids[:, :P] = prompt
+    mask = torch.zeros((1, P + G), dtype=torch.uint8, device=dev)
+    mask[:, P:] = 1
+    lg = torch.empty((B, cfg.vocab), dtype=torch.float32, device=dev)
+    tk = torch.empty(B, dtype=torch.int32, device=dev)
+    cf = torch.empty(B, dtype=torch.float32, device=dev)
+    dec.set_debug_outputs(lg, tk, cf)
+    dec.prefill_cache(ids, mask, P, B, run.threshold)
+    dec.block_step(ids, mask, run.threshold)
+    dec.sync()
+    fin = torch.isfinite(lg)
+    assert fin.sum(dim=1).eq(cfg.vocab - 1).all()      # only the mask token is excluded
+    assert not fin[:, cfg.mask_id].any()
+    assert torch.equal(tk.long(), torch.where(fin, lg, torch.full_like(lg, -float("inf"))).argmax(dim=1))
+    # confidence = 1 / sum exp(l - l_max), from the same logits
+    ref = 1.0 / torch.exp(lg[fin].view(B, -1) - lg[fin].view(B, -1).max(dim=1, keepdim=True).values).sum(dim=1)
+    assert torch.allclose(cf, ref, rtol=1e-4, atol=1e-6)
+    assert ((cf > 0) & (cf <= 1)).all()
+    dec.close()
