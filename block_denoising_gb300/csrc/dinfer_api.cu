@@ -170,7 +170,7 @@ size_t gemm_ws_floats(int grid) { return (size_t)grid * 2 * 256 * 128; }
 struct GemmSched {
   int stream_k, grid;
 };
-GemmSched gemm_schedule(int M, int n_tiles, int K, int BN) {
+GemmSched gemm_schedule(int M, int n_tiles, int K, int BN, bool whole_only = false) {
   const int m_tiles = (M + BN - 1) / BN;
   const long long tiles = (long long)m_tiles * n_tiles;
   const int k_tiles = K / 64;
@@ -180,7 +180,7 @@ GemmSched gemm_schedule(int M, int n_tiles, int K, int BN) {
   const long long wgrid = (tiles + per - 1) / per;
   // weight streaming (few token rows): ~80 busy SMs already saturate HBM;
   // tensor-bound (many rows): whole tiles only if they keep >= 90% of the SMs busy
-  const bool whole = M <= 128 ? tiles * 10 >= (long long)sms * 6 : tiles * 10 >= (long long)sms * per * 9;
+  const bool whole = whole_only || (M <= 128 ? tiles * 10 >= (long long)sms * 6 : tiles * 10 >= (long long)sms * per * 9);
   if (whole) {
     g.stream_k = 0;
     g.grid = (int)wgrid;
@@ -194,10 +194,11 @@ GemmSched gemm_schedule(int M, int n_tiles, int K, int BN) {
   return g;
 }
 
-cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s, bool defer_resid = false) {
+cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s, bool defer_resid = false,
+                           bool whole_only = false) {
   a.m_tiles = (a.M + BN - 1) / BN;
   a.k_tiles = a.K / 64;
-  const GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN);
+  const GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN, whole_only);
   a.stream_k = gs.stream_k;
   a.grid = gs.grid;
   const long long units = (long long)a.m_tiles * a.n_tiles * (a.stream_k ? a.k_tiles : 1);
@@ -311,17 +312,29 @@ cudaError_t enqueue_moe_ffn(const MoeBufs& b, const void* xn, int rows, int D, i
   return launch_gemm_grouped(md, da, bng, s);
 }
 
-ResidPlan resid_plan(const GemmArgs& a, int BN, const float* ws) {
+ResidPlan resid_plan(const GemmArgs& a, int BN, const float* ws, bool whole_only = false) {
   ResidPlan p;
   p.ws = ws;
   p.BN = BN;
   p.m_tiles = (a.M + BN - 1) / BN;
   p.n_tiles = a.n_tiles;
   p.k_tiles = a.K / 64;
-  const GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN);
+  const GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN, whole_only);
   p.stream_k = gs.stream_k;
   p.grid = gs.grid;
   return p;
+}
+
+// Residual norm over `rows` rows (one CTA each): the many-rows variant when
+// the grid is larger than one CTA per SM.
+cudaError_t launch_resid_norm(int rows, int nthr, cudaStream_t s, float* h, const __nv_bfloat16* g,
+                              __nv_bfloat16* out, int d, float eps, int rows_per_seq, int L, int gather,
+                              const DevState* st, const ResidPlan& rp) {
+  if (rows > num_sms())
+    return launchk(resid_norm_kernel<__nv_bfloat16, true>, dim3(rows), dim3(nthr), 0, s, 1, h, g, out, d, eps,
+                   rows_per_seq, L, gather, st, rp, 1);
+  return launchk(resid_norm_kernel<__nv_bfloat16, false>, dim3(rows), dim3(nthr), 0, s, 1, h, g, out, d, eps,
+                 rows_per_seq, L, gather, st, rp, 1);
 }
 
 int lmhead_grid(int M, int V) {
@@ -654,8 +667,15 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
              (const float*)c->h, (const __nv_bfloat16*)c->LW(0, 0), (__nv_bfloat16*)c->xn, rows, D, d.rms_eps, 0,
              rm, (const DevState*)c->st));
   const int BN = bn_for_rows(rows);
+  // O projection of many rows: 128-token tiles dealt whole (three per CTA on
+  // 128 SMs at 1536 x 4096) add to h in the GEMM, so the FFN norm gathers no
+  // stream-K partials -- when they keep at least 80% of the SMs busy
+  const long long o_tiles = (long long)((rows + 127) / 128) * (D / 128);
+  const long long o_per = (o_tiles + num_sms() - 1) / num_sms();
+  const bool o_whole = rows > 128 && o_tiles * 10 >= o_per * num_sms() * 8;
+  const int BNo = o_whole ? 128 : BN;
   GemmMaps mx{}, mo{}, mact{};
-  if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BN) ||
+  if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BNo) ||
       (!d.n_experts && !make_map(&mact.b, c->act, rows, F, BN)))
     return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
@@ -697,10 +717,10 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       GemmArgs a{};
       a.M = rows; a.N = D; a.K = D; a.n_tiles = D / 128; a.a_mode = A_SINGLE;
       a.resid = c->h; a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
-      CK(launch_gemm_tc(m, a, BN, s, true));
-      CK(launchk(resid_norm_kernel<__nv_bfloat16>, dim3(rows), dim3(nthr), 0, s, 1, c->h,
-                 (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, D, d.rms_eps, f.rows_per_seq, f.L, 0,
-                 (const DevState*)c->st, resid_plan(a, BN, c->gemm_ws), rows <= num_sms() ? 1 : 0));
+      CK(launch_gemm_tc(m, a, BNo, s, true, o_whole));
+      CK(launch_resid_norm(rows, nthr, s, c->h, (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, D,
+                           d.rms_eps, f.rows_per_seq, f.L, 0, (const DevState*)c->st,
+                           resid_plan(a, BNo, c->gemm_ws, o_whole)));
     }
     const bool last = l + 1 == d.n_layers;
     const void* gn = last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0);
@@ -735,9 +755,8 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       b.M = rows; b.N = D; b.K = F; b.n_tiles = D / 128; b.a_mode = A_SINGLE;
       b.resid = c->h; b.ws = c->gemm_ws; b.status = c->st; b.state = c->st;
       CK(launch_gemm_tc(m2, b, BN, s, true));
-      CK(launchk(resid_norm_kernel<__nv_bfloat16>, dim3(nrows), dim3(nthr), 0, s, 1, c->h,
-                 (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps, f.B, f.L, gather,
-                 (const DevState*)c->st, resid_plan(b, BN, c->gemm_ws), nrows <= num_sms() ? 1 : 0));
+      CK(launch_resid_norm(nrows, nthr, s, c->h, (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps,
+                           f.B, f.L, gather, (const DevState*)c->st, resid_plan(b, BN, c->gemm_ws)));
     }
   }
   return DINFER_OK;

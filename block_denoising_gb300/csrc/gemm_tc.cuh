@@ -303,6 +303,12 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
   }
 }
 
+// h[m0 .. m0+15, n] of a residual GEMM (zeros past M), all 16 loads in flight.
+__device__ __forceinline__ void resid_load16(const GemmArgs& a, int n, int m0, float (&hv)[16]) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) hv[c] = (m0 + c < a.M) ? a.resid[(size_t)(m0 + c) * a.N + n] : 0.f;
+}
+
 // The segments (tile t, k-steps [kb, ke)) of one CTA's unit range.  In
 // stream-K mode the range [u0, u1) covers the tail of tile tf, whole tiles,
 // and the head of tile tl; the partial segments are processed FIRST so that
@@ -556,8 +562,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int acc = j & 1;
       const uint32_t use = j >> 1;
       const bool whole = (kb == 0 && ke == a.k_tiles);
-      // loads of the tile's first RoPE factors overlap its main loop
+      const int n = tr.nt * 128 + row;
+      float hcur[16];  // residual: h of the chunk being finished
+      // loads of the tile's first RoPE factors or residual values overlap its
+      // main loop (a whole tile's h is written by this thread only)
       if (a.q_out != nullptr && whole) qkv_rope_fetch(a, base_pos, row, tr.nt, tr.mt * BN, rope[0], rope[1]);
+      if (a.resid != nullptr && whole) resid_load16(a, n, tr.mt * BN, hcur);
       if (!mbar_wait(&p.tfull[acc], use & 1, p.abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
@@ -603,6 +613,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             rope[0][i] = next[0][i];
             rope[1][i] = next[1][i];
           }
+        }
+      } else if (a.resid != nullptr) {
+        // residual: h of chunk c + 1 loads while chunk c is finished
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          const int m0 = tr.mt * BN + c * 16;
+          float v[16], hnext[16];
+          tmem_ld16(tbase + c * 16, v);
+          if (c + 1 < BN / 16) resid_load16(a, n, m0 + 16, hnext);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (m0 + i < a.M) a.resid[(size_t)(m0 + i) * a.N + n] = hcur[i] + v[i];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hcur[i] = hnext[i];
         }
       } else {
 #pragma unroll 1
@@ -701,6 +725,8 @@ struct ResidPlan {
 // that cover those features (the tile's contributors, summed in CTA order so
 // the result does not depend on timing); h is written back when partials
 // were added (a tile owned whole by one CTA was already added by it).
+// kBatch contributors' loads in flight at a time.
+template <int kBatch>
 __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src, int f0, int d, const ResidPlan& rp,
                                                float (&x)[16]) {
   float* hp = h + src * d + f0;
@@ -722,10 +748,10 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
   const int c_first = rp.stream_k ? sc.owner(tu0) : 0;
   const int c_last = rp.stream_k ? sc.owner(tu0 + rp.k_tiles - 1) : 0;
   if (c_first == c_last) return;
-  for (int c0 = c_first; c0 <= c_last; c0 += 4) {
-    float4 buf[4][4];
+  for (int c0 = c_first; c0 <= c_last; c0 += kBatch) {
+    float4 buf[kBatch][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kBatch; ++q) {
       const int cc = c0 + q;
       if (cc <= c_last) {
         const int w = ((unsigned)t == sc.start(cc) / sc.KT) ? 0 : 1;
@@ -736,7 +762,7 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < kBatch; ++q)
       if (c0 + q <= c_last)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -751,21 +777,23 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
   for (int i = 0; i < 4; ++i) ho[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
 }
 
-// gain[16] = g[f0 .. f0+15] (loaded early, off the reduction's critical path)
-template <typename Tg>
-__device__ __forceinline__ void load_gain16(const Tg* __restrict__ g, int f0, float (&gain)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) gain[i] = (float)g[f0 + i];
+// the bf16 gains g[f0 .. f0+15], packed in 8 registers
+__device__ __forceinline__ void load_gain16(const __nv_bfloat16* __restrict__ g, int f0, uint4 (&gain)[2]) {
+  const uint4* gp = reinterpret_cast<const uint4*>(g + f0);
+  gain[0] = __ldg(gp);
+  gain[1] = __ldg(gp + 1);
 }
 
 // out[16] = bf16(x * inv_rms * gain)
-__device__ __forceinline__ void norm_store16g(const float (&x)[16], float inv, const float (&gain)[16], int f0,
+__device__ __forceinline__ void norm_store16g(const float (&x)[16], float inv, const uint4 (&gain)[2], int f0,
                                               __nv_bfloat16* __restrict__ out) {
   uint4 o[2];
   uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+  const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(gain);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * i] * inv * gain[2 * i], x[2 * i + 1] * inv * gain[2 * i + 1]);
+    const float2 gf = __bfloat1622float2(gb[i]);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * i] * inv * gf.x, x[2 * i + 1] * inv * gf.y);
     ow[i] = *reinterpret_cast<uint32_t*>(&b2);
   }
   uint4* op = reinterpret_cast<uint4*>(out + f0);
@@ -791,15 +819,18 @@ __device__ __forceinline__ void norm_store16(const float (&x)[16], float inv, co
   op[1] = o[1];
 }
 
-template <typename Tg>
-__global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, const Tg* __restrict__ g,
+// kMany: a grid of many rows (a refresh), held to 64 registers a thread so
+// that four 256-thread CTAs share an SM; otherwise (a block's rows, one CTA
+// per SM) four contributors' partials and the gains are in flight together.
+template <typename Tg, bool kMany>
+__global__ void __launch_bounds__(512, kMany ? 2 : 1) resid_norm_kernel(float* __restrict__ h, const Tg* __restrict__ g,
                                                          __nv_bfloat16* __restrict__ out, int d, float eps,
                                                          int rows_per_seq, int L, int pos_from_state,
                                                          const DevState* st, ResidPlan rp, int trigger_early) {
   __shared__ float red[32];
-  // a grid of at most one CTA per SM lets the next GEMM become resident on
-  // the other SMs and request its first weight tiles meanwhile (with more
-  // CTAs, early dependents would take the SMs this grid still needs)
+  // the next GEMM may launch once every CTA of this grid has started (they
+  // are all resident by then): it becomes resident beside the last ones and
+  // requests its first weight tiles meanwhile
   if (trigger_early) pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
@@ -811,12 +842,14 @@ __global__ void __launch_bounds__(512) resid_norm_kernel(float* __restrict__ h, 
   // blockDim is a whole number of warps; threads past d / 16 hold zeros
   const bool active = threadIdx.x * 16 < d;
   const int f0 = active ? threadIdx.x * 16 : 0;
-  float x[16], gain[16];
+  float x[16];
+  uint4 gain[2] = {};
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = 0.f;
   if (active) {
-    load_gain16(g, f0, gain);
-    resid_gather16(h, src, f0, d, rp, x);
+    if (!kMany) load_gain16(g, f0, gain);
+    resid_gather16<kMany ? 2 : 4>(h, src, f0, d, rp, x);
+    if (kMany) load_gain16(g, f0, gain);  // in flight during the block reduction
   }
   float ss = 0.f;
 #pragma unroll
