@@ -421,7 +421,7 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
     ach = flops / dt / 1e12
     # DRAM bytes of one launch of this kernel at the LLaDA-8B shape, from one ncu
     # capture (profiles/gemm_tc_kernel_llada8b_refresh_gateup.md)
-    traffic = 214110208 + 115611648 if (M, N, K) == (1536, 24576, 4096) else None
+    traffic = 213997824 + 115565568 if (M, N, K) == (1536, 24576, 4096) else None
     return {"bound": "tensor", "kernel": f"gemm_tc_kernel<256> (refresh GEMM {M}x{N}x{K}, fp32 out)",
             "achieved": ach, "peak": peak_tflops, "unit": "TFLOP/s", "frac": ach / peak_tflops,
             "traffic": traffic, "traffic_unit": "bytes per launch", "us_per_launch": dt * 1e6,

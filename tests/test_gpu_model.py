@@ -30,6 +30,7 @@ dev = torch.device("cuda:0")
 # about twice it.  Flags then follow from delta exactly (see flags_for).
 FP32 = dict(delta=1e-4, logit_mean=1e-5)
 BF16_SMALL = dict(delta=0.6, logit_mean=0.08)
+BF16_LONG = dict(delta=0.8, logit_mean=0.14)  # d_model 1024, refresh of 2048 rows
 NS_GAP, NS_CONF = 1e-2, 1e-2  # flag widths stated for the method's parity check
 
 
@@ -255,6 +256,26 @@ def test_small_bf16_teacher_forced(D, batch, P, G, B, tau):
     print(st)
     assert st["max_err"] < BF16_SMALL["delta"]
     assert st["mean_err"] < BF16_SMALL["logit_mean"]
+    assert st["conf_outside"] == 0
+    assert st["unflagged_mismatch"] == 0
+
+
+# A refresh of 2048 rows at d_model 1024: the O projection runs as whole
+# 128-token tiles (128 CTAs, residual added in the GEMM's epilogue), the other
+# GEMMs stream-K, and both residual norms take the many-rows variant (the FFN
+# norm a plain row norm, the next-layer norm with the down projection's
+# partials).  First block only: its refresh and cached iterations.
+LONG_BF16 = inputs.shrink(inputs.LLADA_8B, n_layers=2, d_model=1024, n_heads=8, ffn=2048, vocab=2048,
+                          mask_id=2047)
+
+
+def test_long_refresh_bf16_teacher_forced(D):
+    W = inputs.make_weights(LONG_BF16, 0)
+    prompt = inputs.make_prompt(LONG_BF16, 1, 1984).numpy()
+    st, _, _ = teacher_forced(D, LONG_BF16, W, prompt, 64, 32, 0.9, BF16_LONG, max_blocks=1)
+    print(st)
+    assert st["max_err"] < BF16_LONG["delta"]
+    assert st["mean_err"] < BF16_LONG["logit_mean"]
     assert st["conf_outside"] == 0
     assert st["unflagged_mismatch"] == 0
 
