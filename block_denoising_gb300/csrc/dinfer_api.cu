@@ -276,17 +276,23 @@ cudaError_t enqueue_moe_ffn(const MoeBufs& b, const void* xn, int rows, int D, i
               b.topk_id, b.topk_w);
   if (e != cudaSuccess) return e;
   const int chunks = (rows + kMoeChunk - 1) / kMoeChunk;
-  e = launchk(moe_count_kernel, dim3(chunks), dim3(kMoeChunk), 0, s, 1, (const int*)b.topk_id, rows, E, K, b.rank,
-              b.chunk_cnt);
-  if (e != cudaSuccess) return e;
   const int pairs = rows * K;
   const int bng = bn_for_rows(std::max(1, (pairs + E - 1) / E));  // token tile of the expert GEMMs
   int* row_off = b.tables;
   int* cum_gu = b.tables + (E + 1);
   int* cum_dn = b.tables + 2 * (E + 1);
-  e = launchk(moe_scan_kernel, dim3(1), dim3(64), 0, s, 1, (const int*)b.chunk_cnt, chunks, E, b.chunk_base, row_off,
-              cum_gu, cum_dn, bng, FE / 64, bng, D / 128);
-  if (e != cudaSuccess) return e;
+  if (chunks == 1 && E <= 64) {
+    e = launchk(moe_route_tables_kernel, dim3(1), dim3(kMoeChunk), 0, s, 1, (const int*)b.topk_id, rows, E, K, b.rank,
+                b.chunk_base, row_off, cum_gu, cum_dn, bng, FE / 64, bng, D / 128);
+    if (e != cudaSuccess) return e;
+  } else {
+    e = launchk(moe_count_kernel, dim3(chunks), dim3(kMoeChunk), 0, s, 1, (const int*)b.topk_id, rows, E, K, b.rank,
+                b.chunk_cnt);
+    if (e != cudaSuccess) return e;
+    e = launchk(moe_scan_kernel, dim3(1), dim3(64), 0, s, 1, (const int*)b.chunk_cnt, chunks, E, b.chunk_base,
+                row_off, cum_gu, cum_dn, bng, FE / 64, bng, D / 128);
+    if (e != cudaSuccess) return e;
+  }
   e = launchk(moe_scatter_kernel, dim3(pairs), dim3(256), 0, s, 1, (const __nv_bfloat16*)xn, D, rows, E, K,
               (const int*)b.topk_id, (const int*)b.rank, (const int*)b.chunk_base, (const int*)row_off, b.inv,
               (__nv_bfloat16*)b.x);

@@ -5,8 +5,9 @@
 //   h += sum over the row's experts of p_e * (silu(x_hat W_g,e^T) * x_hat W_u,e^T) W_d,e^T
 //
 // Device pipeline: router logits (tcgen05 GEMM, fp32 out) -> moe_topk_kernel
-// (one warp per row) -> moe_count_kernel + moe_scan_kernel + moe_scatter_kernel
-// (a counting sort of the (row, expert) pairs by expert, rows in ascending
+// (one warp per row) -> moe_count_kernel + moe_scan_kernel (or, for at most
+// 256 rows and 64 experts, moe_route_tables_kernel) + moe_scatter_kernel (a
+// counting sort of the (row, expert) pairs by expert, rows in ascending
 // order inside an expert, so the permutation does not depend on timing) ->
 // grouped gate/up and down GEMMs over the permuted rows (gemm_tc_kernel in
 // grouped mode, tile tables written here) -> moe_combine_norm_kernel
@@ -118,6 +119,82 @@ __global__ void moe_scan_kernel(const int* __restrict__ chunk_cnt, int n_chunks,
     row_off[E] = ro;
     tile_cum_gu[E] = tg;
     tile_cum_dn[E] = td;
+  }
+  pdl_trigger();
+}
+
+// The counting sort of a block's rows (M <= kMoeChunk, E <= 64) in one CTA,
+// with the results of moe_count_kernel + moe_scan_kernel for a single chunk:
+// per expert a bitmask of the rows that select it (set with atomicOr, whose
+// result does not depend on the order), a row's rank among the expert's rows
+// = the population count of the mask below the row (ascending row order),
+// then exclusive scans of the counts and tile counts over the experts (one
+// warp, two experts a lane).
+__global__ void __launch_bounds__(kMoeChunk) moe_route_tables_kernel(
+    const int* __restrict__ topk_id, int M, int E, int K, int* __restrict__ local_rank, int* __restrict__ chunk_base,
+    int* __restrict__ row_off, int* __restrict__ tile_cum_gu, int* __restrict__ tile_cum_dn, int bn_gu, int nt_gu,
+    int bn_dn, int nt_dn) {
+  constexpr int W = kMoeChunk / 32;  // mask words per expert
+  __shared__ uint32_t bits[64 * W];
+  __shared__ int cnt[64];
+  pdl_wait();
+  const int r = threadIdx.x;
+  for (int i = r; i < E * W; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  int ids[kMoeMaxK];
+#pragma unroll
+  for (int k = 0; k < kMoeMaxK; ++k) ids[k] = (r < M && k < K) ? topk_id[(size_t)r * K + k] : -1;
+#pragma unroll
+  for (int k = 0; k < kMoeMaxK; ++k)
+    if (ids[k] >= 0) atomicOr(&bits[ids[k] * W + (r >> 5)], 1u << (r & 31));
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kMoeMaxK; ++k) {
+    if (ids[k] < 0) continue;
+    const uint32_t* b = bits + ids[k] * W;
+    int rank = __popc(b[r >> 5] & ((1u << (r & 31)) - 1u));
+    for (int w = 0; w < (r >> 5); ++w) rank += __popc(b[w]);
+    local_rank[(size_t)r * K + k] = rank;
+  }
+  if (r < E) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) c += __popc(bits[r * W + w]);
+    cnt[r] = c;
+    chunk_base[r] = 0;
+  }
+  __syncthreads();
+  if (r < 32) {
+    const int e0 = 2 * r, e1 = 2 * r + 1;
+    const int c0 = e0 < E ? cnt[e0] : 0, c1 = e1 < E ? cnt[e1] : 0;
+    const int g0 = ((c0 + bn_gu - 1) / bn_gu) * nt_gu, g1 = ((c1 + bn_gu - 1) / bn_gu) * nt_gu;
+    const int d0 = ((c0 + bn_dn - 1) / bn_dn) * nt_dn, d1 = ((c1 + bn_dn - 1) / bn_dn) * nt_dn;
+    int sc = c0 + c1, sg = g0 + g1, sd = d0 + d1;  // inclusive scans over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int tc = __shfl_up_sync(0xffffffffu, sc, o), tg = __shfl_up_sync(0xffffffffu, sg, o);
+      const int td = __shfl_up_sync(0xffffffffu, sd, o);
+      if (r >= o) {
+        sc += tc;
+        sg += tg;
+        sd += td;
+      }
+    }
+    if (e0 < E) {
+      row_off[e0] = sc - c0 - c1;
+      tile_cum_gu[e0] = sg - g0 - g1;
+      tile_cum_dn[e0] = sd - d0 - d1;
+    }
+    if (e1 < E) {
+      row_off[e1] = sc - c1;
+      tile_cum_gu[e1] = sg - g1;
+      tile_cum_dn[e1] = sd - d1;
+    }
+    if (r == 31) {
+      row_off[E] = sc;
+      tile_cum_gu[E] = sg;
+      tile_cum_dn[E] = sd;
+    }
   }
   pdl_trigger();
 }
