@@ -198,7 +198,19 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
                            bool whole_only = false) {
   a.m_tiles = (a.M + BN - 1) / BN;
   a.k_tiles = a.K / 64;
-  const GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN, whole_only);
+  GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN, whole_only);
+  if (gs.stream_k && !defer_resid && a.M <= 128) {
+    // a split tile here costs a fixup launch (~5 us); whole tiles are better
+    // when one SM streaming its weight tiles (~85 GB/s) is not slower than
+    // all SMs streaming the whole matrix (~6.8 TB/s) plus that launch
+    const long long tiles = (long long)a.m_tiles * a.n_tiles;
+    const long long per = (tiles + num_sms() - 1) / num_sms();
+    const long long tile_bytes = (long long)std::min(a.N, 128) * a.K * 2;
+    if (per * tile_bytes / 85 <= tiles * tile_bytes / 6800 + 5000) {
+      gs.stream_k = 0;
+      gs.grid = (int)((tiles + per - 1) / per);
+    }
+  }
   a.stream_k = gs.stream_k;
   a.grid = gs.grid;
   const long long units = (long long)a.m_tiles * a.n_tiles * (a.stream_k ? a.k_tiles : 1);
