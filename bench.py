@@ -49,12 +49,14 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # algorithmic work (per unit) of the hot path
 # ---------------------------------------------------------------------------
-def _ffn_params(cfg, touched=True):
-    """FFN weights per layer: dense SwiGLU, or router + experts (all experts: a
-    block of 64 rows touches every one of 64 experts with probability ~1)."""
+def _ffn_params(cfg, experts=None):
+    """FFN weights per layer: dense SwiGLU, or router + the experts the rows
+    select (`experts` per layer on average, as counted on the device; all of
+    them when not given)."""
     d = cfg.d_model
     if cfg.n_experts:
-        return cfg.n_experts * d + cfg.n_experts * 3 * cfg.expert_ffn * d
+        e = cfg.n_experts if experts is None else experts
+        return cfg.n_experts * d + e * 3 * cfg.expert_ffn * d
     return 3 * d * cfg.ffn
 
 
@@ -65,11 +67,12 @@ def _ffn_flops_per_row(cfg):
     return 2 * 3 * d * cfg.ffn
 
 
-def iteration_bytes(cfg, b, L, B):
+def iteration_bytes(cfg, b, L, B, experts=None):
     """Bytes one cached denoising iteration must move: every weight read once
-    (embedding rows aside) plus the cached K/V of the L - B non-block positions."""
+    (embedding rows aside; of the experts, those the block's rows select) plus
+    the cached K/V of the L - B non-block positions."""
     d, nl, V = cfg.d_model, cfg.n_layers, cfg.vocab
-    w = nl * (4 * d * d + _ffn_params(cfg)) + V * d
+    w = nl * (4 * d * d + _ffn_params(cfg, experts)) + V * d
     kv = b * (L - B) * 2 * d * nl
     return 2 * (w + kv)
 
@@ -313,12 +316,15 @@ def run_ours(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ids2, mask2 = ids.clone(), mask.clone()
         dec.block_step(ids2, mask2, 2.0)  # threshold above 1: one commit per step, block never empties
+        dec.moe_experts_touched()  # restart the device's count of selected experts
         e0.record(stream)
         for _ in range(n_it):
             dec.block_step(ids2, mask2, 2.0)
         e1.record(stream)
         stream.synchronize()
         us_iter = 1000.0 * e0.elapsed_time(e1) / n_it
+        # experts per MoE layer that the block's rows selected, on average
+        experts = dec.moe_experts_touched() / (n_it * cfg.n_layers) if cfg.n_experts else None
         e0.record(stream)
         for _ in range(3):
             dec.prefill_cache(ids, mask, P, B, run.threshold, commit=False)
@@ -342,7 +348,7 @@ def run_ours(args):
     e2e = tokens / t_e2e
     if rank == 0:
         ipb = iters[-1]
-        bytes_it = iteration_bytes(cfg, b, L, B)
+        bytes_it = iteration_bytes(cfg, b, L, B, experts)
         ach_gbs = bytes_it / (us_iter * 1e-6) / 1e9
         it_roof_us = max(bytes_it / (hbm * 1e9), iteration_flops(cfg, b, L, B) / (tf_burst * 1e12)) * 1e6
         it_roof_us_8t = max(bytes_it / 8e12, iteration_flops(cfg, b, L, B) / (tf_burst * 1e12)) * 1e6
@@ -364,6 +370,7 @@ def run_ours(args):
             "us_per_iteration": us_iter,
             "us_per_refresh": us_refresh,
             "iteration_roofline": {"bound": "hbm", "bytes": bytes_it, "achieved_gbs": ach_gbs,
+                                   "experts_per_layer": experts,
                                    "roofline_us_measured_peak": it_roof_us, "roofline_us_8tbs": it_roof_us_8t,
                                    "frac_of_measured": it_roof_us / us_iter, "frac_of_8tbs": it_roof_us_8t / us_iter,
                                    "peak_source": peak_src},

@@ -295,14 +295,14 @@ cudaError_t enqueue_moe_ffn(const MoeBufs& b, const void* xn, int rows, int D, i
   int* cum_dn = b.tables + 2 * (E + 1);
   if (chunks == 1 && E <= 64) {
     e = launchk(moe_route_tables_kernel, dim3(1), dim3(kMoeChunk), 0, s, 1, (const int*)b.topk_id, rows, E, K, b.rank,
-                b.chunk_base, row_off, cum_gu, cum_dn, bng, FE / 64, bng, D / 128);
+                b.chunk_base, row_off, cum_gu, cum_dn, bng, FE / 64, bng, D / 128, b.st);
     if (e != cudaSuccess) return e;
   } else {
     e = launchk(moe_count_kernel, dim3(chunks), dim3(kMoeChunk), 0, s, 1, (const int*)b.topk_id, rows, E, K, b.rank,
                 b.chunk_cnt);
     if (e != cudaSuccess) return e;
     e = launchk(moe_scan_kernel, dim3(1), dim3(64), 0, s, 1, (const int*)b.chunk_cnt, chunks, E, b.chunk_base,
-                row_off, cum_gu, cum_dn, bng, FE / 64, bng, D / 128);
+                row_off, cum_gu, cum_dn, bng, FE / 64, bng, D / 128, b.st);
     if (e != cudaSuccess) return e;
   }
   e = launchk(moe_scatter_kernel, dim3(pairs), dim3(256), 0, s, 1, (const __nv_bfloat16*)xn, D, rows, E, K,
@@ -1192,6 +1192,17 @@ dinfer_status dinfer_set_debug_outputs(dinfer_ctx* c, float* logits, int32_t* to
 dinfer_status dinfer_sync(dinfer_ctx* c) {
   if (!c) return DINFER_EINVAL;
   return read_status(c);
+}
+
+dinfer_status dinfer_moe_experts_touched(dinfer_ctx* c, int64_t* touched) {
+  if (!c || !touched) return fail(c, DINFER_EINVAL, "NULL argument");
+  uint32_t v = 0;
+  uint32_t* dev = &c->st->moe_touched;
+  CK(cudaStreamSynchronize(c->stream));
+  CK(cudaMemcpy(&v, dev, sizeof(v), cudaMemcpyDeviceToHost));
+  CK(cudaMemset(dev, 0, sizeof(v)));
+  *touched = v;
+  return DINFER_OK;
 }
 
 dinfer_status dinfer_prefill_cache(dinfer_ctx* c, int32_t* ids, uint8_t* mask, int32_t batch, int32_t seq_len,

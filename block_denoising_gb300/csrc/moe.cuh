@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kMoeChunk) moe_count_kernel(const int* __restr
 // the two grouped GEMMs (n-tiles per expert x token tiles of that expert).
 __global__ void moe_scan_kernel(const int* __restrict__ chunk_cnt, int n_chunks, int E, int* __restrict__ chunk_base,
                                 int* __restrict__ row_off, int* __restrict__ tile_cum_gu, int* __restrict__ tile_cum_dn,
-                                int bn_gu, int nt_gu, int bn_dn, int nt_dn) {
+                                int bn_gu, int nt_gu, int bn_dn, int nt_dn, DevState* st) {
   __shared__ int tot[kMoeMaxE];
   pdl_wait();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -107,8 +107,9 @@ __global__ void moe_scan_kernel(const int* __restrict__ chunk_cnt, int n_chunks,
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int ro = 0, tg = 0, td = 0;
+    int ro = 0, tg = 0, td = 0, touched = 0;
     for (int e = 0; e < E; ++e) {
+      touched += tot[e] > 0;
       row_off[e] = ro;
       tile_cum_gu[e] = tg;
       tile_cum_dn[e] = td;
@@ -119,6 +120,7 @@ __global__ void moe_scan_kernel(const int* __restrict__ chunk_cnt, int n_chunks,
     row_off[E] = ro;
     tile_cum_gu[E] = tg;
     tile_cum_dn[E] = td;
+    atomicAdd(&st->moe_touched, (uint32_t)touched);
   }
   pdl_trigger();
 }
@@ -133,7 +135,7 @@ __global__ void moe_scan_kernel(const int* __restrict__ chunk_cnt, int n_chunks,
 __global__ void __launch_bounds__(kMoeChunk) moe_route_tables_kernel(
     const int* __restrict__ topk_id, int M, int E, int K, int* __restrict__ local_rank, int* __restrict__ chunk_base,
     int* __restrict__ row_off, int* __restrict__ tile_cum_gu, int* __restrict__ tile_cum_dn, int bn_gu, int nt_gu,
-    int bn_dn, int nt_dn) {
+    int bn_dn, int nt_dn, DevState* st) {
   constexpr int W = kMoeChunk / 32;  // mask words per expert
   __shared__ uint32_t bits[64 * W];
   __shared__ int cnt[64];
@@ -195,6 +197,9 @@ __global__ void __launch_bounds__(kMoeChunk) moe_route_tables_kernel(
       tile_cum_gu[E] = sg;
       tile_cum_dn[E] = sd;
     }
+    // experts that received rows, for the measured byte count
+    const int touched = __popc(__ballot_sync(0xffffffffu, c0 > 0)) + __popc(__ballot_sync(0xffffffffu, c1 > 0));
+    if (r == 0) atomicAdd(&st->moe_touched, (uint32_t)touched);
   }
   pdl_trigger();
 }

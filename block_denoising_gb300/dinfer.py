@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
     L.dinfer_set_debug_outputs.restype = i32
     L.dinfer_sync.argtypes = [vp]
     L.dinfer_sync.restype = i32
+    L.dinfer_moe_experts_touched.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
+    L.dinfer_moe_experts_touched.restype = i32
     L.dinfer_op_workspace_bytes.argtypes = []
     L.dinfer_op_workspace_bytes.restype = sz
     L.dinfer_op_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, vp, sz, vp]
@@ -160,6 +162,13 @@ class Decoder:
 
     def sync(self):
         _check(lib().dinfer_sync(self.h), self.h)
+
+    def moe_experts_touched(self):
+        """(MoE layer forward, expert) pairs that received rows since the
+        previous call (the count restarts); 0 for dense models."""
+        n = ctypes.c_int64(0)
+        _check(lib().dinfer_moe_experts_touched(self.h, ctypes.byref(n)), self.h)
+        return int(n.value)
 
 
 # ---------------------------------------------------------------------------

@@ -139,6 +139,14 @@ dinfer_status dinfer_set_debug_outputs(dinfer_ctx* ctx, float* logits, int32_t* 
 /* Wait for the context's stream and report the device status word. */
 dinfer_status dinfer_sync(dinfer_ctx* ctx);
 
+/* Measurement hook for the byte count of a mixture-of-experts iteration (the
+ * weights of the experts its rows select): *touched receives the number of
+ * (MoE layer forward, expert) pairs that received at least one row since the
+ * context was created or since the previous call, and the count restarts at
+ * zero.  Waits for the context's stream.  Always 0 for dense models.
+ * Errors: DINFER_EINVAL for NULL arguments, DINFER_ECUDA if the copy fails. */
+dinfer_status dinfer_moe_experts_touched(dinfer_ctx* ctx, int64_t* touched);
+
 #ifdef __cplusplus
 }
 #endif

@@ -430,6 +430,64 @@ def test_small_moe_generate_invariants(D):
     dec.close()
 
 
+# 64 experts, top-2: a block's rows leave some experts unselected, so the
+# count the bench turns into weight bytes is not simply layers x experts.
+MANY_EXPERTS = inputs.shrink(inputs.LLADA_MOE, n_layers=2, d_model=256, n_heads=2, vocab=2048, mask_id=2047,
+                             n_experts=64, top_k=2, expert_ffn=128)
+
+
+def test_moe_experts_touched_matches_oracle_routing(D):
+    """The device's count of (layer forward, expert) pairs with rows, against
+    the oracle's routing of the same refresh; a row whose 2nd and 3rd router
+    logits are within 0.02 may route differently under bf16 rounding, so each
+    such row may move the count by one."""
+    cfg = MANY_EXPERTS
+    W = inputs.make_weights(cfg, 0)
+    P, G, B = 64, 32, 32
+    prompt = inputs.make_prompt(cfg, 1, P).numpy()
+    x = np.full((1, P + G), cfg.mask_id)
+    x[0, :P] = prompt
+    mask = np.zeros((1, P + G), bool)
+    mask[0, P:] = True
+    m = O.Model(O.Desc.from_config(cfg), [w.float().numpy() for w in W])
+    chosen, near = [], 0
+    orig = O.route
+
+    def recording(a, router, top_k):
+        nonlocal near
+        p, idx = orig(a, router, top_k)
+        lg = np.sort(O.linear(a, router), axis=-1)[:, ::-1]
+        near += int(((lg[:, top_k - 1] - lg[:, top_k]) < 0.02).sum())
+        chosen.append(np.unique(idx).size)
+        return p, idx
+
+    O.route = recording
+    try:
+        O.refresh_step(m, x.copy(), mask.copy(), P, B, 0.9, O.Cache(m.desc, 1, P + G), commit=False)
+    finally:
+        O.route = orig
+    expected = sum(chosen)
+    assert len(chosen) == cfg.n_layers and expected < cfg.n_layers * cfg.n_experts
+    dec = D.Decoder(cfg, [w.to(dev) for w in W], max_batch=1, max_seq=P + G)
+    ids = torch.tensor(x, dtype=torch.int32, device=dev)
+    mk = torch.tensor(mask.astype(np.uint8), device=dev)
+    dec.moe_experts_touched()
+    dec.prefill_cache(ids, mk, P, B, 0.9, commit=False)
+    got = dec.moe_experts_touched()
+    print("experts touched: gpu", got, "oracle", expected, "near-tie rows", near)
+    assert abs(got - expected) <= near
+    # cached iterations: between one and min(E, B * top_k) experts per layer
+    for _ in range(3):
+        dec.block_step(ids, mk, 2.0)
+    it = dec.moe_experts_touched()
+    assert 3 * cfg.n_layers <= it <= 3 * cfg.n_layers * min(cfg.n_experts, B * cfg.top_k)
+    assert dec.moe_experts_touched() == 0  # the count restarted
+    dec.close()
+    dense = D.Decoder(SMALL_BF16, [w.to(dev) for w in inputs.make_weights(SMALL_BF16, 0)], max_batch=1, max_seq=96)
+    assert dense.moe_experts_touched() == 0
+    dense.close()
+
+
 # ---------------------------------------------------------------------------
 # full-size models (the workloads' shapes and launch configuration): properties
 # that hold at any size -- the fp64 oracle cannot run 32 LLaDA-8B layers
