@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -280,8 +281,8 @@ def run_ours(args):
     # the 15 GB of weights streamed every iteration exceed the 129 MB L2, so no
     # flush is needed between steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_rank{rank}.csv")
+    clocks = ClockSampler(args.clock_log.replace("{rank}", str(rank)) if args.clock_log else
+                          os.path.join(tempfile.gettempdir(), f"dinfer_clocks_rank{rank}.csv"))
     iters = []
     with clocks:
         if world > 1:
@@ -506,6 +507,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llada8b_b1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="CSV of the nvidia-smi clock samples taken during the timed region "
+                         "('{rank}' is replaced by the rank; default: the temp directory)")
     ap.add_argument("--profile", choices=["iteration", "refresh", "gemm", "lmhead", "attention"], default=None)
     ap.add_argument("--gemm", type=int, nargs=3, default=[64, 24576, 4096], metavar=("M", "N", "K"))
     args = ap.parse_args()
