@@ -92,17 +92,6 @@ __device__ __forceinline__ SoftmaxState sm_merge(SoftmaxState x, SoftmaxState y)
   r.s = x.s * exp2f(x.m - r.m) + y.s * exp2f(y.m - r.m);
   return r;
 }
-__device__ __forceinline__ SoftmaxState warp_sm_merge(SoftmaxState v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    SoftmaxState w;
-    w.m = __shfl_xor_sync(0xffffffffu, v.m, o);
-    w.s = __shfl_xor_sync(0xffffffffu, v.s, o);
-    w.a = __shfl_xor_sync(0xffffffffu, v.a, o);
-    v = sm_merge(v, w);
-  }
-  return v;
-}
 
 // ---------------------------------------------------------------------------
 // shared-memory addresses, mbarriers
@@ -139,19 +128,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of a phase (try_wait may suspend the thread for a
-// hardware time slice; a polling loop with other work must not).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 // Wait for the phase with the given parity to complete.  Gives up after
 // about kWaitCycles SM cycles (~1 s), sets *abort and returns false.
@@ -324,7 +300,5 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // attribute); allow the next kernel of the stream to start launching.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-__device__ __forceinline__ float bf16r(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 }  // namespace dinfer

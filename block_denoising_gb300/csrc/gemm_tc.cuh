@@ -24,14 +24,6 @@
 
 namespace dinfer {
 
-enum EpiKind : int {
-  EPI_STORE_F32 = 0,   // out_f32[m * ldo + n] = acc
-  EPI_STORE_BF16 = 1,  // out_bf16[m * ldo + n] = bf16(acc)
-  EPI_RESID = 2,       // resid[m * N + n] += acc
-  EPI_QKV = 3,         // q (RoPE) -> q_out; k (RoPE), v -> dual cache slots
-  EPI_SWIGLU = 4,      // tile rows 0-63 gate, 64-127 up -> act = bf16(silu(g) * u)
-};
-
 enum AMode : int {
   A_SINGLE = 0,  // one weight map, 128-row boxes
   A_THREE = 1,   // three maps (wq, wk, wv) of a_rows rows each, 128-row boxes
@@ -167,19 +159,6 @@ __device__ __forceinline__ void load_stage_a(const GemmMaps& maps, const GemmArg
     tma_load_2d(sa, &maps.a[nt / per], bar, kx, (nt % per) * 128, pol_w);
   } else {
     tma_load_2d(sa, &maps.a[0], bar, kx, nt * 128, pol_w);
-  }
-}
-// L2 prefetch of the weight tile load_stage_a would load (dense modes).
-__device__ __forceinline__ void prefetch_stage_a(const GemmMaps& maps, const GemmArgs& a, int nt, int k) {
-  const int kx = k * 64;
-  if (a.a_mode == A_PAIR) {
-    tma_prefetch_2d(&maps.a[0], kx, nt * 64);
-    tma_prefetch_2d(&maps.a[1], kx, nt * 64);
-  } else if (a.a_mode == A_THREE) {
-    const int per = a.a_rows / 128;
-    tma_prefetch_2d(&maps.a[nt / per], kx, (nt % per) * 128);
-  } else {
-    tma_prefetch_2d(&maps.a[0], kx, nt * 128);
   }
 }
 template <int BN>

@@ -90,11 +90,6 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 __device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ uint4 ld_relaxed_v4(const uint32_t* p) {
   uint4 v;
@@ -201,16 +196,6 @@ __device__ __forceinline__ void chain_prefetch_a(const ChainLoad& L, int t, int 
   }
 }
 
-__device__ __forceinline__ TileRef chain_tile(int t) {
-  TileRef r;
-  r.nt = t;
-  r.mt = 0;
-  r.a_base = 0;
-  r.b_row = 0;
-  r.m_lim = 0;
-  r.out_base = 0;
-  return r;
-}
 
 // TMA producer (one thread): weight tiles run ahead into free stages, token
 // tiles follow once their data is ready.
