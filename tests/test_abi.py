@@ -78,6 +78,9 @@ def test_calls_on_null_context_are_rejected(L):
     assert L.dinfer_block_step(None, None, None, 0.9, None) == dinfer.EINVAL
     assert L.dinfer_generate(None, None, 1, 1, 1, 1, 0.9, None, None) == dinfer.EINVAL
     assert L.dinfer_op_gemm_bf16(None, None, None, 1, 128, 64, None, 0, None) == dinfer.EINVAL
+    n = ctypes.c_int64(7)
+    assert L.dinfer_moe_experts_touched(None, ctypes.byref(n)) == dinfer.EINVAL and n.value == 7
+    assert L.dinfer_sync(None) == dinfer.EINVAL
 
 
 def _start(U, G, c):
