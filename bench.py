@@ -393,7 +393,11 @@ def run_ours(args):
 def launches_per_generation(cfg, ipb):
     """Kernels of ours launched by one generation: per forward embed + 7 per
     layer (2 norms, 4 GEMMs, attention) + final norm + LM head; per block
-    begin/inner-condition/advance; one init."""
+    begin/inner-condition/advance; one init.  MoE layers launch 11 kernels in
+    a block-rows forward (QKV, attention, O, norm, router, top-k, routing
+    tables, scatter, two grouped GEMMs, combine) and up to 14 in a refresh
+    (split-K fixups of the QKV and router GEMMs, a two-kernel counting sort);
+    they are counted as 12."""
     per_layer = 7 if not cfg.n_experts else 12
     per_fwd = 1 + per_layer * cfg.n_layers + 2
     return 1 + len(ipb) * 3 + sum(ipb) * per_fwd
