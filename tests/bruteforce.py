@@ -47,10 +47,38 @@ def silu(v):
     return v / (1.0 + math.exp(-v))
 
 
+def swiglu(wg, wu, wd, a, R):
+    """(silu(a Wg^T) * a Wu^T) Wd^T with the product rounded by R."""
+    gg, uu = matvec(wg, a), matvec(wu, a)
+    act = [R(silu(gg[i]) * uu[i]) for i in range(len(gg))]
+    return matvec(wd, act)
+
+
+def moe(desc, router, w13, w2, a, R):
+    """Mixture of experts for one row: softmax over all experts' router
+    logits; the top_k experts by probability (lower index first on equal
+    probability) each add p_e times their own SwiGLU output; the selected
+    probabilities are used as they are (no renormalisation)."""
+    E, k, fe = desc.n_experts, desc.top_k, desc.expert_ffn
+    logit = matvec(router, a)
+    top = max(logit)
+    ex = [math.exp(v - top) for v in logit]
+    z = sum(ex)
+    p = [v / z for v in ex]
+    order = sorted(range(E), key=lambda e: (-p[e], e))
+    out = [0.0] * len(a)
+    for e in order[:k]:
+        y = swiglu(w13[e][:fe], w13[e][fe:], w2[e], a, R)
+        for i in range(len(a)):
+            out[i] += p[e] * y[i]
+    return out
+
+
 def forward_logits(desc, weights, ids, bf16_mode=False):
     """Full forward of one sequence ids [L]; returns logits [L][V] (mask logit -inf).
 
-    weights: list in pointer order (dense models only), as nested lists.
+    weights: list in pointer order (dense or mixture-of-experts layers), as
+    nested lists.
     """
     R = bf16 if bf16_mode else (lambda v: v)
     d, H, hd = desc.d_model, desc.n_heads, desc.head_dim
@@ -61,7 +89,11 @@ def forward_logits(desc, weights, ids, bf16_mode=False):
         b = 1 + 9 * l
         g1, wq, wk, wv, wo, g2, wg, wu, wd = weights[b:b + 9]
         g1, g2 = [float(v) for v in g1], [float(v) for v in g2]
-        wq, wk, wv, wo, wg, wu, wd = map(_mat, (wq, wk, wv, wo, wg, wu, wd))
+        wq, wk, wv, wo = map(_mat, (wq, wk, wv, wo))
+        if getattr(desc, "n_experts", 0):   # router [E][d], w13 [E][2fe][d], w2 [E][d][fe]
+            wg, wu, wd = _mat(wg), [_mat(m) for m in wu], [_mat(m) for m in wd]
+        else:
+            wg, wu, wd = map(_mat, (wg, wu, wd))
         Q, K, V = [], [], []
         for t in range(L):
             a = [R(v) for v in rms(h[t], g1, desc.rms_eps)]
@@ -88,9 +120,10 @@ def forward_logits(desc, weights, ids, bf16_mode=False):
             ho = matvec(wo, o)
             ht = [h[t][i] + ho[i] for i in range(d)]
             a = [R(v) for v in rms(ht, g2, desc.rms_eps)]
-            gg, uu = matvec(wg, a), matvec(wu, a)
-            act = [R(silu(gg[i]) * uu[i]) for i in range(len(gg))]
-            dn = matvec(wd, act)
+            if getattr(desc, "n_experts", 0):
+                dn = moe(desc, wg, wu, wd, a, R)
+            else:
+                dn = swiglu(wg, wu, wd, a, R)
             newh.append([ht[i] + dn[i] for i in range(d)])
         h = newh
     gf = [float(v) for v in weights[1 + 9 * desc.n_layers]]

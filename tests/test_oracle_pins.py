@@ -217,6 +217,65 @@ def test_moe_all_experts_is_softmax_mixture():
     np.testing.assert_allclose(got, np.einsum("re,red->rd", p, y), rtol=1e-12)
 
 
+def _moe_hand_case():
+    """Two rows, four experts, top-2, expert FFN width 1; router logits are
+    logarithms so that the router softmax is an exact fraction:
+    row 0: logits ln[4, 2, 2, 1] -> p = [4, 2, 2, 1] / 9, experts {0, 1}
+           (experts 1 and 2 tie: the lower index is taken);
+    row 1: logits ln[1, 2, 4, 1] -> p = [1, 2, 4, 1] / 8, experts {2, 1}.
+    Expert e's gate and up rows read features 0 and 1 with weights g_e and
+    u_e, and its down column writes feature e only, so expert e alone fills
+    output feature e with silu(g_e) * u_e."""
+    d, E, fe = 4, 4, 1
+    g = np.array([1.0, -2.0, 0.5, 3.0])
+    u = np.array([2.0, -1.0, 4.0, 1.0])
+    router = np.zeros((E, d))
+    router[:, 0] = np.log([4.0, 2.0, 2.0, 1.0])
+    router[:, 1] = np.log([1.0, 2.0, 4.0, 1.0])
+    w13 = np.zeros((E, 2 * fe, d))
+    w13[:, 0, 0] = w13[:, 0, 1] = g
+    w13[:, 1, 0] = w13[:, 1, 1] = u
+    w2 = np.zeros((E, d, fe))
+    for e in range(E):
+        w2[e, e, 0] = 1.0
+    a = np.array([[1.0, 0, 0, 0], [0, 1.0, 0, 0]])
+    y = g * scipy.special.expit(g) * u          # silu(g_e) * u_e
+    expect = np.array([[4 / 9 * y[0], 2 / 9 * y[1], 0.0, 0.0],
+                       [0.0, 2 / 8 * y[1], 4 / 8 * y[2], 0.0]])
+    desc = tiny_desc(d_model=d, n_heads=1, head_dim=4, n_experts=E, top_k=2, expert_ffn=fe, ffn=0)
+    return a, {"router": router, "w13": w13, "w2": w2}, desc, expect
+
+
+def test_moe_hand_example_weights_are_the_full_softmax():
+    # 1 < k < E: the chosen experts keep their probabilities under the softmax
+    # over ALL experts (4/9 and 2/9), not renormalised over the chosen two
+    a, lw, desc, expect = _moe_hand_case()
+    got = O.moe_ffn(a, lw, desc, O.Precision("fp32"))
+    np.testing.assert_allclose(got, expect, rtol=1e-13, atol=1e-15)
+    p, idx = O.route(a, lw["router"], 2)
+    assert idx.tolist() == [[0, 1], [2, 1]]
+    np.testing.assert_allclose(p, [[4 / 9, 2 / 9, 2 / 9, 1 / 9], [1 / 8, 2 / 8, 4 / 8, 1 / 8]], rtol=1e-13)
+
+
+def _moe_model():
+    desc = tiny_desc(n_experts=4, top_k=2, expert_ffn=4, ffn=0)
+    return desc, tiny_model(desc, std=0.4)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_moe_forward_matches_bruteforce(dtype):
+    desc = tiny_desc(n_experts=4, top_k=2, expert_ffn=4, ffn=0, dtype=dtype)
+    m, ws = tiny_model(desc, std=0.4)
+    ids = np.array([3, 7, 15, 15, 1, 15])
+    bf = np.array(BF.forward_logits(desc, [w.tolist() for w in ws], list(ids), bf16_mode=(dtype == "bf16")))
+    hid = O.forward(m, ids[None], O.Cache(desc, 1, len(ids)), np.arange(len(ids)))
+    lg = O.lm_head_logits(m, hid[0])
+    fin = np.isfinite(bf)
+    assert np.array_equal(fin, np.isfinite(lg))
+    tol = 1e-9 if dtype == "fp32" else 2e-2
+    np.testing.assert_allclose(lg[fin], bf[fin], rtol=0, atol=tol)
+
+
 def test_route_topk_matches_full_sort():
     rng = np.random.default_rng(7)
     a = rng.normal(size=(40, 16))
@@ -448,9 +507,101 @@ def test_planted_mistake_is_caught(monkeypatch, name, fake):
     assert _bruteforce_gap(m, ws, desc) > 1e-6
 
 
-def test_planted_commit_mistakes_are_caught():
-    conf = np.array([0.9, 0.95, 0.2]); masked = np.ones(3, bool)
-    good = O.threshold_commit(conf, masked, 0.9)
-    # '>=' instead of '>' would commit position 0 as well
-    assert good.tolist() == [False, True, False]
-    assert (masked & (conf >= 0.9)).tolist() != good.tolist()
+COMMIT_CASES = test_threshold_commit_cases.pytestmark[0].args[1]
+
+
+def _commit_cases_failing():
+    """How many of the threshold-commit pin cases the oracle's commit fails."""
+    bad = 0
+    for conf, masked, tau, expect in COMMIT_CASES:
+        got = O.threshold_commit(np.array(conf), np.array(masked, bool), tau)
+        bad += int(got.astype(int).tolist() != expect)
+    return bad
+
+
+def _commit_ge(conf, masked, tau):
+    """'>=' in place of the strict '>' of "exceeds the threshold"."""
+    masked = np.asarray(masked, dtype=bool)
+    if not masked.any():
+        return np.zeros_like(masked)
+    sel = masked & (np.asarray(conf) >= tau)
+    if not sel.any():
+        c = np.where(masked, conf, -np.inf)
+        sel = np.zeros_like(masked)
+        sel[int(np.argmax(c))] = True
+    return sel
+
+
+def _commit_fallback_last(conf, masked, tau):
+    """Fallback to the highest position among equally confident ones."""
+    masked = np.asarray(masked, dtype=bool)
+    if not masked.any():
+        return np.zeros_like(masked)
+    sel = masked & (np.asarray(conf) > tau)
+    if not sel.any():
+        c = np.where(masked, conf, -np.inf)
+        sel = np.zeros_like(masked)
+        sel[len(c) - 1 - int(np.argmax(c[::-1]))] = True
+    return sel
+
+
+def _commit_always_argmax_only(conf, masked, tau):
+    """Only ever the single most confident position (no parallel commit)."""
+    masked = np.asarray(masked, dtype=bool)
+    sel = np.zeros_like(masked)
+    if masked.any():
+        sel[int(np.argmax(np.where(masked, conf, -np.inf)))] = True
+    return sel
+
+
+@pytest.mark.parametrize("fake", [_commit_ge, _commit_fallback_last, _commit_always_argmax_only])
+def test_planted_commit_mistakes_are_caught(monkeypatch, fake):
+    assert _commit_cases_failing() == 0
+    monkeypatch.setattr(O, "threshold_commit", fake)
+    assert _commit_cases_failing() > 0
+
+
+# MoE: each plausible slip in the routing weights must fail the hand example
+# or the brute force (1 < k < E)
+def _moe_gaps():
+    a, lw, desc, expect = _moe_hand_case()
+    hand = float(np.max(np.abs(O.moe_ffn(a, lw, desc, O.Precision("fp32")) - expect)))
+    desc2 = tiny_desc(n_experts=4, top_k=2, expert_ffn=4, ffn=0)
+    m, ws = tiny_model(desc2, std=0.4)
+    return hand, _bruteforce_gap(m, ws, desc2)
+
+
+def _route_renormalised(a, router, top_k):
+    p, idx = _ORIG["route"](a, router, top_k)
+    q = np.zeros_like(p)
+    rows = np.arange(p.shape[0])[:, None]
+    q[rows, idx] = p[rows, idx] / p[rows, idx].sum(-1, keepdims=True)
+    return q, idx
+
+
+def _route_softmax_of_chosen(a, router, top_k):
+    p, idx = _ORIG["route"](a, router, top_k)
+    lg = O.linear(a, router)
+    rows = np.arange(p.shape[0])[:, None]
+    q = np.zeros_like(p)
+    q[rows, idx] = scipy.special.softmax(lg[rows, idx], axis=-1)
+    return q, idx
+
+
+def _route_ties_to_higher_index(a, router, top_k):
+    p, _ = _ORIG["route"](a, router, top_k)
+    E = p.shape[-1]
+    rev = np.argsort(-p[:, ::-1], axis=-1, kind="stable")[:, :top_k]
+    return p, E - 1 - rev
+
+
+_ORIG["route"] = O.route
+
+
+@pytest.mark.parametrize("fake", [_route_renormalised, _route_softmax_of_chosen, _route_ties_to_higher_index])
+def test_planted_moe_routing_mistakes_are_caught(monkeypatch, fake):
+    hand, brute = _moe_gaps()
+    assert hand < 1e-12 and brute < 1e-9
+    monkeypatch.setattr(O, "route", fake)
+    hand, brute = _moe_gaps()
+    assert max(hand, brute) > 1e-6
