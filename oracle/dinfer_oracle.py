@@ -4,8 +4,8 @@ TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
 only the tests, the smoke check and the benchmark's CPU-baseline leg do.  It
 shares no code with the CUDA library.
 
-Plain numpy in float64 (a matmul, einsum and softmax are the only library
-primitives), written to be read against the method, not to be fast.
+Plain numpy in float64 (matmul is the only library primitive), written to be
+read against the method, not to be fast.
 
 What it follows
 ---------------
@@ -171,12 +171,22 @@ def softmax(x, axis=-1):
     return e / np.sum(e, axis=axis, keepdims=True)
 
 
-def attention(q, k, v):
-    """Bidirectional attention, no mask: q [nq,H,hd], k/v [nk,H,hd] -> [nq,H,hd]."""
+def attention(q, k, v, rows_per_group=1024):
+    """Bidirectional attention, no mask: q [nq,H,hd], k/v [nk,H,hd] -> [nq,H,hd].
+
+    o[i, h] = sum_j softmax_j(q[i, h] . k[j, h] / sqrt(hd)) v[j, h].  Every
+    query row is independent of the others; rows are taken in groups only to
+    bound the memory of the [H, rows, nk] score array at long contexts.
+    """
     hd = q.shape[-1]
-    s = np.einsum("qhd,khd->hqk", _f64(q), _f64(k)) / np.sqrt(hd)
-    p = softmax(s, axis=-1)
-    return np.einsum("hqk,khd->qhd", p, _f64(v))
+    q, kt, vh = _f64(q), _f64(k).transpose(1, 2, 0), _f64(v).transpose(1, 0, 2)
+    out = np.empty(q.shape, dtype=np.float64)
+    for r0 in range(0, q.shape[0], rows_per_group):
+        r1 = min(q.shape[0], r0 + rows_per_group)
+        s = np.matmul(q[r0:r1].transpose(1, 0, 2), kt) / np.sqrt(hd)   # [H, rows, nk]
+        p = softmax(s, axis=-1)
+        out[r0:r1] = np.matmul(p, vh).transpose(1, 0, 2)
+    return out
 
 
 def dense_ffn(a, lw, prec):

@@ -107,6 +107,11 @@ def test_attention_closed_forms():
     # no mask: permuting the keys and values together changes nothing
     perm = rng.permutation(9)
     np.testing.assert_allclose(O.attention(q, k[perm], v[perm]), O.attention(q, k, v), rtol=1e-12)
+    # query rows are independent: grouping them (memory bound) changes nothing
+    q7 = rng.normal(size=(7, 2, 4))
+    np.testing.assert_allclose(O.attention(q7, k, v, rows_per_group=2), O.attention(q7, k, v), rtol=1e-13)
+    for i in range(7):
+        np.testing.assert_allclose(O.attention(q7[i:i + 1], k, v)[0], O.attention(q7, k, v)[i], rtol=1e-13)
 
 
 # ---------------------------------------------------------------------------

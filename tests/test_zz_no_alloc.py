@@ -27,6 +27,8 @@ def L():
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.dinfer_op_gemm_bf16_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp]
     lib.dinfer_op_gemm_bf16_noalloc.restype = i32
+    lib.dinfer_op_gemm_bf16_noalloc_status.argtypes = [vp]
+    lib.dinfer_op_gemm_bf16_noalloc_status.restype = i32
     return dinfer, lib
 
 
@@ -55,6 +57,11 @@ def test_noalloc_gemm_matches_regular_entry_point_twice(L, M, N, K):
         y = Y.cpu().numpy().astype(np.float64)
         assert np.isfinite(y).all(), f"call {call}: output not fully written"
         assert np.all(np.abs(y - r) <= 2 * bound), f"call {call}"
+        # no pipeline wait timed out (the query also clears the word)
+        assert lib.dinfer_op_gemm_bf16_noalloc_status(stream) == D.OK, lib.dinfer_last_error(None)
+        if torch.cuda.get_device_properties(dev).multi_processor_count <= 152:
+            # the same schedule as the workspace entry point: the same fp32 sums
+            assert torch.equal(Y, ref), f"call {call}: not bitwise equal to dinfer_op_gemm_bf16"
 
 
 def test_noalloc_gemm_rejects_rows_beyond_its_scratch(L):
