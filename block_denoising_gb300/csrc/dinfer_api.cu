@@ -14,8 +14,10 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstddef>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -25,7 +27,6 @@
 #include "attention.cuh"
 #include "attention_tc.cuh"
 #include "gemm_tc.cuh"
-#include "layer_chain.cuh"
 #include "lmhead_tc.cuh"
 #include "moe.cuh"
 #include "noalloc.cuh"
@@ -88,14 +89,31 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t batch, uint64_t rows, 
 
 int bn_for_rows(int M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
 
-int g_num_sms = 0;
-int num_sms() {
-  if (!g_num_sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+// Per-device set-up state (SM count, kernel attributes): a process may drive
+// several GPUs, each with its own.
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+int g_num_sms[kMaxDevices] = {};
+bool g_attrs_done[kMaxDevices] = {};
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 0;
   }
-  return g_num_sms;
+  return dev;
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    std::lock_guard<std::mutex> lk(g_setup_mutex);
+    g_num_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_num_sms[dev];
 }
 
 // Launch with programmatic dependent launch (the kernel may start while the
@@ -130,8 +148,9 @@ cudaError_t launchk(void (*kernel)(ExpTypes...), dim3 grid, dim3 block, size_t s
 }
 
 bool set_smem_attrs() {
-  static bool done = false;
-  if (done) return true;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lk(g_setup_mutex);
+  if (g_attrs_done[dev]) return true;
   bool ok = true;
   ok &= cudaFuncSetAttribute(gemm_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              GemmCfg<64>::kSmem) == cudaSuccess;
@@ -147,13 +166,11 @@ bool set_smem_attrs() {
                              LmCfg<256>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtcSmem) ==
         cudaSuccess;
-  ok &= cudaFuncSetAttribute(layer_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem) ==
-        cudaSuccess;
   ok &= cudaFuncSetAttribute(lmhead_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
         cudaSuccess;
   ok &= cudaFuncSetAttribute(attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
         cudaSuccess;
-  done = ok;
+  g_attrs_done[dev] = ok;
   return ok;
 }
 
@@ -194,16 +211,14 @@ GemmSched gemm_schedule(int M, int n_tiles, int K, int BN, bool whole_only = fal
   return g;
 }
 
-cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s, bool defer_resid = false,
-                           bool whole_only = false) {
-  a.m_tiles = (a.M + BN - 1) / BN;
-  a.k_tiles = a.K / 64;
+// The schedule a GEMM launch takes: gemm_schedule, except that a GEMM whose
+// split tiles would need a fixup launch (~5 us) takes whole tiles when one SM
+// streaming its weight tiles (~85 GB/s) is not slower than all SMs streaming
+// the whole matrix (~6.8 TB/s) plus that launch.
+GemmSched launch_schedule(const GemmArgs& a, int BN, bool defer_resid, bool whole_only) {
   GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN, whole_only);
   if (gs.stream_k && !defer_resid && a.M <= 128) {
-    // a split tile here costs a fixup launch (~5 us); whole tiles are better
-    // when one SM streaming its weight tiles (~85 GB/s) is not slower than
-    // all SMs streaming the whole matrix (~6.8 TB/s) plus that launch
-    const long long tiles = (long long)a.m_tiles * a.n_tiles;
+    const long long tiles = (long long)((a.M + BN - 1) / BN) * a.n_tiles;
     const long long per = (tiles + num_sms() - 1) / num_sms();
     const long long tile_bytes = (long long)std::min(a.N, 128) * a.K * 2;
     if (per * tile_bytes / 85 <= tiles * tile_bytes / 6800 + 5000) {
@@ -211,6 +226,14 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
       gs.grid = (int)((tiles + per - 1) / per);
     }
   }
+  return gs;
+}
+
+cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_t s, bool defer_resid = false,
+                           bool whole_only = false) {
+  a.m_tiles = (a.M + BN - 1) / BN;
+  a.k_tiles = a.K / 64;
+  const GemmSched gs = launch_schedule(a, BN, defer_resid, whole_only);
   a.stream_k = gs.stream_k;
   a.grid = gs.grid;
   const long long units = (long long)a.m_tiles * a.n_tiles * (a.stream_k ? a.k_tiles : 1);
@@ -452,8 +475,6 @@ struct dinfer_ctx {
   DevState* st = nullptr;
   DevState* st_host = nullptr;  // pinned
   float* gemm_ws = nullptr;
-  uint32_t* chain_sync = nullptr;  // layer-chain counters (zero between launches)
-  int use_chain = 0;               // 1: persistent layer chain for cached iterations (DINFER_LAYER_CHAIN=1)
   SoftmaxState* lm_part = nullptr;
   int* lm_ticket = nullptr;
 
@@ -574,98 +595,6 @@ struct Fwd {
   float threshold;
 };
 
-// The persistent layer chain serves cached iterations of dense bf16 models
-// whose block rows fit one token tile, when its segment table and norm
-// layout cover the shapes.
-bool chain_fits(const dinfer_ctx* c, const Fwd& f) {
-  const dinfer_model_desc& d = c->desc;
-  if (!c->bf16 || !c->use_chain || d.n_experts || f.refresh || f.rows > 64) return false;
-  const int G = num_sms();
-  const int D = d.d_model, F = d.ffn;
-  if (f.rows > G || D % 128 || F % 64 || F / 64 > kChainMaxGuTiles)
-    return false;
-  if (3 * D / 128 > kChainMaxQkvTiles) return false;
-  // segments of one CTA: a stream-K range spans at most ceil(range / k) + 1 tiles
-  auto sk = [&](long long tiles, long long kt) {
-    const long long per = (tiles * kt + G - 1) / G;
-    return (per + kt - 1) / kt + 1;
-  };
-  auto whole = [&](long long tiles) { return (tiles + G - 1) / G; };
-  const long long n = sk(D / 128, D / 64) + whole(F / 64) + sk(D / 128, F / 64) + whole(3 * D / 128);
-  return n <= kChainMaxSegs;
-}
-
-// Layer l from the O projection to the next layer's QKV (see layer_chain.cuh).
-cudaError_t launch_chain(dinfer_ctx* c, const Fwd& f, int l, const GemmMaps& mx, const GemmMaps& mo,
-                         const GemmMaps& mact, cudaStream_t s) {
-  const dinfer_model_desc& d = c->desc;
-  const int D = d.d_model, F = d.ffn, rows = f.rows, G = num_sms();
-  const bool last = l + 1 == d.n_layers;
-  ChainMaps cm{};
-  ChainArgs ca{};
-  cm.m[CH_O] = mo;
-  cm.m[CH_O].a[0] = c->m_wo[l];
-  cm.m[CH_GU] = mx;
-  cm.m[CH_GU].a[0] = c->m_wg[l];
-  cm.m[CH_GU].a[1] = c->m_wu[l];
-  cm.m[CH_DN] = mact;
-  cm.m[CH_DN].a[0] = c->m_wd[l];
-  GemmArgs& o = ca.g[CH_O];
-  o.M = rows; o.N = D; o.K = D; o.m_tiles = 1; o.n_tiles = D / 128; o.k_tiles = D / 64; o.stream_k = 1;
-  // the partial slots of the four phases: [G][2][64 * 128] fp32 each
-  float* ws[CH_PHASES];
-  for (int ph = 0; ph < CH_PHASES; ++ph) ws[ph] = c->gemm_ws + (size_t)ph * G * 2 * 64 * 128;
-  o.a_mode = A_SINGLE; o.resid = c->h; o.ws = ws[CH_O]; o.grid = std::min(G, (D / 128) * (D / 64));
-  o.slot_tok_major = 1;
-  o.status = c->st; o.state = c->st;
-  GemmArgs& gu = ca.g[CH_GU];
-  gu.M = rows; gu.N = F; gu.K = D; gu.m_tiles = 1; gu.n_tiles = F / 64; gu.k_tiles = D / 64;
-  // gate/up and QKV: whole tiles dealt over the last CTAs (the first ones
-  // run the row norms), as many tiles per CTA as whole-tile GEMMs take
-  auto whole_grid = [&](int tiles) {
-    const int per = (tiles + G - 1) / G;
-    return (tiles + per - 1) / per;
-  };
-  gu.a_mode = A_PAIR; gu.out_bf16 = (__nv_bfloat16*)c->act; gu.ldo = F; gu.stream_k = 0;
-  gu.ws = ws[CH_GU]; gu.grid = whole_grid(F / 64);
-  ca.cta0[CH_GU] = G - gu.grid;
-  gu.status = c->st; gu.state = c->st;
-  GemmArgs& dn = ca.g[CH_DN];
-  dn.M = rows; dn.N = D; dn.K = F; dn.m_tiles = 1; dn.n_tiles = D / 128; dn.k_tiles = F / 64; dn.stream_k = 1;
-  dn.a_mode = A_SINGLE; dn.resid = c->h; dn.ws = ws[CH_DN];
-  dn.grid = std::min(G, (D / 128) * (F / 64));
-  dn.slot_tok_major = 1; dn.status = c->st; dn.state = c->st;
-  if (!last) {
-    cm.m[CH_QKV] = mx;
-    cm.m[CH_QKV].a[0] = c->m_wq[l + 1];
-    cm.m[CH_QKV].a[1] = c->m_wk[l + 1];
-    cm.m[CH_QKV].a[2] = c->m_wv[l + 1];
-    GemmArgs& qk = ca.g[CH_QKV];
-    qk.M = rows; qk.N = 3 * D; qk.K = D; qk.m_tiles = 1; qk.n_tiles = 3 * D / 128; qk.k_tiles = D / 64;
-    qk.a_mode = A_THREE; qk.a_rows = D;
-    qk.q_out = (__nv_bfloat16*)c->q;
-    qk.k_cache = (__nv_bfloat16*)c->kc_layer(l + 1);
-    qk.v_cache = (__nv_bfloat16*)c->vc_layer(l + 1);
-    qk.rope_cos = c->rope_cos; qk.rope_sin = c->rope_sin;
-    qk.d_model = D; qk.head_dim = d.head_dim;
-    qk.rows_per_seq = f.rows_per_seq; qk.seq_len = f.L; qk.pos_from_state = f.pos_from_state;
-    qk.state = c->st; qk.status = c->st; qk.stream_k = 0;
-    qk.ws = ws[CH_QKV]; qk.grid = whole_grid(3 * D / 128);
-    ca.cta0[CH_QKV] = G - qk.grid;
-  }
-  ca.has_qkv = last ? 0 : 1;
-  ca.M = rows;
-  ca.d = D;
-  ca.eps = d.rms_eps;
-  ca.g_ffn = (const __nv_bfloat16*)c->LW(l, 5);
-  ca.g_next = (const __nv_bfloat16*)(last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0));
-  ca.h = c->h;
-  ca.xn = (__nv_bfloat16*)c->xn;
-  ca.sync = c->chain_sync;
-  ca.status = c->st;
-  return launchk(layer_chain_kernel, dim3(G), dim3(kGemmThreads), kChainSmem, s, 1, cm, ca);
-}
-
 // Enqueue one forward over f.rows rows, final norm of the block rows, LM head,
 // decode and (optionally) the commit.  Works eagerly or under stream capture.
 // bf16 layer sequence (per layer, all on the tensor-core path):
@@ -699,11 +628,9 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
   const int nthr = ((D / 16 + 31) / 32) * 32;  // fused-norm threads per row: whole warps
   if (nthr > 512 || D % 128) return fail(c, DINFER_EINVAL, "d_model unsupported by the fused residual norm");
-  const bool chain = chain_fits(c, f);
   for (int l = 0; l < d.n_layers; ++l) {
-    // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue (inside the
-    // previous layer's chain after layer 0 when the chain runs)
-    if (!chain || l == 0) {
+    // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue
+    {
       GemmMaps m = mx;
       m.a[0] = c->m_wq[l];
       m.a[1] = c->m_wk[l];
@@ -724,10 +651,6 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
     // a3: attention over the dual cache
     CK(launch_attention(c->q, c->kc_layer(l), c->vc_layer(l), c->attn_o, f.batch, f.rows_per_seq, H, f.L, ap,
                         c->st, s));
-    if (chain) {  // a4 - a5 and the next a2 in one persistent launch
-      CK(launch_chain(c, f, l, mx, mo, mact, s));
-      continue;
-    }
     // a4: O projection + residual, fused with the FFN norm
     {
       GemmMaps m = mo;
@@ -1054,13 +977,6 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
   dinfer_ctx* c = new dinfer_ctx();
   c->desc = *desc;
   c->bf16 = desc->dtype == DINFER_BF16;
-  {
-    // the per-operation kernels are the default path: the chain is measured
-    // slower on the LLaDA-8B batch-1 iteration (its row norms and the
-    // cross-CTA signals cost more than the kernel boundaries they remove)
-    const char* e = getenv("DINFER_LAYER_CHAIN");
-    c->use_chain = (e && e[0] == '1') ? 1 : 0;
-  }
   c->w.assign(weights, weights + nw);
   auto bail = [&](dinfer_status s) {
     g_create_error = c->err;
@@ -1140,8 +1056,6 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
   CKC(cudaMallocHost((void**)&c->st_host, sizeof(DevState)));
   const int G = num_sms();
   AL(c->gemm_ws, gemm_ws_floats(G) * 4);
-  AL(c->chain_sync, kChainSyncWords * 4);
-  CKC(cudaMemset(c->chain_sync, 0, kChainSyncWords * 4));
   AL(c->lm_part, (size_t)G * 1024 * sizeof(SoftmaxState));
   AL(c->lm_ticket, 16);
   CKC(cudaMemset(c->lm_ticket, 0, 16));
@@ -1510,10 +1424,34 @@ extern "C" dinfer_status dinfer_op_moe_ffn_bf16(const void* X, const void* route
 // allocation-free GEMM entry point (include/dinfer_ops.h)
 // ===========================================================================
 namespace {
-// Device addresses of the fixed scratch, looked up once per device.
-constexpr int kMaxDevices = 64;
+// Device addresses of the fixed scratch and its status word, looked up once
+// per device under the set-up mutex.
 float* g_noalloc_ptr[kMaxDevices] = {};
 DevState* g_noalloc_state_ptr[kMaxDevices] = {};
+
+dinfer_status noalloc_setup(int* dev_out) {
+  dinfer_ctx* c = nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return fail(c, DINFER_ECUDA, "no current CUDA device");
+  }
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lk(g_setup_mutex);
+  if (g_noalloc_ptr[dev]) return DINFER_OK;
+  // the host-side names of the __device__ arrays are not device addresses
+  void* p = nullptr;
+  void* q = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(&q, g_noalloc_state);
+  if (e != cudaSuccess || !p || !q) {
+    cudaGetLastError();
+    return fail(c, DINFER_ECUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
+  }
+  g_noalloc_state_ptr[dev] = reinterpret_cast<DevState*>(q);
+  g_noalloc_ptr[dev] = reinterpret_cast<float*>(p);
+  return DINFER_OK;
+}
 }  // namespace
 
 extern "C" dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* W, float* Y, int32_t M, int32_t N,
@@ -1525,24 +1463,8 @@ extern "C" dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* 
                 M);
   if (N < 128 || N % 128 || K < 64 || K % 64) return fail(c, DINFER_EINVAL, "unsupported GEMM shape");
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    cudaGetLastError();
-    return fail(c, DINFER_ECUDA, "no current CUDA device");
-  }
-  // set-up on the first call on this device: the host-side names of the
-  // __device__ arrays are not device addresses, so look the addresses up
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    void* q = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e == cudaSuccess) e = cudaGetSymbolAddress(&q, g_noalloc_state);
-    if (e != cudaSuccess || !p || !q) {
-      cudaGetLastError();
-      return fail(c, DINFER_ECUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
-    }
-    g_noalloc_state_ptr[dev] = reinterpret_cast<DevState*>(q);
-    g_noalloc_ptr[dev] = reinterpret_cast<float*>(p);
-  }
+  dinfer_status st = noalloc_setup(&dev);
+  if (st != DINFER_OK) return st;
   if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
   constexpr int BN = 64;  // M <= 64: one token tile
   GemmMaps m{};
@@ -1553,9 +1475,11 @@ extern "C" dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* 
   a.out_f32 = Y; a.ldo = N;
   a.m_tiles = 1;
   a.k_tiles = K / 64;
-  const GemmSched gs = gemm_schedule(M, a.n_tiles, K, BN);
+  // the schedule dinfer_op_gemm_bf16 takes; the scratch holds two partial
+  // tiles for each of at most kNoAllocMaxCtas CTAs
+  const GemmSched gs = launch_schedule(a, BN, false, false);
   a.stream_k = gs.stream_k;
-  a.grid = std::min(gs.grid, kNoAllocMaxCtas);  // the scratch holds two partial tiles per CTA
+  a.grid = std::min(gs.grid, kNoAllocMaxCtas);
   if ((unsigned long long)a.n_tiles * (a.stream_k ? a.k_tiles : 1) * a.grid >= (1ull << 32))
     return fail(c, DINFER_EINVAL, "GEMM too large for the allocation-free entry point");
   a.slot_tok_major = 0;
@@ -1568,4 +1492,27 @@ extern "C" dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* 
   CK(launchk(gemm_tc_kernel<BN>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<BN>::kSmem, s, 1, m, a));
   if (a.stream_k) CK(launchk(splitk_fixup_kernel<BN>, dim3(a.n_tiles * 4), dim3(128), 0, s, 1, a));
   return DINFER_OK;
+}
+
+extern "C" dinfer_status dinfer_op_gemm_bf16_noalloc_status(void* stream) {
+  dinfer_ctx* c = nullptr;
+  int dev = 0;
+  dinfer_status st = noalloc_setup(&dev);
+  if (st != DINFER_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word[5] = {};  // status, diag[4]
+  const size_t off = offsetof(DevState, status);
+  CK(cudaStreamSynchronize(s));
+  CK(cudaMemcpyFromSymbolAsync(&word[0], g_noalloc_state, 4, off, cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyFromSymbolAsync(&word[1], g_noalloc_state, 16, offsetof(DevState, diag), cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  if (word[0] == 0) return DINFER_OK;
+  const uint32_t zero[5] = {};
+  CK(cudaMemcpyToSymbolAsync(g_noalloc_state, &zero[0], 4, off, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyToSymbolAsync(g_noalloc_state, &zero[1], 16, offsetof(DevState, diag), cudaMemcpyHostToDevice, s));
+  CK(cudaStreamSynchronize(s));
+  return fail(c, DINFER_EDEVICE,
+              "allocation-free GEMM: device status word 0x%x (1 = a pipeline wait timed out; the output of the "
+              "calls since the last check is not valid); first timeout: site 0x%x block 0x%x z/step 0x%x thread %u",
+              word[0], word[1], word[2], word[3], word[4]);
 }

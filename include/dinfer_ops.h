@@ -72,17 +72,29 @@ dinfer_status dinfer_op_moe_ffn_bf16(const void* X, const void* router, const vo
  * method itself: it exists for callers that cannot allocate device memory
  * when they run a projection -- code inside another framework's memory pool,
  * real-time paths, plug-ins that must not grow their footprint).  Same
- * operands and result as dinfer_op_gemm_bf16 for M <= 64 token rows; no
- * workspace argument and no allocation: the split-K partial tiles go to a
- * fixed 9.5 MiB array in the library's module, present on every GPU that
- * loads the library until the process exits.  The first call on a device
- * looks the array's device address up (cudaGetSymbolAddress); make that first
- * call before any stream capture.  All calls share the array, so calls that
- * overlap on the GPU race and must be serialised by the caller.
+ * operands as dinfer_op_gemm_bf16 for M <= 64 token rows, and the same
+ * schedule with its grid capped at 152 CTAs, so on a GPU of at most 152 SMs
+ * (a GB300) the result is bitwise the same.  No workspace argument and no
+ * allocation: the split-K partial tiles go to a fixed 9.5 MiB array in the
+ * library's module, present on every GPU that loads the library until the
+ * process exits.  The first call on a device looks the array's device address
+ * up (cudaGetSymbolAddress, guarded so that concurrent first calls from
+ * several host threads are safe); make that first call before any stream
+ * capture.  All calls share the array, so calls that overlap on the GPU race
+ * and must be serialised by the caller.  A pipeline wait that times out on the
+ * device is not reported by this call (it returns before the kernels run):
+ * it sets a status word that dinfer_op_gemm_bf16_noalloc_status reports.
  * Errors: DINFER_EINVAL for M > 64 or an unsupported shape, DINFER_ECUDA if
  * the set-up or a launch fails. */
 dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* W, float* Y, int32_t M, int32_t N, int32_t K,
                                           void* stream);
+
+/* Device status of the allocation-free GEMM: waits for `stream`, reads the
+ * status word its kernels share, and clears it.  DINFER_EDEVICE (with the
+ * first timed-out wait's kernel, site, CTA and thread in dinfer_last_error)
+ * means that the output of some call since the previous check is not valid;
+ * DINFER_OK that no wait timed out.  Allocates nothing. */
+dinfer_status dinfer_op_gemm_bf16_noalloc_status(void* stream);
 
 #ifdef __cplusplus
 }
