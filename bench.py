@@ -143,74 +143,116 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle on a bounded sample of the workload
 # ---------------------------------------------------------------------------
-def oracle_sample(cfg, run, iters_per_block=None):
-    """Time the oracle on one layer of a refresh, one layer of a cached
-    iteration and the LM head of one block, at the workload's full shapes;
-    extrapolate to the whole generation.  iters_per_block None: assume every
-    block completes at its refresh (an upper bound on the oracle's tokens/s)."""
+def seeded_sample_weights(cfg, n_layers, W_dev=None):
+    """The workload's own seeded weights for its first n_layers layers, the
+    final norm and the LM head, as host arrays (copied from the device copy
+    when one is given, else drawn with the same generator; on a GPU when one
+    is visible, which gives the same bits as the host generator)."""
+    import numpy as np
+    import torch
+    from block_denoising_gb300 import inputs
+    nl = cfg.n_layers
+    idx = list(range(1 + 9 * n_layers)) + [1 + 9 * nl, 2 + 9 * nl]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    out = []
+    for i in idx:
+        t = W_dev[i] if W_dev is not None else inputs.make_weight(cfg, i, 0, device=dev)
+        out.append(t.float().cpu().numpy())
+    return out
+
+
+def tiny_sample(cfg, run, n_layers=2, max_seqs=2):
+    """The oracle runs this workload's whole generation within the sample's bound."""
+    return cfg.n_layers <= n_layers and run.batch <= max_seqs and run.seq_len <= 512
+
+
+def oracle_sample(cfg, run, iters_per_block=None, W_host=None, n_layers=2, max_seqs=2):
+    """Time the oracle on a bounded sample of the workload.
+
+    The tiny model: the whole generation, timed.  The others: a model with the
+    workload's first `n_layers` seeded layers, its final norm and LM head, at
+    the workload's sequence length; for block 0 and for a middle block (earlier
+    blocks filled with seeded ids, as if committed) one refresh and two cached
+    iterations, forward and decode timed apart; at most `max_seqs` sequences
+    of the batch (sequences are independent).  The generation time is
+    extrapolated from these: forward times x (layers / n_layers), x (batch /
+    sequences timed); per block one refresh and (iterations - 1) cached
+    iterations, with this run's iteration counts (or, without them, one
+    iteration per block: an upper bound on the oracle's tokens/s)."""
     import numpy as np
     from block_denoising_gb300 import inputs
     from oracle import dinfer_oracle as O
 
     b, P, G, B = run.batch, run.prompt_len, run.gen_length, run.block_length
     L = P + G
-    # The time of the oracle's float64 matmuls does not depend on the values,
-    # so the sample uses same-shape arrays tiled from a small N(0, 0.02) block
-    # instead of regenerating the seeded weights on the host.
-    rng = np.random.default_rng(0)
-    blk = (rng.standard_normal(1 << 16) * 0.02).astype(np.float32)
-
-    def arr(shape):
-        n = int(np.prod(shape))
-        return np.resize(blk, n).reshape(shape)
-
-    one = inputs.shrink(cfg, n_layers=1)
-    shapes = [sh for (_, sh, _) in inputs.weight_specs(one)]
-    W = [np.broadcast_to(arr((1, cfg.d_model)), shapes[0])]  # embedding rows are gathered only
-    for sh, (_, _, init) in zip(shapes[1:-2], inputs.weight_specs(one)[1:-2]):
-        W.append(np.ones(sh, np.float32) if init == "ones" else arr(sh))
-    W += [np.ones(cfg.d_model, np.float32), arr(shapes[-1])]
-    m = O.Model(O.Desc.from_config(one), W)
-    x = np.full((b, L), cfg.mask_id)
-    x[:, :P] = inputs.make_prompt(cfg, b, P).numpy()
-    h_all = O.embed(m, x[0])
-    K = np.zeros((L, cfg.n_heads, cfg.head_dim))
-    V = np.zeros_like(K)
-    t0 = time.perf_counter()
-    O.layer_forward(m, 0, h_all, np.arange(L), K, V)
-    t_layer_refresh = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    hb = O.layer_forward(m, 0, h_all[P:P + B], np.arange(P, P + B), K, V)
-    t_layer_iter = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    lg = O.lm_head_logits(m, hb)
-    O.top1_confidence(lg)
-    t_lm = time.perf_counter() - t0
-    per_refresh = b * (cfg.n_layers * t_layer_refresh) + b * t_lm
-    per_iter = b * (cfg.n_layers * t_layer_iter + t_lm)
     nblk = G // B
+    cores = os.cpu_count()
+    try:
+        import threadpoolctl
+        cores = max([i.get("num_threads", 0) for i in threadpoolctl.threadpool_info()] + [1])
+    except Exception:
+        pass
+    if tiny_sample(cfg, run, n_layers, max_seqs):
+        m = O.Model(O.Desc.from_config(cfg), [w.float().numpy() for w in inputs.make_weights(cfg, 0)])
+        prompt = inputs.make_prompt(cfg, b, P).numpy()
+        t0 = time.perf_counter()
+        O.generate(m, prompt, G, B, run.threshold)
+        total = time.perf_counter() - t0
+        return {"value": b * G / total, "unit": UNIT, "cores": cores, "kind": "oracle", "extrapolated": False,
+                "sample": f"float64 numpy oracle: the whole generation ({total:.2f} s), batch {b}"}
+    one = inputs.shrink(cfg, n_layers=n_layers)
+    m = O.Model(O.Desc.from_config(one), W_host if W_host is not None else seeded_sample_weights(cfg, n_layers))
+    bs = min(b, max_seqs)
+    prompt = inputs.make_prompt(cfg, b, P).numpy()[:bs]
+    rng_ids = inputs.make_prompt(cfg, bs, L, seed=2).numpy()  # stand-in for committed ids
+    mid = nblk // 2
+    t_fwd_r, t_fwd_i, t_dec = [], [], []
+    for blk in sorted({0, mid}):
+        s0 = P + blk * B
+        x = np.full((bs, L), cfg.mask_id, dtype=np.int64)
+        x[:, :P] = prompt
+        x[:, P:s0] = rng_ids[:, P:s0]
+        mask = np.zeros((bs, L), bool)
+        mask[:, s0:] = True
+        cache = O.Cache(m.desc, bs, L)
+        t0 = time.perf_counter()
+        hid = O.forward(m, x, cache, np.arange(L))
+        t1 = time.perf_counter()
+        O.decode_block(m, hid[:, s0:s0 + B], x, mask, s0, B, run.threshold)
+        t2 = time.perf_counter()
+        t_fwd_r.append(t1 - t0)
+        t_dec.append(t2 - t1)
+        for _ in range(2):
+            t0 = time.perf_counter()
+            hid = O.forward(m, x, cache, np.arange(s0, s0 + B))
+            t1 = time.perf_counter()
+            O.decode_block(m, hid, x, mask, s0, B, run.threshold)
+            t2 = time.perf_counter()
+            t_fwd_i.append(t1 - t0)
+            t_dec.append(t2 - t1)
+    scale_l = cfg.n_layers / n_layers
+    scale_b = b / bs
+    dec = statistics.mean(t_dec) * scale_b
+    per_refresh = statistics.mean(t_fwd_r) * scale_l * scale_b + dec
+    per_iter = statistics.mean(t_fwd_i) * scale_l * scale_b + dec
     if iters_per_block is None:
         total = nblk * per_refresh
-        note = "each block assumed complete at its refresh (upper bound on oracle tokens/s)"
+        note = "every block assumed complete at its refresh (an upper bound on the oracle's tokens/s)"
     else:
         total = nblk * per_refresh + (sum(iters_per_block) - nblk) * per_iter
         note = "with the iteration counts of this run"
-    cores = os.cpu_count()  # numpy's BLAS runs on every host core
-    try:
-        import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        cores = max([i.get("num_threads", 0) for i in info] + [1])
-    except Exception:
-        pass
+    timed = sum(t_fwd_r) + sum(t_fwd_i) + sum(t_dec)
     return {
         "value": b * G / total,
         "unit": UNIT,
         "cores": cores,
         "kind": "oracle",
-        "sample": (f"float64 numpy oracle: 1 of {cfg.n_layers} layers of a refresh over L={L} rows "
-                   f"({t_layer_refresh:.2f} s), 1 layer of a cached iteration over B={B} rows "
-                   f"({t_layer_iter:.3f} s), LM head of the block ({t_lm:.2f} s), batch {b}; "
-                   f"extrapolated to {nblk} blocks, {note}"),
+        "extrapolated": True,
+        "sample": (f"float64 numpy oracle on the seeded weights of {n_layers} of {cfg.n_layers} layers + LM head, "
+                   f"{bs} of {b} sequences, L={L}: one refresh and two cached iterations of block 0 and of block "
+                   f"{mid} ({timed:.1f} s timed; refresh forward {statistics.mean(t_fwd_r):.2f} s, iteration "
+                   f"forward {statistics.mean(t_fwd_i):.3f} s, decode {statistics.mean(t_dec):.2f} s); extrapolated "
+                   f"x{scale_l:g} layers, x{scale_b:g} sequences to {nblk} blocks, {note}"),
         "us_per_refresh": per_refresh * 1e6,
         "us_per_iteration": per_iter * 1e6,
     }
@@ -224,22 +266,31 @@ def run_reference(args):
     if rank != 0:
         return
     vals = []
+    W = None
     for i in range(args.warmup + args.steps):
-        s = oracle_sample(cfg, run)
+        if W is None and not tiny_sample(cfg, run):
+            W = seeded_sample_weights(cfg, 2)  # drawn once, outside the timed samples
+        s = oracle_sample(cfg, run, W_host=W)
+        progress(f"reference sample {i + 1}: {s['value']:.4g} tokens/s")
         if i >= args.warmup:
             vals.append(s)
     v = statistics.median([s["value"] for s in vals])
     ms = 1000.0 * run.batch * run.gen_length / v
+    ex = vals[-1]["extrapolated"]
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "extrapolated": ex,
         "config": {"workload": args.workload, "description": desc, "global_batch": run.batch,
                    "seq_len": run.seq_len},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": vals[-1]["cores"], "kind": "oracle",
-                         "sample": vals[-1]["sample"]},
+                         "extrapolated": ex, "sample": vals[-1]["sample"]},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if ex:
+        line["note"] = ("ms_per_step and value are the oracle's whole-generation time extrapolated from the timed "
+                        "sample (see cpu_baseline.sample); one step times that sample")
     print(json.dumps(line), flush=True)
 
 
@@ -337,7 +388,7 @@ def run_ours(args):
     progress(f"iteration {us_iter:.1f} us, refresh {us_refresh:.1f} us")
     # ---- dominant kernel: the refresh GEMMs (tensor-bound) --------------------
     hbm, tf_burst, tf_sus, peak_src = load_peaks()
-    dom = gemm_roofline(cfg, run, dinfer, stream, tf_sus)
+    dom = gemm_roofline(cfg, run, dinfer, stream, tf_burst)
 
     # max over ranks
     t = torch.tensor([t_dev, t_e2e], dtype=torch.float64, device="cuda")
@@ -357,8 +408,10 @@ def run_ours(args):
         n_launch = launches_per_generation(cfg, ipb)
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            cpu = oracle_sample(cfg, run, ipb)
-            cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+            progress("CPU oracle sample")
+            Wh = None if tiny_sample(cfg, run) else seeded_sample_weights(cfg, 2, W)
+            cpu = oracle_sample(cfg, run, ipb, W_host=Wh)
+            cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "extrapolated", "sample")}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 * t_dev / args.steps, "higher_is_better": True,
@@ -431,13 +484,23 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
     dt = e0.elapsed_time(e1) / 1000.0 / n
     flops = 2.0 * M * N * K
     ach = flops / dt / 1e12
-    # DRAM bytes of one launch of this kernel at the LLaDA-8B shape, from one ncu
-    # capture (profiles/gemm_tc_kernel_llada8b_refresh_gateup.md)
-    traffic = 213997824 + 115565568 if (M, N, K) == (1536, 24576, 4096) else None
+    rw = NCU_DRAM_BYTES.get((M, N, K))
     return {"bound": "tensor", "kernel": f"gemm_tc_kernel<256> (refresh GEMM {M}x{N}x{K}, fp32 out)",
-            "achieved": ach, "peak": peak_tflops, "unit": "TFLOP/s", "frac": ach / peak_tflops,
-            "traffic": traffic, "traffic_unit": "bytes per launch", "us_per_launch": dt * 1e6,
-            "flops_per_launch": flops}
+            "achieved": ach, "peak": peak_tflops, "peak_kind": "measured burst (kernel timed alone)",
+            "unit": "TFLOP/s", "frac": ach / peak_tflops,
+            "traffic": None if rw is None else rw[0] + rw[1], "traffic_unit": "DRAM bytes per launch (ncu)",
+            "us_per_launch": dt * 1e6, "flops_per_launch": flops}
+
+
+# DRAM bytes (read, write) of one launch of the dominant kernel, from
+#   python bench.py --profile gemm --gemm 1536 24576 4096 &&
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+#       --profile-from-start off -k regex:gemm_tc -c 1 python bench.py --profile gemm --gemm 1536 24576 4096
+# on a GB300, taken with the current gemm_tc_kernel (a change to that kernel
+# removes the entry until it is captured again).
+NCU_DRAM_BYTES = {
+    (1536, 24576, 4096): (213997824, 115565568),
+}
 
 
 def run_profile(args):
