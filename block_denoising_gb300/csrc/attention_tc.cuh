@@ -60,6 +60,13 @@ constexpr int kAtcSmem = 1024 + kAtcOffBar + 256;
 constexpr int kAtcTmemCols = 512;       // S0 | S1 | O | unused
 constexpr float kAtcLazy = 8.0f;        // log2 growth of the max tolerated before rescaling O
 
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -195,6 +202,17 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (elect_one_sync()) {
+      // The cached keys / values outside the block slot do not depend on the
+      // preceding kernel: request them into L2 before the dependency wait (the
+      // block slot's lines are written by the preceding kernel; a prefetch only
+      // warms L2, which stays coherent).
+      for (int j = 0; j < nck; ++j) {
+        const int key0 = (c_begin + j) * kAtcKeys;
+        tma_prefetch_3d(&maps.k, hc, key0, bi);
+        tma_prefetch_3d(&maps.k, hc + 64, key0, bi);
+        tma_prefetch_3d(&maps.v, hc, key0, bi);
+        tma_prefetch_3d(&maps.v, hc + 64, key0, bi);
+      }
       pdl_wait();
       mbar_arrive_expect_tx(q_full, kAtcTile);
       tma_load_3d(sm, &maps.q, q_full, hc, row0, bi);

@@ -72,6 +72,14 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Feature layout of the row kernels (residual norms, MoE combine): thread t
+// of a row holds 16 features of the 128-feature tile t / 8, as four groups of
+// 4 consecutive features kRowGroupStride apart, starting at row_f0(t).  The 8
+// threads of a tile then read or write 128 contiguous bytes of fp32 (64 of
+// bf16) per instruction, so every cache line is fetched whole and once.
+constexpr int kRowGroupStride = 32;
+__device__ __forceinline__ int row_f0(int t) { return (t >> 3) * 128 + (t & 7) * 4; }
+
 // Online-softmax state over a set of logits, in the log2 domain:
 // m = max t, s = sum 2^(t - m), a = index of the max (lowest on ties).
 struct SoftmaxState {

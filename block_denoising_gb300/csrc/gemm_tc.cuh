@@ -690,8 +690,8 @@ __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
 // Residual GEMM finish fused with the next RMSNorm.  The O and down
 // projections leave tiles shared by several CTAs as token-major fp32 partials
 // (whole tiles were already added to h by the GEMM).  One CTA per output row r
-// (token src(r)), d / 16 threads, 16 consecutive features per thread (one
-// weight tile of 128 features per 8 threads):
+// (token src(r)), d / 16 threads, 16 features per thread in the row-kernel
+// layout (one weight tile of 128 features per 8 threads):
 //   h[src] += sum of the partials of every shared tile, in CTA order;
 //   out[r] = bf16(h[src] / sqrt(mean(h[src]^2) + eps) * g).
 struct ResidPlan {
@@ -700,7 +700,8 @@ struct ResidPlan {
   int stream_k;  // 0: the GEMM owned whole tiles, nothing left to add
 };
 
-// x = h[src, f0 .. f0+15] plus the stream-K partials of the residual GEMM
+// x = h[src] at the thread's 16 features (row-kernel layout from f0) plus the
+// stream-K partials of the residual GEMM
 // that cover those features (the tile's contributors, summed in CTA order so
 // the result does not depend on timing); h is written back when partials
 // were added (a tile owned whole by one CTA was already added by it).
@@ -709,10 +710,9 @@ template <int kBatch>
 __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src, int f0, int d, const ResidPlan& rp,
                                                float (&x)[16]) {
   float* hp = h + src * d + f0;
-  const float4* h4 = reinterpret_cast<const float4*>(hp);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float4 t = h4[i];
+    const float4 t = *reinterpret_cast<const float4*>(hp + kRowGroupStride * i);
     x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
   }
   const int m = (int)src;
@@ -734,10 +734,9 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
       const int cc = c0 + q;
       if (cc <= c_last) {
         const int w = ((unsigned)t == sc.start(cc) / sc.KT) ? 0 : 1;
-        const float4* sp = reinterpret_cast<const float4*>(rp.ws + ((size_t)cc * 2 + w) * (rp.BN * 128) +
-                                                           (size_t)ml * 128 + fl);
+        const float* sp = rp.ws + ((size_t)cc * 2 + w) * (rp.BN * 128) + (size_t)ml * 128 + fl;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) buf[q][i] = __ldcg(sp + i);
+        for (int i = 0; i < 4; ++i) buf[q][i] = __ldcg(reinterpret_cast<const float4*>(sp + kRowGroupStride * i));
       }
     }
 #pragma unroll
@@ -751,51 +750,30 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
           x[4 * i + 3] += buf[q][i].w;
         }
   }
-  float4* ho = reinterpret_cast<float4*>(hp);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) ho[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4*>(hp + kRowGroupStride * i) = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
 }
 
-// the bf16 gains g[f0 .. f0+15], packed in 8 registers
+// the bf16 gains of the thread's 16 features, packed in 8 registers
 __device__ __forceinline__ void load_gain16(const __nv_bfloat16* __restrict__ g, int f0, uint4 (&gain)[2]) {
-  const uint4* gp = reinterpret_cast<const uint4*>(g + f0);
-  gain[0] = __ldg(gp);
-  gain[1] = __ldg(gp + 1);
+  uint2* gw = reinterpret_cast<uint2*>(gain);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) gw[i] = __ldg(reinterpret_cast<const uint2*>(g + f0 + kRowGroupStride * i));
 }
 
-// out[16] = bf16(x * inv_rms * gain)
+// the thread's 16 outputs: bf16(x * inv_rms * gain)
 __device__ __forceinline__ void norm_store16g(const float (&x)[16], float inv, const uint4 (&gain)[2], int f0,
                                               __nv_bfloat16* __restrict__ out) {
-  uint4 o[2];
-  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
   const __nv_bfloat162* gb = reinterpret_cast<const __nv_bfloat162*>(gain);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float2 gf = __bfloat1622float2(gb[i]);
-    __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * i] * inv * gf.x, x[2 * i + 1] * inv * gf.y);
-    ow[i] = *reinterpret_cast<uint32_t*>(&b2);
+  for (int i = 0; i < 4; ++i) {
+    const float2 g0 = __bfloat1622float2(gb[2 * i]), g1 = __bfloat1622float2(gb[2 * i + 1]);
+    __nv_bfloat162 a0 = __floats2bfloat162_rn(x[4 * i] * inv * g0.x, x[4 * i + 1] * inv * g0.y);
+    __nv_bfloat162 a1 = __floats2bfloat162_rn(x[4 * i + 2] * inv * g1.x, x[4 * i + 3] * inv * g1.y);
+    *reinterpret_cast<uint2*>(out + f0 + kRowGroupStride * i) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&a0), *reinterpret_cast<uint32_t*>(&a1));
   }
-  uint4* op = reinterpret_cast<uint4*>(out + f0);
-  op[0] = o[0];
-  op[1] = o[1];
-}
-
-// out[16] = bf16(x * inv_rms * g[f0 .. f0+15])
-template <typename Tg>
-__device__ __forceinline__ void norm_store16(const float (&x)[16], float inv, const Tg* __restrict__ g, int f0,
-                                             __nv_bfloat16* __restrict__ out) {
-  uint4 o[2];
-  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a0 = x[2 * i] * inv * (float)g[f0 + 2 * i];
-    const float a1 = x[2 * i + 1] * inv * (float)g[f0 + 2 * i + 1];
-    __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
-    ow[i] = *reinterpret_cast<uint32_t*>(&b2);
-  }
-  uint4* op = reinterpret_cast<uint4*>(out + f0);
-  op[0] = o[0];
-  op[1] = o[1];
 }
 
 // kMany: a grid of many rows (a refresh), held to 64 registers a thread so
@@ -820,7 +798,7 @@ __global__ void __launch_bounds__(512, kMany ? 2 : 1) resid_norm_kernel(float* _
   }
   // blockDim is a whole number of warps; threads past d / 16 hold zeros
   const bool active = threadIdx.x * 16 < d;
-  const int f0 = active ? threadIdx.x * 16 : 0;
+  const int f0 = active ? row_f0(threadIdx.x) : 0;
   float x[16];
   uint4 gain[2] = {};
 #pragma unroll

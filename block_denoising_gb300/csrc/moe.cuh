@@ -241,27 +241,27 @@ __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict
     const int bi = r / rows_per_seq;
     src = (size_t)bi * L + st->block_start + (r - bi * rows_per_seq);
   }
-  // blockDim is a whole number of warps; threads past d / 16 hold zeros
+  // blockDim is a whole number of warps; threads past d / 16 hold zeros.
+  // Features in the row-kernel layout (row_f0, kRowGroupStride).
   const bool active = threadIdx.x * 16 < d;
-  const int f0 = active ? threadIdx.x * 16 : 0;
+  const int f0 = active ? row_f0(threadIdx.x) : 0;
   float* hp = h + src * d + f0;
   float x[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = 0.f;
   if (active) {
-    const float4* h4 = reinterpret_cast<const float4*>(hp);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float4 t = h4[i];
+      const float4 t = *reinterpret_cast<const float4*>(hp + kRowGroupStride * i);
       x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
     }
   }
   for (int k = 0; k < K && active; ++k) {
     const float w = topk_w[src * K + k];
-    const float4* yp = reinterpret_cast<const float4*>(y + (size_t)inv[src * K + k] * d + f0);
+    const float* yp = y + (size_t)inv[src * K + k] * d + f0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float4 t = __ldcg(yp + i);
+      const float4 t = __ldcg(reinterpret_cast<const float4*>(yp + kRowGroupStride * i));
       x[4 * i] = fmaf(w, t.x, x[4 * i]);
       x[4 * i + 1] = fmaf(w, t.y, x[4 * i + 1]);
       x[4 * i + 2] = fmaf(w, t.z, x[4 * i + 2]);
@@ -269,9 +269,9 @@ __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict
     }
   }
   if (active) {
-    float4* h4 = reinterpret_cast<float4*>(hp);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) h4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(hp + kRowGroupStride * i) = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
   }
   if (out == nullptr) {
     pdl_trigger();
@@ -290,19 +290,16 @@ __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict
   }
   __syncthreads();
   const float inv_rms = rsqrtf(red[0] / (float)d + eps);
-  uint4 o[2];
-  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a0 = x[2 * i] * inv_rms * (float)g[f0 + 2 * i];
-    const float a1 = x[2 * i + 1] * inv_rms * (float)g[f0 + 2 * i + 1];
-    __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
-    ow[i] = *reinterpret_cast<uint32_t*>(&b2);
-  }
   if (active) {
-    uint4* op = reinterpret_cast<uint4*>(out + (size_t)r * d + f0);
-    op[0] = o[0];
-    op[1] = o[1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int f = f0 + kRowGroupStride * i;
+      __nv_bfloat162 a0 = __floats2bfloat162_rn(x[4 * i] * inv_rms * (float)g[f], x[4 * i + 1] * inv_rms * (float)g[f + 1]);
+      __nv_bfloat162 a1 =
+          __floats2bfloat162_rn(x[4 * i + 2] * inv_rms * (float)g[f + 2], x[4 * i + 3] * inv_rms * (float)g[f + 3]);
+      *reinterpret_cast<uint2*>(out + (size_t)r * d + f) =
+          make_uint2(*reinterpret_cast<uint32_t*>(&a0), *reinterpret_cast<uint32_t*>(&a1));
+    }
   }
   pdl_trigger();
 }
