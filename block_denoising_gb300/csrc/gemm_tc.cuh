@@ -115,12 +115,18 @@ __device__ __forceinline__ TileRef decode_tile(const GemmArgs& a, int t) {
 
 constexpr int kGemmThreads = 192;
 
+// Pipeline depth: as many stages as fit in shared memory beside the epilogue
+// exchange buffer (the weight bytes in flight per SM set the streaming rate
+// of a CTA: nine 16 KB weight tiles at 64 tokens).
 template <int BN>
+constexpr int gemm_default_stages() { return BN == 64 ? 9 : (BN == 128 ? 6 : 4); }
+
+template <int BN, int ST = gemm_default_stages<BN>()>
 struct GemmCfg {
   static constexpr int kStageA = 128 * 64 * 2;
   static constexpr int kStageB = BN * 64 * 2;
   static constexpr int kStage = kStageA + kStageB;
-  static constexpr int kStages = (BN == 64) ? 8 : (BN == 128 ? 6 : 4);
+  static constexpr int kStages = ST;
   static constexpr int kXchgFloats = 128 * 17;
   static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStage + kXchgFloats * 4 + 512;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
@@ -363,10 +369,10 @@ struct Pipe {
 // TMA producer loop (one elected thread of warp 0).  The weight tiles of the
 // first pipeline stages do not depend on the preceding kernel, so they are
 // requested before griddepcontrol.wait; the activation tiles after it.
-template <int BN>
+template <int BN, int ST = gemm_default_stages<BN>()>
 __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArgs& a, const SegList& sl,
                                              const Pipe& p, int m_tiles) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, ST>;
   // weight tiles used by a single token tile stream through L2 once; with
   // several token tiles the following tiles re-read them from L2
   const uint64_t pol_w = (m_tiles == 1 && !a.grouped) ? l2_policy_evict_first() : l2_policy_evict_normal();
@@ -413,9 +419,9 @@ __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArg
 }
 
 // MMA issue loop (one elected thread of warp 1).
-template <int BN>
+template <int BN, int ST = gemm_default_stages<BN>()>
 __device__ __forceinline__ void run_mma(const SegList& sl, const Pipe& p, uint32_t tmem_base) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, ST>;
   constexpr uint32_t idesc = make_idesc_bf16(128, BN);
   uint32_t it = 0;
   for (int j = 0; j < sl.nseg && !*p.abort_flag; ++j) {
@@ -449,10 +455,10 @@ __device__ __forceinline__ void run_mma(const SegList& sl, const Pipe& p, uint32
 }
 
 // Carve the shared memory of a GEMM CTA and initialise its barriers.
-template <int BN>
+template <int BN, int ST = gemm_default_stages<BN>()>
 __device__ __forceinline__ Pipe setup_pipe(uint8_t* smem_raw, float*& xchg, uint32_t*& tmem_slot,
                                            volatile int*& misc) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, ST>;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Pipe p;
   p.stages = smem;

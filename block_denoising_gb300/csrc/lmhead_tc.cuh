@@ -25,18 +25,22 @@ struct LmArgs {
 template <int BN>
 struct LmCfg {
   static constexpr int kMaxM = 1024;
-  static constexpr int kSmem = GemmCfg<BN>::kSmem + kMaxM * 12 + 4 * 16 * 12 + 128;
+  // one stage fewer than a plain GEMM at 64 tokens: the running softmax
+  // states take the room
+  static constexpr int kStages = BN == 64 ? 8 : gemm_default_stages<BN>();
+  static constexpr int kSmem = GemmCfg<BN, kStages>::kSmem + kMaxM * 12 + 4 * 16 * 12 + 128;
 };
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs ga, const LmArgs la) {
-  using C = GemmCfg<BN>;
+  constexpr int ST = LmCfg<BN>::kStages;
+  using C = GemmCfg<BN, ST>;
   extern __shared__ uint8_t smem_raw[];
   float* xchg;
   uint32_t* tmem_slot;
   volatile int* misc;
-  const Pipe p = setup_pipe<BN>(smem_raw, xchg, tmem_slot, misc);
+  const Pipe p = setup_pipe<BN, ST>(smem_raw, xchg, tmem_slot, misc);
   volatile int* last_flag = misc + 1;
   // running softmax state per token, after the GEMM's shared memory
   uint8_t* extra = reinterpret_cast<uint8_t*>(const_cast<int*>(misc + 24));
@@ -75,9 +79,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) pdl_trigger();
 
   if (warp == 0) {
-    if (elect_one_sync()) run_producer<BN>(maps, ga, sl, p, ga.m_tiles);
+    if (elect_one_sync()) run_producer<BN, ST>(maps, ga, sl, p, ga.m_tiles);
   } else if (warp == 1) {
-    if (elect_one_sync()) run_mma<BN>(sl, p, tmem_base);
+    if (elect_one_sync()) run_mma<BN, ST>(sl, p, tmem_base);
   } else {
     pdl_wait();
     const int q = warp & 3;
