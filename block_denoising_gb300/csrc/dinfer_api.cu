@@ -498,6 +498,9 @@ struct dinfer_ctx {
   float* dbg_logits = nullptr;
   int32_t* dbg_tok = nullptr;
   float* dbg_conf = nullptr;
+  float* dbg_hidden = nullptr;  // [n_layers][batch * B][d] residual stream of the block rows
+  void* dbg_final = nullptr;    // [batch * B][d] LM-head input (model dtype)
+  int dbg_block_start = -1;     // block start of the forward being enqueued (host-known), -1 inside generate
 
   // geometry of the last prefill (for dinfer_block_step)
   int cur_batch = 0, cur_L = 0, cur_B = 0, cur_s = 0;
@@ -595,6 +598,17 @@ struct Fwd {
   float threshold;
 };
 
+// Test hook: copy the residual stream of the block rows after layer l (the
+// rows of a refresh sit at the block start of each sequence).
+cudaError_t debug_copy_hidden(dinfer_ctx* c, const Fwd& f, int l, cudaStream_t s) {
+  if (!c->dbg_hidden || c->dbg_block_start < 0) return cudaSuccess;
+  const size_t d = c->desc.d_model, brows = (size_t)f.batch * f.B;
+  float* dst = c->dbg_hidden + (size_t)l * brows * d;
+  if (!f.refresh) return cudaMemcpyAsync(dst, c->h, brows * d * 4, cudaMemcpyDeviceToDevice, s);
+  return cudaMemcpy2DAsync(dst, (size_t)f.B * d * 4, c->h + (size_t)c->dbg_block_start * d, (size_t)f.L * d * 4,
+                           (size_t)f.B * d * 4, f.batch, cudaMemcpyDeviceToDevice, s);
+}
+
 // Enqueue one forward over f.rows rows, final norm of the block rows, LM head,
 // decode and (optionally) the commit.  Works eagerly or under stream capture.
 // bf16 layer sequence (per layer, all on the tensor-core path):
@@ -678,6 +692,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
                  (const float*)c->moe_y, (const float*)c->moe_topk_w, (const int*)c->moe_inv, d.top_k,
                  (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps, f.B, f.L, gather,
                  (const DevState*)c->st));
+      CK(debug_copy_hidden(c, f, l, s));
       continue;
     }
     // a5: SwiGLU FFN (gate/up with the SiLU*up epilogue, down + residual)
@@ -698,6 +713,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       CK(launch_gemm_tc(m2, b, BN, s, true));
       CK(launch_resid_norm(nrows, nthr, s, c->h, (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps,
                            f.B, f.L, gather, (const DevState*)c->st, resid_plan(b, BN, c->gemm_ws)));
+      CK(debug_copy_hidden(c, f, l, s));
     }
   }
   return DINFER_OK;
@@ -749,6 +765,7 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
         gemm_f32_kernel<<<g2, 256, 0, s>>>((const float*)c->act, (const float*)c->LW(l, 8), c->h, rows, D, F, D, 1);
       }
       CK(cudaGetLastError());
+      CK(debug_copy_hidden(c, f, l, s));
     }
     // a6: final norm of the block rows (gathered from the full sequence at a refresh)
     const int brows = f.batch * f.B;
@@ -761,6 +778,8 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
 
   // a6 + a7: LM head, online softmax, threshold commit
   const int brows = f.batch * f.B;
+  if (c->dbg_final)
+    CK(cudaMemcpyAsync(c->dbg_final, c->xn, (size_t)brows * D * c->esize(), cudaMemcpyDeviceToDevice, s));
   DecodeArgs dec{};
   dec.M = brows; dec.batch = f.batch; dec.L = f.L; dec.B = f.B;
   dec.threshold = f.threshold; dec.commit = f.commit;
@@ -791,7 +810,9 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   return DINFER_OK;
 }
 
-bool debug_on(const dinfer_ctx* c) { return c->dbg_logits || c->dbg_tok || c->dbg_conf; }
+bool debug_on(const dinfer_ctx* c) {
+  return c->dbg_logits || c->dbg_tok || c->dbg_conf || c->dbg_hidden || c->dbg_final;
+}
 
 bool is_device_ptr(const void* p) {
   cudaPointerAttributes at;
@@ -1103,6 +1124,13 @@ dinfer_status dinfer_set_debug_outputs(dinfer_ctx* c, float* logits, int32_t* to
   return DINFER_OK;
 }
 
+dinfer_status dinfer_set_debug_hidden(dinfer_ctx* c, float* hidden, void* final_in) {
+  if (!c) return DINFER_EINVAL;
+  c->dbg_hidden = hidden;
+  c->dbg_final = final_in;
+  return DINFER_OK;
+}
+
 dinfer_status dinfer_sync(dinfer_ctx* c) {
   if (!c) return DINFER_EINVAL;
   return read_status(c);
@@ -1137,6 +1165,7 @@ dinfer_status dinfer_prefill_cache(dinfer_ctx* c, int32_t* ids, uint8_t* mask, i
   set_block_kernel<<<1, 1, 0, s>>>(c->st, block_start, 1);
   CK(cudaGetLastError());
   Fwd f{batch, seq_len, block_len, batch * seq_len, seq_len, 0, true, commit ? 1 : 0, 1, 0, 0, threshold};
+  c->dbg_block_start = block_start;
   if (debug_on(c)) {
     st = enqueue_forward(c, f, s);
     if (st != DINFER_OK) return st;
@@ -1177,6 +1206,7 @@ dinfer_status dinfer_block_step(dinfer_ctx* c, int32_t* ids, uint8_t* mask, floa
   set_block_kernel<<<1, 1, 0, s>>>(c->st, c->cur_s, 0);
   CK(cudaGetLastError());
   Fwd f{batch, L, B, batch * B, B, 1, false, 1, 1, 0, 0, threshold};
+  c->dbg_block_start = c->cur_s;
   dinfer_status st;
   if (debug_on(c)) {
     st = enqueue_forward(c, f, s);
@@ -1219,6 +1249,7 @@ dinfer_status dinfer_generate(dinfer_ctx* c, const int32_t* prompt, int32_t batc
                        p_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, s));
   const int B = block_length, nblk = gen_length / block_length;
   const bool eager = debug_on(c) || getenv("DINFER_NO_GRAPH") != nullptr;
+  c->dbg_block_start = -1;  // the block start advances on the device: no hidden-state copies
   if (eager) {
     init_sequence_kernel<<<256, 256, 0, s>>>(c->prompt_dev, c->ids, c->mask, batch, prompt_len, L, c->desc.mask_id,
                                              c->st, nblk);

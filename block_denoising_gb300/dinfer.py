@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
     L.dinfer_generate.restype = i32
     L.dinfer_set_debug_outputs.argtypes = [vp, vp, vp, vp]
     L.dinfer_set_debug_outputs.restype = i32
+    L.dinfer_set_debug_hidden.argtypes = [vp, vp, vp]
+    L.dinfer_set_debug_hidden.restype = i32
     L.dinfer_sync.argtypes = [vp]
     L.dinfer_sync.restype = i32
     L.dinfer_moe_experts_touched.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
@@ -159,6 +161,10 @@ class Decoder:
 
     def set_debug_outputs(self, logits=None, tok=None, conf=None):
         _check(lib().dinfer_set_debug_outputs(self.h, _ptr(logits), _ptr(tok), _ptr(conf)), self.h)
+
+    def set_debug_hidden(self, hidden=None, final_in=None):
+        """Per-layer residual stream [n_layers, rows, d] fp32 and LM-head input [rows, d] of the block rows."""
+        _check(lib().dinfer_set_debug_hidden(self.h, _ptr(hidden), _ptr(final_in)), self.h)
 
     def sync(self):
         _check(lib().dinfer_sync(self.h), self.h)

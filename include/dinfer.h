@@ -136,6 +136,16 @@ dinfer_status dinfer_generate(dinfer_ctx* ctx, const int32_t* prompt, int32_t ba
  * Calls made while any is set run without CUDA graphs. */
 dinfer_status dinfer_set_debug_outputs(dinfer_ctx* ctx, float* logits, int32_t* tok, float* conf);
 
+/* Test hook for the per-layer parity diagnostics: while set, every
+ * dinfer_prefill_cache / dinfer_block_step also writes the residual stream of
+ * the block rows after each layer, hidden [n_layers][rows][d_model] fp32, and
+ * the LM head's input (the final RMSNorm of the block rows, rounded to the
+ * model's storage type), final_in [rows][d_model] (bf16 or fp32); rows =
+ * batch * block_len, block rows in sequence order.  Either may be NULL.  Calls
+ * made while any is set run without CUDA graphs; dinfer_generate writes
+ * neither. */
+dinfer_status dinfer_set_debug_hidden(dinfer_ctx* ctx, float* hidden, void* final_in);
+
 /* Wait for the context's stream and report the device status word. */
 dinfer_status dinfer_sync(dinfer_ctx* ctx);
 

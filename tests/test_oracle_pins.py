@@ -610,3 +610,20 @@ def test_planted_moe_routing_mistakes_are_caught(monkeypatch, fake):
     monkeypatch.setattr(O, "route", fake)
     hand, brute = _moe_gaps()
     assert max(hand, brute) > 1e-6
+
+
+def test_parity_helper_generation_is_the_oracle_generation():
+    # the GPU tests replay the oracle block by block through tests/parity.py;
+    # that replay must be the oracle's own generate
+    from tests import parity as PT
+    cfg, run, _ = inputs.WORKLOADS["tiny_fp32"]
+    m = O.Model(O.Desc.from_config(cfg), [w.numpy() for w in inputs.make_weights(cfg)])
+    prompt = inputs.make_prompt(cfg, run.batch, run.prompt_len).numpy()
+    x, tr = O.generate(m, prompt, run.gen_length, run.block_length, run.threshold)
+    y, recs = PT.oracle_generation(m, prompt, run.gen_length, run.block_length, run.threshold)
+    np.testing.assert_array_equal(x, y)
+    assert len(recs) == len(tr)
+    for a, b in zip(tr, recs):
+        assert (a.block, a.iteration) == (b.block, b.iteration)
+        np.testing.assert_array_equal(a.commit, b.commit)
+        np.testing.assert_array_equal(a.tok, b.tok)
