@@ -30,6 +30,12 @@ Readings where the pages are silent (each listed in the design notes):
 * the mask token's logit is excluded from argmax and softmax;
 * decoder argument ``0`` is temperature 0 (greedy top-1, no sampling);
 * the refresh forward at a block boundary is also iteration 1 of the block;
+* the KV-cache family (README "Step 3": KVCacheFactory('dual') names one
+  member of a family; README introduction: a vicinity refresh against cache
+  staleness): each cached iteration recomputes a window of positions around
+  the block -- the block (dual), the block and the suffix (prefix-only
+  cache), the block and w positions each side (vicinity refresh), or all
+  positions (no cache) -- and attends over the whole cached sequence;
 * RMSNorm gains, no biases, untied LM head, rotate-half RoPE at absolute
   positions, attention scale 1/sqrt(head_dim), no causal mask;
 * MoE: softmax over all experts, top-k by probability, weights not
@@ -361,6 +367,39 @@ def cached_step(model: Model, x, mask, s0, B, tau, cache: Cache, commit=True) ->
     return decode_block(model, hid, x, mask, s0, B, tau, commit)
 
 
+def window_step(model: Model, x, mask, s0, B, tau, cache: Cache, r0: int, r1: int, commit=True) -> StepResult:
+    """A denoising iteration that recomputes the positions [r0, r1) -- the
+    block and the part of the cache around it that the cache policy
+    refreshes -- writing their K/V into the cache, with attention over the
+    whole cached sequence; then decodes the block."""
+    assert r0 <= s0 and s0 + B <= r1
+    hid = forward(model, x, cache, np.arange(r0, r1))
+    return decode_block(model, hid[:, s0 - r0:s0 - r0 + B], x, mask, s0, B, tau, commit)
+
+
+CACHE_MODES = ("dual", "none", "prefix", "vicinity")
+
+
+def recompute_window(cache_mode: str, s0: int, B: int, L: int, w: int = 0):
+    """The positions a cached iteration recomputes under each KV-cache policy.
+
+    dual: the block only (prefix and suffix K/V are cached at the block
+    boundary); none: every position (no cache: full recomputation);
+    prefix: the block and the suffix after it (only the prefix is cached);
+    vicinity: the block and up to w positions on each side of it (the cached
+    K/V nearest the block are refreshed every iteration).
+    """
+    if cache_mode == "dual":
+        return s0, s0 + B
+    if cache_mode == "none":
+        return 0, L
+    if cache_mode == "prefix":
+        return s0, L
+    if cache_mode == "vicinity":
+        return max(0, s0 - w), min(L, s0 + B + w)
+    raise ValueError(cache_mode)
+
+
 def nocache_step(model: Model, x, mask, s0, B, tau, commit=True) -> StepResult:
     """Brute force: full recomputation of the whole sequence, then decode the block."""
     cache = Cache(model.desc, x.shape[0], x.shape[1])
@@ -380,11 +419,15 @@ class Iteration:
 
 
 def generate(model: Model, prompt, gen_length: int, block_length: int, tau: float,
-             cache_mode: str = "dual", keep_logits: bool = False, max_blocks: Optional[int] = None):
+             cache_mode: str = "dual", keep_logits: bool = False, max_blocks: Optional[int] = None,
+             window: int = 0):
     """Block-wise generation; returns (ids [b, P+G], list of Iteration records).
 
-    cache_mode "dual": refresh at each block boundary, cached iterations
-    inside the block; "none": full recomputation at every iteration.
+    Every block starts with a refresh (a forward over all positions that
+    fills the cache).  Its later iterations recompute the positions that
+    recompute_window gives for cache_mode ("dual": the block; "none":
+    everything -- full recomputation; "prefix": the block and the suffix;
+    "vicinity": the block and `window` positions on each side).
     """
     d = model.desc
     prompt = np.asarray(prompt, dtype=np.int64)
@@ -407,8 +450,11 @@ def generate(model: Model, prompt, gen_length: int, block_length: int, tau: floa
             xb, mb = x.copy(), mask.copy()
             if it == 1 or cache_mode == "none":
                 r = refresh_step(model, x, mask, s0, B, tau, cache)
-            else:
+            elif cache_mode == "dual":
                 r = cached_step(model, x, mask, s0, B, tau, cache)
+            else:
+                r0, r1 = recompute_window(cache_mode, s0, B, L, window)
+                r = window_step(model, x, mask, s0, B, tau, cache, r0, r1)
             trace.append(Iteration(blk, it, xb, mb, r.tok, r.conf, r.commit,
                                    r.logits if keep_logits else None))
     return x, trace

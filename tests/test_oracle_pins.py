@@ -627,3 +627,106 @@ def test_parity_helper_generation_is_the_oracle_generation():
         assert (a.block, a.iteration) == (b.block, b.iteration)
         np.testing.assert_array_equal(a.commit, b.commit)
         np.testing.assert_array_equal(a.tok, b.tok)
+
+
+# ---------------------------------------------------------------------------
+# the KV-cache family: dual, no cache, prefix-only, vicinity refresh
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("mode,s0,B,L,w,expect", [
+    ("dual", 8, 4, 20, 3, (8, 12)),
+    ("none", 8, 4, 20, 3, (0, 20)),
+    ("prefix", 8, 4, 20, 3, (8, 20)),
+    ("vicinity", 8, 4, 20, 3, (5, 15)),
+    ("vicinity", 1, 4, 20, 3, (0, 8)),      # clipped at the sequence start
+    ("vicinity", 16, 4, 20, 3, (13, 20)),   # clipped at the sequence end
+    ("vicinity", 8, 4, 20, 0, (8, 12)),     # w = 0 is the dual cache
+])
+def test_recompute_windows(mode, s0, B, L, w, expect):
+    assert O.recompute_window(mode, s0, B, L, w) == expect
+
+
+def test_window_steps_reduce_to_dual_and_no_cache():
+    desc = tiny_desc(n_layers=2, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc)
+    x, mask = _state(desc, 5, 8)
+    x[0, 5] = 3; mask[0, 5] = False        # a commit after the refresh: the cache is stale
+    s0, B, L = 5, 4, 13
+    fresh = lambda: O.Cache(desc, 1, L)
+    c1, c2 = fresh(), fresh()
+    O.refresh_step(m, *_state(desc, 5, 8), s0, B, 0.9, c1, commit=False)
+    O.refresh_step(m, *_state(desc, 5, 8), s0, B, 0.9, c2, commit=False)
+    a = O.window_step(m, x.copy(), mask.copy(), s0, B, 0.9, c1, s0, s0 + B, commit=False)
+    b = O.cached_step(m, x.copy(), mask.copy(), s0, B, 0.9, c2, commit=False)
+    np.testing.assert_array_equal(a.logits, b.logits)          # window = block: the dual cache
+    c3 = fresh()
+    O.refresh_step(m, *_state(desc, 5, 8), s0, B, 0.9, c3, commit=False)
+    full = O.window_step(m, x.copy(), mask.copy(), s0, B, 0.9, c3, 0, L, commit=False)
+    ref = O.nocache_step(m, x.copy(), mask.copy(), s0, B, 0.9, commit=False)
+    np.testing.assert_array_equal(full.logits, ref.logits)     # window = all: no cache
+
+
+def test_window_step_leaves_the_cache_outside_the_window():
+    desc = tiny_desc(n_layers=2, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc)
+    x, mask = _state(desc, 5, 8)
+    cache = O.Cache(desc, 1, 13)
+    O.refresh_step(m, x, mask.copy(), 5, 4, 0.9, cache, commit=False)
+    before = [k.copy() for k in cache.K]
+    x2 = x.copy(); x2[0, 6] = 7; mask2 = mask.copy(); mask2[0, 6] = False
+    O.window_step(m, x2, mask2, 5, 4, 0.9, cache, 3, 11, commit=False)
+    for l in range(2):
+        np.testing.assert_array_equal(cache.K[l][0, :3], before[l][0, :3])
+        np.testing.assert_array_equal(cache.K[l][0, 11:], before[l][0, 11:])
+    assert np.max(np.abs(cache.K[1][0, 3:11] - before[1][0, 3:11])) > 1e-9   # recomputed (stale no more)
+
+
+@pytest.mark.parametrize("mode", ["prefix", "vicinity", "dual"])
+def test_one_layer_every_cache_mode_equals_no_cache(mode):
+    # with one layer the cached K/V depend only on embeddings and positions,
+    # so every cache policy is exact
+    desc = tiny_desc(n_layers=1, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc, std=0.5)
+    prompt = np.array([[1, 5, 9, 2, 7]])
+    for tau in (0.9, 0.5):
+        xa, ta = O.generate(m, prompt, 12, 4, tau, cache_mode=mode, window=2)
+        xb, tb = O.generate(m, prompt, 12, 4, tau, cache_mode="none")
+        np.testing.assert_array_equal(xa, xb)
+        assert [t.commit.tolist() for t in ta] == [t.commit.tolist() for t in tb]
+
+
+def test_vicinity_wider_than_the_sequence_is_no_cache():
+    desc = tiny_desc(n_layers=2, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc, std=0.5)
+    prompt = np.array([[1, 5, 9, 2, 7]])
+    xa, ta = O.generate(m, prompt, 12, 4, 0.6, cache_mode="vicinity", window=17, keep_logits=True)
+    xb, tb = O.generate(m, prompt, 12, 4, 0.6, cache_mode="none", keep_logits=True)
+    np.testing.assert_array_equal(xa, xb)
+    for a, b in zip(ta, tb):
+        np.testing.assert_array_equal(a.logits, b.logits)
+
+
+def test_prefix_cache_is_an_approximation_between_dual_and_no_cache():
+    # two layers, after a commit: the prefix-only cache recomputes the suffix,
+    # so it differs from the dual cache and (stale prefix) from no cache
+    desc = tiny_desc(n_layers=2, vocab=32, mask_id=31)
+    m, _ = tiny_model(desc, std=0.5)
+    x, mask = _state(desc, 5, 8)
+    caches = [O.Cache(desc, 1, 13) for _ in range(2)]
+    for c in caches:
+        O.refresh_step(m, x.copy(), mask.copy(), 5, 4, 0.9, c, commit=False)
+    x[0, 5] = 3; mask[0, 5] = False
+    pre = O.window_step(m, x.copy(), mask.copy(), 5, 4, 0.9, caches[0], 5, 13, commit=False).logits
+    dual = O.cached_step(m, x.copy(), mask.copy(), 5, 4, 0.9, caches[1], commit=False).logits
+    none = O.nocache_step(m, x.copy(), mask.copy(), 5, 4, 0.9, commit=False).logits
+    fin = np.isfinite(pre)
+    assert np.max(np.abs(pre[fin] - dual[fin])) > 1e-9
+    assert np.max(np.abs(pre[fin] - none[fin])) > 1e-9
+
+
+@pytest.mark.parametrize("mode", O.CACHE_MODES)
+def test_invariants_every_cache_mode(mode):
+    desc = tiny_desc(vocab=32, mask_id=31)
+    m, _ = tiny_model(desc)
+    prompts = np.array([[1, 2, 3], [4, 5, 6]])
+    x, tr = O.generate(m, prompts, 12, 4, 0.6, cache_mode=mode, window=2)
+    check_invariants(x, tr, prompts, 3, 12, 4, 31)
