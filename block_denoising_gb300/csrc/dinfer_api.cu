@@ -370,12 +370,12 @@ ResidPlan resid_plan(const GemmArgs& a, int BN, const float* ws, bool whole_only
 // the grid is larger than one CTA per SM.
 cudaError_t launch_resid_norm(int rows, int nthr, cudaStream_t s, float* h, const __nv_bfloat16* g,
                               __nv_bfloat16* out, int d, float eps, int rows_per_seq, int L, int gather,
-                              const DevState* st, const ResidPlan& rp) {
+                              int gather_off, const DevState* st, const ResidPlan& rp) {
   if (rows > num_sms())
     return launchk(resid_norm_kernel<__nv_bfloat16, true>, dim3(rows), dim3(nthr), 0, s, 1, h, g, out, d, eps,
-                   rows_per_seq, L, gather, st, rp, 1);
+                   rows_per_seq, L, gather, gather_off, st, rp, 1);
   return launchk(resid_norm_kernel<__nv_bfloat16, false>, dim3(rows), dim3(nthr), 0, s, 1, h, g, out, d, eps,
-                 rows_per_seq, L, gather, st, rp, 1);
+                 rows_per_seq, L, gather, gather_off, st, rp, 1);
 }
 
 int lmhead_grid(int M, int V) {
@@ -505,8 +505,11 @@ struct dinfer_ctx {
   // geometry of the last prefill (for dinfer_block_step)
   int cur_batch = 0, cur_L = 0, cur_B = 0, cur_s = 0;
   bool have_prefill = false;
+  // KV-cache policy of the cached iterations (dinfer_set_cache_mode)
+  int cache_mode = DINFER_CACHE_DUAL;
+  int cache_window = 0;
 
-  std::map<std::tuple<int, int, int, int, int>, GraphSet> graphs;  // (kind, b, L, B, extra)
+  std::map<std::tuple<int, int, int, int, int, int>, GraphSet> graphs;  // (kind, b, L, B, extra, window)
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;
 
   size_t cache_layer_elems() const { return (size_t)desc.max_batch * desc.max_seq * desc.d_model; }
@@ -586,9 +589,9 @@ const char* validate_desc(const dinfer_model_desc* d) {
 // ---------------------------------------------------------------------------
 struct Fwd {
   int batch, L, B;
-  int rows;          // rows computed: batch * B (iteration) or batch * L (refresh)
-  int rows_per_seq;  // B or L
-  int pos_from_state;
+  int rows;          // rows computed: batch * rows_per_seq
+  int rows_per_seq;  // B (dual-cache iteration), L (refresh), or a window's length
+  int pos_from_state;  // 1: computed rows start at the block start (read on the device)
   bool refresh;
   // decode
   int commit;
@@ -596,6 +599,9 @@ struct Fwd {
   cudaGraphConditionalHandle cond;
   int use_cond;
   float threshold;
+  int row_off = 0;   // first computed position (added to the block start when pos_from_state)
+  // the block rows sit at offset (block start - first computed position) in each sequence's rows
+  bool gathers_block() const { return rows_per_seq != B; }
 };
 
 // Test hook: copy the residual stream of the block rows after layer l (the
@@ -604,8 +610,9 @@ cudaError_t debug_copy_hidden(dinfer_ctx* c, const Fwd& f, int l, cudaStream_t s
   if (!c->dbg_hidden || c->dbg_block_start < 0) return cudaSuccess;
   const size_t d = c->desc.d_model, brows = (size_t)f.batch * f.B;
   float* dst = c->dbg_hidden + (size_t)l * brows * d;
-  if (!f.refresh) return cudaMemcpyAsync(dst, c->h, brows * d * 4, cudaMemcpyDeviceToDevice, s);
-  return cudaMemcpy2DAsync(dst, (size_t)f.B * d * 4, c->h + (size_t)c->dbg_block_start * d, (size_t)f.L * d * 4,
+  if (!f.gathers_block()) return cudaMemcpyAsync(dst, c->h, brows * d * 4, cudaMemcpyDeviceToDevice, s);
+  const size_t off = (size_t)(c->dbg_block_start - f.row_off);  // window rows start at row_off
+  return cudaMemcpy2DAsync(dst, (size_t)f.B * d * 4, c->h + off * d, (size_t)f.rows_per_seq * d * 4,
                            (size_t)f.B * d * 4, f.batch, cudaMemcpyDeviceToDevice, s);
 }
 
@@ -621,7 +628,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   const dinfer_model_desc& d = c->desc;
   const int D = d.d_model, F = d.ffn, H = d.n_heads, hd = d.head_dim;
   const int rows = f.rows;
-  RowMap rm{f.rows_per_seq, f.L, f.pos_from_state};
+  RowMap rm{f.rows_per_seq, f.L, f.pos_from_state, f.row_off};
   CK(launchk(embed_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, 1, (const __nv_bfloat16*)c->W(0),
              (const int32_t*)c->ids, c->h, rows, D, d.vocab, rm, c->st));
   CK(launchk(rmsnorm_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(rows), dim3(256), 0, s, 1,
@@ -659,6 +666,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.rope_cos = c->rope_cos; a.rope_sin = c->rope_sin;
       a.d_model = D; a.head_dim = hd;
       a.rows_per_seq = f.rows_per_seq; a.seq_len = f.L; a.pos_from_state = f.pos_from_state;
+      a.row_off = f.row_off;
       a.state = c->st; a.ws = c->gemm_ws; a.status = c->st;
       CK(launch_gemm_tc(m, a, BN, s));
     }
@@ -674,14 +682,15 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.resid = c->h; a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
       CK(launch_gemm_tc(m, a, BNo, s, true, o_whole));
       CK(launch_resid_norm(rows, nthr, s, c->h, (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, D,
-                           d.rms_eps, f.rows_per_seq, f.L, 0, (const DevState*)c->st,
+                           d.rms_eps, f.rows_per_seq, f.L, 0, 0, (const DevState*)c->st,
                            resid_plan(a, BNo, c->gemm_ws, o_whole)));
     }
     const bool last = l + 1 == d.n_layers;
     const void* gn = last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0);
-    // after the last layer only the block rows go on (to the LM head)
+    // after the last layer only the block rows go on (to the LM head),
+    // gathered from the rows of each sequence when more rows were computed
     const int nrows = last ? f.batch * f.B : rows;
-    const int gather = last && f.refresh ? 1 : 0;
+    const int gather = last && f.gathers_block() ? 1 : 0;
     if (d.n_experts) {
       // a5': routed experts, then the weighted combine + residual + next norm
       MoeBufs mb{c->moe_logits, c->moe_topk_id, c->moe_topk_w, c->moe_rank, c->moe_chunk_cnt, c->moe_chunk_base,
@@ -690,8 +699,8 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
                          c->m_w2[l], s));
       CK(launchk(moe_combine_norm_kernel<__nv_bfloat16>, dim3(nrows), dim3(nthr), 0, s, 1, c->h,
                  (const float*)c->moe_y, (const float*)c->moe_topk_w, (const int*)c->moe_inv, d.top_k,
-                 (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps, f.B, f.L, gather,
-                 (const DevState*)c->st));
+                 (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps, f.B, f.rows_per_seq, gather,
+                 -f.row_off, (const DevState*)c->st));
       CK(debug_copy_hidden(c, f, l, s));
       continue;
     }
@@ -712,7 +721,8 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       b.resid = c->h; b.ws = c->gemm_ws; b.status = c->st; b.state = c->st;
       CK(launch_gemm_tc(m2, b, BN, s, true));
       CK(launch_resid_norm(nrows, nthr, s, c->h, (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps,
-                           f.B, f.L, gather, (const DevState*)c->st, resid_plan(b, BN, c->gemm_ws)));
+                           f.B, f.rows_per_seq, gather, -f.row_off, (const DevState*)c->st,
+                           resid_plan(b, BN, c->gemm_ws)));
       CK(debug_copy_hidden(c, f, l, s));
     }
   }
@@ -725,7 +735,7 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   const dinfer_model_desc& d = c->desc;
   const int D = d.d_model, F = d.ffn, H = d.n_heads, hd = d.head_dim;
   const int rows = f.rows;
-  RowMap rm{f.rows_per_seq, f.L, f.pos_from_state};
+  RowMap rm{f.rows_per_seq, f.L, f.pos_from_state, f.row_off};
   if (c->bf16) {
     dinfer_status st = enqueue_layers_bf16(c, f, s);
     if (st != DINFER_OK) return st;
@@ -769,10 +779,10 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
     }
     // a6: final norm of the block rows (gathered from the full sequence at a refresh)
     const int brows = f.batch * f.B;
-    RowMap rb{f.B, f.L, 1};
+    RowMap rb{f.B, f.rows_per_seq, 1, -f.row_off};
     rmsnorm_kernel<float, float><<<brows, 256, 0, s>>>(c->h, (const float*)c->W(1 + 9 * d.n_layers),
-                                                       (float*)c->xn, brows, D, d.rms_eps, f.refresh ? 1 : 0, rb,
-                                                       c->st);
+                                                       (float*)c->xn, brows, D, d.rms_eps,
+                                                       f.gathers_block() ? 1 : 0, rb, c->st);
     CK(cudaGetLastError());
   }
 
@@ -932,6 +942,86 @@ dinfer_status build_generate_graph(dinfer_ctx* c, int batch, int P, int G, int B
     return fail(c, DINFER_ECUDA, "graph instantiation failed: %s", cudaGetErrorString(e));
   }
   gs.graph = g;
+  return DINFER_OK;
+}
+
+// Positions [r0, r1) a cached iteration recomputes under the context's cache
+// policy (block start s0, block length B, sequence length L).
+void cache_window(const dinfer_ctx* c, int s0, int B, int L, int& r0, int& r1) {
+  switch (c->cache_mode) {
+    case DINFER_CACHE_NONE: r0 = 0; r1 = L; break;
+    case DINFER_CACHE_PREFIX: r0 = s0; r1 = L; break;
+    case DINFER_CACHE_VICINITY:
+      r0 = std::max(0, s0 - c->cache_window);
+      r1 = std::min(L, s0 + B + c->cache_window);
+      break;
+    default: r0 = s0; r1 = s0 + B; break;
+  }
+}
+
+// The forward of a cached iteration: the dual cache's block rows (positions
+// read on the device, one graph for every block), or a window of host-known
+// positions.
+Fwd iteration_fwd(const dinfer_ctx* c, int batch, int L, int B, int s0, float thr, int commit,
+                  cudaGraphConditionalHandle cond, int use_cond) {
+  int r0, r1;
+  cache_window(c, s0, B, L, r0, r1);
+  if (c->cache_mode == DINFER_CACHE_DUAL) return Fwd{batch, L, B, batch * B, B, 1, false, commit, 1, cond, use_cond, thr};
+  Fwd f{batch, L, B, batch * (r1 - r0), r1 - r0, 0, false, commit, 1, cond, use_cond, thr};
+  f.row_off = r0;
+  return f;
+}
+
+// Graph of a block's cached iterations for the host-driven block loop: set the
+// loop condition from the refresh's commit, then WHILE (masks left) { one
+// cached iteration over the window of block start s0 }.
+dinfer_status build_block_loop_graph(dinfer_ctx* c, int batch, int L, int B, int s0, float thr, GraphSet& gs) {
+  cudaStream_t s = c->cap_stream, s2 = c->cap_stream2;
+  cudaGraph_t g = nullptr;
+  CK(cudaGraphCreate(&g, 0));
+  cudaGraphConditionalHandle h;
+  CK(cudaGraphConditionalHandleCreate(&h, g, 0, cudaGraphCondAssignDefault));
+  cudaGraph_t body = nullptr;
+  CK(cudaStreamBeginCaptureToGraph(s, g, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
+  set_inner_cond_kernel<<<1, 1, 0, s>>>(c->st, h);
+  dinfer_status st = add_while_node(c, s, h, &body);
+  {
+    cudaGraph_t g2 = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s, &g2);
+    if (st != DINFER_OK) return st;
+    if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "capture (block loop): %s", cudaGetErrorString(e));
+  }
+  CK(cudaStreamBeginCaptureToGraph(s2, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
+  const Fwd fi = iteration_fwd(c, batch, L, B, s0, thr, 1, h, 1);
+  st = enqueue_forward(c, fi, s2);
+  {
+    cudaGraph_t g2 = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s2, &g2);
+    if (st != DINFER_OK) return st;
+    if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "capture (window iteration): %s", cudaGetErrorString(e));
+  }
+  cudaError_t e = cudaGraphInstantiate(&gs.exec, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return fail(c, DINFER_ECUDA, "graph instantiation failed: %s", cudaGetErrorString(e));
+  }
+  gs.graph = g;
+  return DINFER_OK;
+}
+
+// A graph from the context's cache (built on first use).
+template <typename Build>
+dinfer_status cached_graph(dinfer_ctx* c, const std::tuple<int, int, int, int, int, int>& key, Build build,
+                           cudaGraphExec_t* out) {
+  GraphSet& gs = c->graphs[key];
+  if (!gs.exec) {
+    dinfer_status st = build(gs);
+    if (st != DINFER_OK) {
+      c->graphs.erase(key);
+      return st;
+    }
+  }
+  *out = gs.exec;
   return DINFER_OK;
 }
 
@@ -1124,6 +1214,16 @@ dinfer_status dinfer_set_debug_outputs(dinfer_ctx* c, float* logits, int32_t* to
   return DINFER_OK;
 }
 
+dinfer_status dinfer_set_cache_mode(dinfer_ctx* c, int32_t mode, int32_t window) {
+  if (!c) return DINFER_EINVAL;
+  if (mode < DINFER_CACHE_DUAL || mode > DINFER_CACHE_VICINITY)
+    return fail(c, DINFER_EINVAL, "cache mode %d is not one of DINFER_CACHE_DUAL / NONE / PREFIX / VICINITY", mode);
+  if (window < 0) return fail(c, DINFER_EINVAL, "vicinity window must be >= 0 (got %d)", window);
+  c->cache_mode = mode;
+  c->cache_window = mode == DINFER_CACHE_VICINITY ? window : 0;
+  return DINFER_OK;
+}
+
 dinfer_status dinfer_set_debug_hidden(dinfer_ctx* c, float* hidden, void* final_in) {
   if (!c) return DINFER_EINVAL;
   c->dbg_hidden = hidden;
@@ -1170,7 +1270,7 @@ dinfer_status dinfer_prefill_cache(dinfer_ctx* c, int32_t* ids, uint8_t* mask, i
     st = enqueue_forward(c, f, s);
     if (st != DINFER_OK) return st;
   } else {
-    auto key = std::make_tuple(1, batch, seq_len, block_len, (int)(commit ? 1 : 0) ^ (int)(threshold * 1e6f) * 2);
+    auto key = std::make_tuple(1, batch, seq_len, block_len, (int)(commit ? 1 : 0) ^ (int)(threshold * 1e6f) * 2, 0);
     GraphSet& gs = c->graphs[key];
     if (!gs.exec) {
       st = build_step_graph(c, f, gs);
@@ -1205,14 +1305,16 @@ dinfer_status dinfer_block_step(dinfer_ctx* c, int32_t* ids, uint8_t* mask, floa
   CK(cudaMemcpyAsync(c->mask, mask, n, cudaMemcpyDeviceToDevice, s));
   set_block_kernel<<<1, 1, 0, s>>>(c->st, c->cur_s, 0);
   CK(cudaGetLastError());
-  Fwd f{batch, L, B, batch * B, B, 1, false, 1, 1, 0, 0, threshold};
+  int r0, r1;
+  cache_window(c, c->cur_s, B, L, r0, r1);
+  const Fwd f = iteration_fwd(c, batch, L, B, c->cur_s, threshold, 1, 0, 0);
   c->dbg_block_start = c->cur_s;
   dinfer_status st;
   if (debug_on(c)) {
     st = enqueue_forward(c, f, s);
     if (st != DINFER_OK) return st;
   } else {
-    auto key = std::make_tuple(2, batch, L, B, (int)(threshold * 1e6f));
+    auto key = std::make_tuple(2, batch, L, B, (int)(threshold * 1e6f), r0 * 65536 + (r1 - r0));
     GraphSet& gs = c->graphs[key];
     if (!gs.exec) {
       st = build_step_graph(c, f, gs);
@@ -1263,24 +1365,49 @@ dinfer_status dinfer_generate(dinfer_ctx* c, const int32_t* prompt, int32_t batc
         CK(cudaMemcpyAsync(c->st_host, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
         if (!c->st_host->any_masked || c->st_host->status) break;
-        Fwd fi{batch, L, B, batch * B, B, 1, false, 1, 1, 0, 0, threshold};
+        const Fwd fi = iteration_fwd(c, batch, L, B, prompt_len + b * B, threshold, 1, 0, 0);
         st = enqueue_forward(c, fi, s);
         if (st != DINFER_OK) return st;
       }
       advance_block_kernel<<<1, 1, 0, s>>>(c->st, B, 0, 0);
       CK(cudaGetLastError());
     }
+  } else if (c->cache_mode == DINFER_CACHE_DUAL) {
+    // one graph: block loop and iteration loop on the device
+    auto key = std::make_tuple(3, batch, prompt_len, gen_length * 4096 + block_length, (int)(threshold * 1e6f), 0);
+    cudaGraphExec_t ex;
+    st = cached_graph(c, key, [&](GraphSet& gs) {
+      return build_generate_graph(c, batch, prompt_len, gen_length, block_length, threshold, gs);
+    }, &ex);
+    if (st != DINFER_OK) return st;
+    CK(cudaGraphLaunch(ex, s));
   } else {
-    auto key = std::make_tuple(3, batch, prompt_len, gen_length * 4096 + block_length, (int)(threshold * 1e6f));
-    GraphSet& gs = c->graphs[key];
-    if (!gs.exec) {
-      st = build_generate_graph(c, batch, prompt_len, gen_length, block_length, threshold, gs);
-      if (st != DINFER_OK) {
-        c->graphs.erase(key);
-        return st;
-      }
+    // windows of host-known positions: the blocks are enqueued from the host
+    // (no synchronisation), each as its refresh graph and a graph whose
+    // conditional WHILE node runs the block's cached iterations on the device
+    init_sequence_kernel<<<256, 256, 0, s>>>(c->prompt_dev, c->ids, c->mask, batch, prompt_len, L, c->desc.mask_id,
+                                             c->st, nblk);
+    CK(cudaGetLastError());
+    const int thr = (int)(threshold * 1e6f);
+    for (int b = 0; b < nblk; ++b) {
+      const int s0 = prompt_len + b * B;
+      begin_block_kernel<<<1, 1, 0, s>>>(c->st);
+      CK(cudaGetLastError());
+      cudaGraphExec_t ex;
+      const Fwd fr{batch, L, B, batch * L, L, 0, true, 1, 1, 0, 0, threshold};
+      st = cached_graph(c, std::make_tuple(1, batch, L, B, 1 ^ thr * 2, 0),
+                        [&](GraphSet& gs) { return build_step_graph(c, fr, gs); }, &ex);
+      if (st != DINFER_OK) return st;
+      CK(cudaGraphLaunch(ex, s));
+      int r0, r1;
+      cache_window(c, s0, B, L, r0, r1);
+      st = cached_graph(c, std::make_tuple(4, batch, L, B, thr, r0 * 65536 + (r1 - r0)),
+                        [&](GraphSet& gs) { return build_block_loop_graph(c, batch, L, B, s0, threshold, gs); }, &ex);
+      if (st != DINFER_OK) return st;
+      CK(cudaGraphLaunch(ex, s));
+      advance_block_kernel<<<1, 1, 0, s>>>(c->st, B, 0, 0);
+      CK(cudaGetLastError());
     }
-    CK(cudaGraphLaunch(gs.exec, s));
   }
   // output: ids [batch, L]
   CK(cudaMemcpyAsync(out, c->ids, (size_t)batch * L * 4, o_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost,
@@ -1445,7 +1572,7 @@ extern "C" dinfer_status dinfer_op_moe_ffn_bf16(const void* X, const void* route
   CK(launchk(moe_combine_norm_kernel<__nv_bfloat16>, dim3(M), dim3(((d / 16 + 31) / 32) * 32), 0, s, 1, out,
              (const float*)b.y,
              (const float*)b.topk_w, (const int*)b.inv, K, (const __nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr,
-             d, 0.f, M, M, 0, (const DevState*)o.st));
+             d, 0.f, M, M, 0, 0, (const DevState*)o.st));
   if (topk_id) CK(cudaMemcpyAsync(topk_id, b.topk_id, pairs * 4, cudaMemcpyDeviceToDevice, s));
   if (topk_w) CK(cudaMemcpyAsync(topk_w, b.topk_w, pairs * 4, cudaMemcpyDeviceToDevice, s));
   return DINFER_OK;

@@ -54,6 +54,7 @@ struct GemmArgs {
   int rows_per_seq;        // rows of one sequence in X (block length or L)
   int seq_len;             // L (cache stride in positions)
   int pos_from_state;      // 1: position = block_start + local row; 0: local row
+  int row_off;             // added to the position (first recomputed position of a window)
   const DevState* state;
   // stream-K partial tiles
   float* ws;               // [grid][2][BN * 128] fp32
@@ -205,7 +206,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
     const int d = a.d_model;
     const int which = (nt * 128) / d;           // 0 q, 1 k, 2 v
     const int nn = nt * 128 - which * d + row;  // feature inside q/k/v
-    const int base_pos = base_pos_in >= 0 ? base_pos_in : (a.pos_from_state ? a.state->block_start : 0);
+    const int base_pos =
+        base_pos_in >= 0 ? base_pos_in : (a.pos_from_state ? a.state->block_start : 0) + a.row_off;
     float cs[16], sn[16];
     if (rope) {
 #pragma unroll
@@ -536,7 +538,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------ epilogue ------------------------------
     pdl_wait();  // global writes only after the preceding kernel completed
-    const int base_pos = (a.q_out != nullptr && a.pos_from_state) ? a.state->block_start : 0;
+    const int base_pos =
+        a.q_out != nullptr ? (a.pos_from_state ? a.state->block_start : 0) + a.row_off : 0;
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;          // output feature row inside the tile
     float rope[2][16];  // QKV: RoPE factors of the next chunk to finish
@@ -789,7 +792,8 @@ template <typename Tg, bool kMany>
 __global__ void __launch_bounds__(512, kMany ? 2 : 1) resid_norm_kernel(float* __restrict__ h, const Tg* __restrict__ g,
                                                          __nv_bfloat16* __restrict__ out, int d, float eps,
                                                          int rows_per_seq, int L, int pos_from_state,
-                                                         const DevState* st, ResidPlan rp, int trigger_early) {
+                                                         int gather_off, const DevState* st, ResidPlan rp,
+                                                         int trigger_early) {
   __shared__ float red[32];
   // the next GEMM may launch once every CTA of this grid has started (they
   // are all resident by then): it becomes resident beside the last ones and
@@ -798,9 +802,9 @@ __global__ void __launch_bounds__(512, kMany ? 2 : 1) resid_norm_kernel(float* _
   pdl_wait();
   const int r = blockIdx.x;
   size_t src = r;
-  if (pos_from_state) {  // gather the block rows of a full-sequence residual
+  if (pos_from_state) {  // gather the block rows from the L rows per sequence of the residual
     const int bi = r / rows_per_seq;
-    src = (size_t)bi * L + st->block_start + (r - bi * rows_per_seq);
+    src = (size_t)bi * L + st->block_start + gather_off + (r - bi * rows_per_seq);
   }
   // blockDim is a whole number of warps; threads past d / 16 hold zeros
   const bool active = threadIdx.x * 16 < d;

@@ -232,14 +232,14 @@ __global__ void __launch_bounds__(512) moe_combine_norm_kernel(float* __restrict
                                                                const Tg* __restrict__ g,
                                                                __nv_bfloat16* __restrict__ out, int d, float eps,
                                                                int rows_per_seq, int L, int gather,
-                                                               const DevState* st) {
+                                                               int gather_off, const DevState* st) {
   __shared__ float red[32];
   pdl_wait();
   const int r = blockIdx.x;
   size_t src = r;
   if (gather) {
     const int bi = r / rows_per_seq;
-    src = (size_t)bi * L + st->block_start + (r - bi * rows_per_seq);
+    src = (size_t)bi * L + st->block_start + gather_off + (r - bi * rows_per_seq);
   }
   // blockDim is a whole number of warps; threads past d / 16 hold zeros.
   // Features in the row-kernel layout (row_f0, kRowGroupStride).

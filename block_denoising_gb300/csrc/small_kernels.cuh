@@ -8,13 +8,15 @@
 namespace dinfer {
 
 // Row r of a rows x d activation belongs to sequence r / rows_per_seq at
-// absolute position base + r % rows_per_seq, where base is the current block
-// start (block rows) or 0 (all positions).
+// absolute position base + row_off + r % rows_per_seq, where base is the
+// current block start (pos_from_state) or 0, and row_off a fixed offset (the
+// first recomputed position of a window; 0 for the block or all positions).
 struct RowMap {
   int rows_per_seq, L, pos_from_state;
+  int row_off;
   __device__ __forceinline__ size_t seq_index(int r, const DevState* st) const {
     const int bi = r / rows_per_seq;
-    const int base = pos_from_state ? st->block_start : 0;
+    const int base = (pos_from_state ? st->block_start : 0) + row_off;
     return (size_t)bi * L + base + (r - bi * rows_per_seq);
   }
 };

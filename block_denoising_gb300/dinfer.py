@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
     L.dinfer_generate.restype = i32
     L.dinfer_set_debug_outputs.argtypes = [vp, vp, vp, vp]
     L.dinfer_set_debug_outputs.restype = i32
+    L.dinfer_set_cache_mode.argtypes = [vp, i32, i32]
+    L.dinfer_set_cache_mode.restype = i32
     L.dinfer_set_debug_hidden.argtypes = [vp, vp, vp]
     L.dinfer_set_debug_hidden.restype = i32
     L.dinfer_sync.argtypes = [vp]
@@ -161,6 +163,12 @@ class Decoder:
 
     def set_debug_outputs(self, logits=None, tok=None, conf=None):
         _check(lib().dinfer_set_debug_outputs(self.h, _ptr(logits), _ptr(tok), _ptr(conf)), self.h)
+
+    CACHE_MODES = {"dual": 0, "none": 1, "prefix": 2, "vicinity": 3}
+
+    def set_cache_mode(self, mode: str, window: int = 0):
+        """KV-cache policy of the cached iterations: "dual", "none", "prefix" or "vicinity" (window w)."""
+        _check(lib().dinfer_set_cache_mode(self.h, self.CACHE_MODES[mode], int(window)), self.h)
 
     def set_debug_hidden(self, hidden=None, final_in=None):
         """Per-layer residual stream [n_layers, rows, d] fp32 and LM-head input [rows, d] of the block rows."""

@@ -102,6 +102,22 @@ void dinfer_destroy(dinfer_ctx* ctx);
  * thread when ctx is NULL).  Valid until the next call on the context. */
 const char* dinfer_last_error(const dinfer_ctx* ctx);
 
+/* KV-cache policy of the cached iterations (the README's cache factory names
+ * the dual cache as one member of a family; its introduction adds a vicinity
+ * refresh against cache staleness).  Every block starts with a refresh (a
+ * forward over all positions that fills the cache); each later iteration of
+ * the block recomputes a window of positions around the block, writing their
+ * keys/values into the cache, and attends over the whole cached sequence:
+ *   DINFER_CACHE_DUAL      the block only (default);
+ *   DINFER_CACHE_NONE      every position (no cache: full recomputation);
+ *   DINFER_CACHE_PREFIX    the block and everything after it (prefix-only cache);
+ *   DINFER_CACHE_VICINITY  the block and `window` positions on each side of it
+ *                          (clipped to the sequence).
+ * Applies to dinfer_block_step and dinfer_generate.  Errors: DINFER_EINVAL for
+ * an unknown mode or window < 0. */
+enum { DINFER_CACHE_DUAL = 0, DINFER_CACHE_NONE = 1, DINFER_CACHE_PREFIX = 2, DINFER_CACHE_VICINITY = 3 };
+dinfer_status dinfer_set_cache_mode(dinfer_ctx* ctx, int32_t mode, int32_t window);
+
 /* Block boundary (cache refresh): full forward over ids[batch, seq_len]
  * (device, int32), storing every layer's K/V of all positions in the dual
  * cache; then decodes the block [block_start, block_start + block_len) and,
@@ -114,18 +130,22 @@ dinfer_status dinfer_prefill_cache(dinfer_ctx* ctx, int32_t* ids, uint8_t* mask,
                                    int32_t* committed);
 
 /* One cached denoising iteration of the block set by the last
- * dinfer_prefill_cache: the block rows of ids [batch, seq_len] (device) are
- * re-run against the dual cache (their fresh K/V overwrite the block slot)
- * and one threshold commit updates ids / mask in place.  committed:
+ * dinfer_prefill_cache: the block rows of ids [batch, seq_len] (device) -- or
+ * the window the cache policy recomputes -- are re-run against the cache
+ * (their fresh K/V overwrite their slots) and one threshold commit updates
+ * ids / mask in place.  committed:
  * optional device int32[batch]; 0 for a sequence whose block had no mask. */
 dinfer_status dinfer_block_step(dinfer_ctx* ctx, int32_t* ids, uint8_t* mask, float threshold, int32_t* committed);
 
 /* Whole generation: prompt [batch, prompt_len] int32 -> out [batch,
  * prompt_len + gen_length] int32 (prompt kept).  prompt and out may be host
- * or device pointers; host buffers are copied inside the call.  The block
- * loop and the iteration loop run on the device (one CUDA graph with
- * conditional nodes); the call synchronises once at the end.  gen_length
- * must be a multiple of block_length.  stats may be NULL. */
+ * or device pointers; host buffers are copied inside the call.  Dual cache:
+ * the block loop and the iteration loop run on the device (one CUDA graph
+ * with conditional nodes).  Other cache policies: the host enqueues each
+ * block (its refresh graph, then a graph whose conditional node runs the
+ * block's iterations on the device) without waiting.  The call synchronises
+ * once at the end.  gen_length must be a multiple of block_length.  stats may
+ * be NULL. */
 dinfer_status dinfer_generate(dinfer_ctx* ctx, const int32_t* prompt, int32_t batch, int32_t prompt_len,
                               int32_t gen_length, int32_t block_length, float threshold, int32_t* out,
                               dinfer_stats* stats);

@@ -132,12 +132,14 @@ def _forward_recording(m, x, cache, rows, s0, B, record):
     return np.stack(hs), (np.stack(per_layer) if record else None)
 
 
-def oracle_iterations(m, starts, B, tau, n_iters, record_hidden=False, route_margins=None):
+def oracle_iterations(m, starts, B, tau, n_iters, record_hidden=False, route_margins=None, cache_mode="dual",
+                      window=0):
     """Run the oracle from each (block index, s0, x, mask) start: the block's
     refresh (iteration 1) and up to n_iters - 1 cached iterations, committing
     as the method does.  Returns the Records in order and the state after each
     start's iterations.  With a RouteMargins context active, each Record keeps
-    its forward's router margins."""
+    its forward's router margins.  Cached iterations recompute the window
+    that cache_mode gives (dinfer_oracle.recompute_window)."""
     recs, finals = [], []
     for start in starts:
         blk, s0, x0, mask0 = start[:4]
@@ -148,13 +150,15 @@ def oracle_iterations(m, starts, B, tau, n_iters, record_hidden=False, route_mar
             if not mask[:, s0:s0 + B].any():
                 break
             xb, mb = x.copy(), mask.copy()
-            rows = np.arange(x.shape[1]) if it == 1 else np.arange(s0, s0 + B)
+            L = x.shape[1]
+            r0, r1 = (0, L) if it == 1 else O.recompute_window(cache_mode, s0, B, L, window)
+            rows = np.arange(r0, r1)
             n0 = len(route_margins.calls) if route_margins is not None else 0
             hid, per_layer = _forward_recording(m, x, cache, rows, s0, B, record_hidden)
-            blk_rows = hid[:, s0:s0 + B] if it == 1 else hid
-            st = O.decode_block(m, blk_rows, x, mask, s0, B, tau_s)
+            st = O.decode_block(m, hid[:, s0 - r0:s0 - r0 + B], x, mask, s0, B, tau_s)
             rec = Record(blk, it, s0, xb, mb, st, per_layer)
             rec.tau = tau_s
+            rec.window = (r0, r1)
             rec.margins = route_margins.calls[n0:] if route_margins is not None else None
             recs.append(rec)
         finals.append((x, mask))
@@ -183,7 +187,8 @@ def model_floor(m, recs, B, tau, route_flags=None):
                 cache = O.Cache(m.desc, x.shape[0], x.shape[1])
                 st = O.refresh_step(m, x, mask, r.s0, B, t, cache, commit=False)
             else:
-                st = O.cached_step(m, x, mask, r.s0, B, t, cache, commit=False)
+                r0, r1 = getattr(r, "window", (r.s0, r.s0 + B))
+                st = O.window_step(m, x, mask, r.s0, B, t, cache, r0, r1, commit=False)
             fin = np.isfinite(r.logits)
             if route_flags is not None:
                 fin = fin & ~route_flags[ri][:, :, None]
@@ -321,9 +326,11 @@ def route_flags_for(recs, margin, B):
         calls = r.margins
         b = r.x_before.shape[0]
         mins = np.full((b, B), np.inf)
+        r0 = getattr(r, "window", (0, 0))[0] if r.iteration > 1 else 0
         for li, mg in enumerate(calls):
             s = li % b
-            mg = mg[r.s0:r.s0 + B] if len(mg) > B else mg
+            off = r.s0 - r0  # the block rows inside the forward's rows
+            mg = mg[off:off + B]
             mins[s] = np.minimum(mins[s], mg)
         out.append(mins < margin)
     return out
@@ -359,7 +366,7 @@ def oracle_generation(m, prompt, G, B, tau, max_blocks=None, **kw):
     return x, recs
 
 
-def follow_gpu(D, dec, m, prompt, G, B, tau, tol_fn, dev):
+def follow_gpu(D, dec, m, prompt, G, B, tau, tol_fn, dev, cache_mode="dual", window=0):
     """Run the generation on the GPU step by step (dinfer_prefill_cache /
     dinfer_block_step) and check every decision against the oracle's at the
     GPU's own state (the oracle keeps a dual cache filled at the same states).
@@ -383,9 +390,12 @@ def follow_gpu(D, dec, m, prompt, G, B, tau, tol_fn, dev):
             assert it <= B, "more than block_length iterations"
             if it == 1:
                 st = O.refresh_step(m, x.copy(), mask.copy(), s0, B, tau, cache)
+                win = (0, L)
             else:
-                st = O.cached_step(m, x.copy(), mask.copy(), s0, B, tau, cache)
+                win = O.recompute_window(cache_mode, s0, B, L, window)
+                st = O.window_step(m, x.copy(), mask.copy(), s0, B, tau, cache, *win)
             rec = Record(blk, it, s0, x.copy(), mask.copy(), st)
+            rec.window = win
             recs.append(rec)
             one = gpu_compare(D, dec, [rec], m, B, tau, dict(delta=1e3), dev)
             x, mask = one["last_ids"].astype(np.int64), one["last_mask"].astype(bool)
