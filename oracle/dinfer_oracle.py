@@ -40,7 +40,10 @@ Readings where the pages are silent (each listed in the design notes):
   positions, attention scale 1/sqrt(head_dim), no causal mask;
 * MoE: softmax over all experts, top-k by probability, weights not
   renormalised;
-* eos_id is not used (every generated position is decoded);
+* eos_id (the decoder's end-of-sequence id; unused unless given): when a
+  block completes and a sequence's block holds eos_id, every later position
+  of that sequence is set to eos_id and unmasked (committed tokens are never
+  rewritten); generation ends once no sequence has masked positions left;
 * batch > 1: blocks advance in lockstep, a sequence whose block is done
   commits nothing until all are done; the fallback is per sequence.
 
@@ -418,16 +421,27 @@ class Iteration:
     logits: Optional[np.ndarray]
 
 
+def eos_stop(x, mask, s0, B, eos_id):
+    """After the block [s0, s0 + B) completed: a sequence whose block holds
+    eos_id ends there -- its later positions become eos_id, unmasked."""
+    for i in range(x.shape[0]):
+        if (x[i, s0:s0 + B] == eos_id).any():
+            x[i, s0 + B:] = eos_id
+            mask[i, s0 + B:] = False
+
+
 def generate(model: Model, prompt, gen_length: int, block_length: int, tau: float,
              cache_mode: str = "dual", keep_logits: bool = False, max_blocks: Optional[int] = None,
-             window: int = 0):
+             window: int = 0, eos_id: Optional[int] = None):
     """Block-wise generation; returns (ids [b, P+G], list of Iteration records).
 
     Every block starts with a refresh (a forward over all positions that
     fills the cache).  Its later iterations recompute the positions that
     recompute_window gives for cache_mode ("dual": the block; "none":
     everything -- full recomputation; "prefix": the block and the suffix;
-    "vicinity": the block and `window` positions on each side).
+    "vicinity": the block and `window` positions on each side).  With eos_id,
+    sequences end at the first completed block that holds it (eos_stop) and
+    the generation ends when no sequence has masked positions left.
     """
     d = model.desc
     prompt = np.asarray(prompt, dtype=np.int64)
@@ -443,6 +457,8 @@ def generate(model: Model, prompt, gen_length: int, block_length: int, tau: floa
     nblk = G // B if max_blocks is None else min(G // B, max_blocks)
     for blk in range(nblk):
         s0 = P + blk * B
+        if not mask.any():
+            break  # every sequence ended (end-of-sequence)
         it = 0
         cache = Cache(d, b, L)
         while mask[:, s0:s0 + B].any():
@@ -457,6 +473,8 @@ def generate(model: Model, prompt, gen_length: int, block_length: int, tau: floa
                 r = window_step(model, x, mask, s0, B, tau, cache, r0, r1)
             trace.append(Iteration(blk, it, xb, mb, r.tok, r.conf, r.commit,
                                    r.logits if keep_logits else None))
+        if eos_id is not None:
+            eos_stop(x, mask, s0, B, eos_id)
     return x, trace
 
 

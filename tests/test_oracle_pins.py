@@ -395,7 +395,6 @@ def test_threshold_zero_is_blockwise_argmax_of_full_forward():
 
 def check_invariants(x, trace, prompt, P, G, B, mask_id):
     for t in trace:
-        assert t.commit.sum(axis=-1).min() >= 1 or not t.mask_before[:, P + t.block * B:P + (t.block + 1) * B].all(axis=-1).any()
         for s in range(x.shape[0]):
             blk = t.mask_before[s, P + t.block * B:P + (t.block + 1) * B]
             if blk.any():
@@ -730,3 +729,91 @@ def test_invariants_every_cache_mode(mode):
     prompts = np.array([[1, 2, 3], [4, 5, 6]])
     x, tr = O.generate(m, prompts, 12, 4, 0.6, cache_mode=mode, window=2)
     check_invariants(x, tr, prompts, 3, 12, 4, 31)
+
+
+# ---------------------------------------------------------------------------
+# end-of-sequence: a sequence ends at the first completed block holding eos_id
+# ---------------------------------------------------------------------------
+def _eos_model():
+    # wider than the other tiny models so that generations vary from block to block
+    desc = tiny_desc(d_model=32, n_heads=2, head_dim=16, ffn=64, vocab=64, mask_id=63)
+    m, _ = tiny_model(desc)
+    return desc, m
+
+
+def _first_seen(x, P, B, k, avoid=()):
+    """An id that the generation x first produces in block k (>= 1)."""
+    for v in x[P + k * B:P + (k + 1) * B]:
+        if v not in x[P:P + k * B] and v not in avoid:
+            return int(v)
+    return None
+
+
+def test_eos_never_generated_changes_nothing():
+    desc, m = _eos_model()
+    prompt = np.array([[1, 2, 3]])
+    x0, t0 = O.generate(m, prompt, 12, 4, 0.6)
+    unused = next(v for v in range(63) if v not in x0[0, 3:])
+    x1, t1 = O.generate(m, prompt, 12, 4, 0.6, eos_id=unused)
+    np.testing.assert_array_equal(x0, x1)
+    assert [t.commit.tolist() for t in t0] == [t.commit.tolist() for t in t1]
+
+
+def test_eos_in_a_block_ends_the_sequence_after_it():
+    desc, m = _eos_model()
+    P, G, B = 3, 16, 4
+    for start in range(1, 40):
+        prompt = np.array([[start, start + 1, start + 2]]) % 63
+        x0, t0 = O.generate(m, prompt, G, B, 0.6)
+        for k in (1, 2):
+            eos = _first_seen(x0[0], P, B, k)
+            if eos is not None:
+                break
+        if eos is not None:
+            break
+    assert eos is not None
+    x1, t1 = O.generate(m, prompt, G, B, 0.6, eos_id=eos)
+    end = P + (k + 1) * B
+    np.testing.assert_array_equal(x1[0, :end], x0[0, :end])      # identical through block k
+    assert (x1[0, end:] == eos).all()                             # the rest is end-of-sequence
+    assert max(t.block for t in t1) == k                          # no iteration after the stop
+    assert len(t1) == sum(1 for t in t0 if t.block <= k)
+
+
+def test_eos_in_a_batch_stops_one_sequence_only():
+    desc, m = _eos_model()
+    P, G, B = 3, 16, 4
+    found = None
+    rng = np.random.default_rng(3)
+    for _ in range(60):
+        prompts = rng.integers(0, 63, size=(2, P))
+        x0, _ = O.generate(m, prompts, G, B, 0.6)
+        for k in (1, 2):
+            eos = _first_seen(x0[0], P, B, k, avoid=set(x0[1, P:].tolist()))
+            if eos is not None:
+                found = prompts, x0, eos, k
+                break
+        if found:
+            break
+    assert found is not None
+    prompts, x0, eos, k = found
+    end = P + (k + 1) * B
+    x1, t1 = O.generate(m, prompts, G, B, 0.6, eos_id=eos)
+    np.testing.assert_array_equal(x1[1], x0[1])                 # the other sequence runs to the end
+    np.testing.assert_array_equal(x1[0, :end], x0[0, :end])
+    assert (x1[0, end:] == eos).all()
+    for t in t1:                                                # the ended sequence commits nothing more
+        if t.block > k:
+            assert not t.commit[0].any()
+    check_invariants(x1, t1, prompts, P, G, B, 63)
+
+
+def test_eos_in_the_prompt_does_not_stop():
+    desc, m = _eos_model()
+    for first in range(63):
+        prompt = np.array([[first, 2, 3]])
+        x0, _ = O.generate(m, prompt, 12, 4, 0.6)
+        if first not in x0[0, 3:]:
+            break
+    x1, _ = O.generate(m, prompt, 12, 4, 0.6, eos_id=first)      # the prompt holds eos_id: no stop
+    np.testing.assert_array_equal(x0, x1)
