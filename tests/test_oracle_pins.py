@@ -393,14 +393,16 @@ def test_threshold_zero_is_blockwise_argmax_of_full_forward():
     assert x[0].tolist() == ids
 
 
-def check_invariants(x, trace, prompt, P, G, B, mask_id):
+def check_invariants(x, trace, prompt, P, G, B, mask_id, eos_id=None):
     for t in trace:
         for s in range(x.shape[0]):
             blk = t.mask_before[s, P + t.block * B:P + (t.block + 1) * B]
             if blk.any():
                 assert t.commit[s].sum() >= 1                   # >= 1 commit per iteration
             assert not (t.commit[s] & ~blk).any()               # only masked positions commit
-            assert t.mask_before[s, P + (t.block + 1) * B:].all()  # later blocks still masked
+            later = slice(P + (t.block + 1) * B, None)
+            ended = eos_id is not None and not t.mask_before[s, later].any() and (t.x_before[s, later] == eos_id).all()
+            assert t.mask_before[s, later].all() or ended       # later blocks still masked (or the sequence ended)
             assert not t.mask_before[s, :P + t.block * B].any()    # earlier blocks done
     for blk, n in O.iterations_per_block(trace).items():
         assert 1 <= n <= B                                       # <= B iterations per block
@@ -805,7 +807,7 @@ def test_eos_in_a_batch_stops_one_sequence_only():
     for t in t1:                                                # the ended sequence commits nothing more
         if t.block > k:
             assert not t.commit[0].any()
-    check_invariants(x1, t1, prompts, P, G, B, 63)
+    check_invariants(x1, t1, prompts, P, G, B, 63, eos_id=eos)
 
 
 def test_eos_in_the_prompt_does_not_stop():
