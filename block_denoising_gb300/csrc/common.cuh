@@ -37,6 +37,8 @@ struct DevState {
   int32_t any_masked;    // 1 while some sequence of the batch has masks in the block
   uint32_t diag[4];      // first timed-out wait: (kernel << 8 | site) + 1, block x | y << 16, block z | step << 16, thread
   uint32_t moe_touched;  // (MoE layer forward, expert) pairs that received rows (measurement count)
+  int32_t eos_id;        // end-of-sequence id (-1: none)
+  int32_t any_left;      // 1 while some sequence has masked positions after the current block
   int32_t committed[kMaxBatch];    // commits of the last iteration, per sequence
   int32_t iters_per_block[kMaxBlocks];
 };

@@ -508,6 +508,7 @@ struct dinfer_ctx {
   // KV-cache policy of the cached iterations (dinfer_set_cache_mode)
   int cache_mode = DINFER_CACHE_DUAL;
   int cache_window = 0;
+  int eos_id = -1;  // end-of-sequence id of dinfer_generate (-1: none)
 
   std::map<std::tuple<int, int, int, int, int, int>, GraphSet> graphs;  // (kind, b, L, B, extra, window)
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;
@@ -919,7 +920,7 @@ dinfer_status build_generate_graph(dinfer_ctx* c, int batch, int P, int G, int B
     set_inner_cond_kernel<<<1, 1, 0, s2>>>(c->st, h_i);
     st = add_while_node(c, s2, h_i, &body_i);
   }
-  if (st == DINFER_OK) advance_block_kernel<<<1, 1, 0, s2>>>(c->st, B, h_o, 1);
+  if (st == DINFER_OK) advance_block_kernel<<<1, 256, 0, s2>>>(c->st, B, h_o, 1, c->ids, c->mask, batch, L);
   {
     cudaGraph_t g2 = nullptr;
     cudaError_t e = cudaStreamEndCapture(s2, &g2);
@@ -972,34 +973,63 @@ Fwd iteration_fwd(const dinfer_ctx* c, int batch, int L, int B, int s0, float th
   return f;
 }
 
-// Graph of a block's cached iterations for the host-driven block loop: set the
-// loop condition from the refresh's commit, then WHILE (masks left) { one
-// cached iteration over the window of block start s0 }.
-dinfer_status build_block_loop_graph(dinfer_ctx* c, int batch, int L, int B, int s0, float thr, GraphSet& gs) {
+// Graph of one block for the host-driven block loop (window cache policies):
+// IF (some sequence has masked positions left) { refresh + commit; WHILE
+// (masks left in the block) { one cached iteration over the window of block
+// start s0 }; end of block (end-of-sequence, next block) }.
+dinfer_status build_block_graph(dinfer_ctx* c, int batch, int L, int B, int s0, float thr, GraphSet& gs) {
   cudaStream_t s = c->cap_stream, s2 = c->cap_stream2;
   cudaGraph_t g = nullptr;
   CK(cudaGraphCreate(&g, 0));
-  cudaGraphConditionalHandle h;
-  CK(cudaGraphConditionalHandleCreate(&h, g, 0, cudaGraphCondAssignDefault));
-  cudaGraph_t body = nullptr;
+  cudaGraphConditionalHandle h_if, h_w;
+  CK(cudaGraphConditionalHandleCreate(&h_if, g, 0, cudaGraphCondAssignDefault));
+  cudaGraph_t body_if = nullptr, body_w = nullptr;
+  dinfer_status st = DINFER_OK;
+  auto end_capture = [&](cudaStream_t cs, const char* what) -> dinfer_status {
+    cudaGraph_t g2 = nullptr;
+    cudaError_t e = cudaStreamEndCapture(cs, &g2);
+    if (st != DINFER_OK) return st;
+    if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "capture (%s): %s", what, cudaGetErrorString(e));
+    return DINFER_OK;
+  };
+  // top level: the block's condition, then its IF node
   CK(cudaStreamBeginCaptureToGraph(s, g, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
-  set_inner_cond_kernel<<<1, 1, 0, s>>>(c->st, h);
-  dinfer_status st = add_while_node(c, s, h, &body);
+  set_block_cond_kernel<<<1, 1, 0, s>>>(c->st, h_if);
   {
-    cudaGraph_t g2 = nullptr;
-    cudaError_t e = cudaStreamEndCapture(s, &g2);
-    if (st != DINFER_OK) return st;
-    if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "capture (block loop): %s", cudaGetErrorString(e));
+    cudaStreamCaptureStatus cs;
+    cudaGraph_t cg = nullptr;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t ndeps = 0;
+    cudaError_t e = cudaStreamGetCaptureInfo(s, &cs, nullptr, &cg, &deps, nullptr, &ndeps);
+    cudaGraphNodeParams p{};
+    p.type = cudaGraphNodeTypeConditional;
+    p.conditional.handle = h_if;
+    p.conditional.type = cudaGraphCondTypeIf;
+    p.conditional.size = 1;
+    cudaGraphNode_t node;
+    if (e == cudaSuccess) e = cudaGraphAddNode(&node, cg, deps, nullptr, ndeps, &p);
+    if (e == cudaSuccess) e = cudaStreamUpdateCaptureDependencies(s, &node, nullptr, 1, cudaStreamSetCaptureDependencies);
+    if (e != cudaSuccess) st = fail(c, DINFER_ECUDA, "conditional IF node: %s", cudaGetErrorString(e));
+    else body_if = p.conditional.phGraph_out[0];
   }
-  CK(cudaStreamBeginCaptureToGraph(s2, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
-  const Fwd fi = iteration_fwd(c, batch, L, B, s0, thr, 1, h, 1);
+  if ((st = end_capture(s, "block")) != DINFER_OK) return st;
+  // IF body: refresh, the iteration loop, end of block
+  CK(cudaGraphConditionalHandleCreate(&h_w, body_if, 0, cudaGraphCondAssignDefault));
+  CK(cudaStreamBeginCaptureToGraph(s2, body_if, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
+  begin_block_kernel<<<1, 1, 0, s2>>>(c->st);
+  const Fwd fr{batch, L, B, batch * L, L, 0, true, 1, 1, 0, 0, thr};
+  st = enqueue_forward(c, fr, s2);
+  if (st == DINFER_OK) {
+    set_inner_cond_kernel<<<1, 1, 0, s2>>>(c->st, h_w);
+    st = add_while_node(c, s2, h_w, &body_w);
+  }
+  if (st == DINFER_OK) advance_block_kernel<<<1, 256, 0, s2>>>(c->st, B, 0, 0, c->ids, c->mask, batch, L);
+  if ((st = end_capture(s2, "block body")) != DINFER_OK) return st;
+  // WHILE body: one cached iteration over the block's window
+  CK(cudaStreamBeginCaptureToGraph(s2, body_w, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
+  const Fwd fi = iteration_fwd(c, batch, L, B, s0, thr, 1, h_w, 1);
   st = enqueue_forward(c, fi, s2);
-  {
-    cudaGraph_t g2 = nullptr;
-    cudaError_t e = cudaStreamEndCapture(s2, &g2);
-    if (st != DINFER_OK) return st;
-    if (e != cudaSuccess) return fail(c, DINFER_ECUDA, "capture (window iteration): %s", cudaGetErrorString(e));
-  }
+  if ((st = end_capture(s2, "window iteration")) != DINFER_OK) return st;
   cudaError_t e = cudaGraphInstantiate(&gs.exec, g, 0);
   if (e != cudaSuccess) {
     cudaGraphDestroy(g);
@@ -1224,6 +1254,14 @@ dinfer_status dinfer_set_cache_mode(dinfer_ctx* c, int32_t mode, int32_t window)
   return DINFER_OK;
 }
 
+dinfer_status dinfer_set_eos(dinfer_ctx* c, int32_t eos_id) {
+  if (!c) return DINFER_EINVAL;
+  if (eos_id != -1 && (eos_id < 0 || eos_id >= c->desc.vocab || eos_id == c->desc.mask_id))
+    return fail(c, DINFER_EINVAL, "eos_id %d is neither -1 nor a token id in [0, vocab) other than mask_id", eos_id);
+  c->eos_id = eos_id;
+  return DINFER_OK;
+}
+
 dinfer_status dinfer_set_debug_hidden(dinfer_ctx* c, float* hidden, void* final_in) {
   if (!c) return DINFER_EINVAL;
   c->dbg_hidden = hidden;
@@ -1352,11 +1390,16 @@ dinfer_status dinfer_generate(dinfer_ctx* c, const int32_t* prompt, int32_t batc
   const int B = block_length, nblk = gen_length / block_length;
   const bool eager = debug_on(c) || getenv("DINFER_NO_GRAPH") != nullptr;
   c->dbg_block_start = -1;  // the block start advances on the device: no hidden-state copies
+  set_eos_kernel<<<1, 1, 0, s>>>(c->st, c->eos_id);
+  CK(cudaGetLastError());
   if (eager) {
     init_sequence_kernel<<<256, 256, 0, s>>>(c->prompt_dev, c->ids, c->mask, batch, prompt_len, L, c->desc.mask_id,
                                              c->st, nblk);
     CK(cudaGetLastError());
     for (int b = 0; b < nblk; ++b) {
+      CK(cudaMemcpyAsync(c->st_host, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, s));
+      CK(cudaStreamSynchronize(s));
+      if (!c->st_host->any_left || c->st_host->status) break;  // every sequence ended
       begin_block_kernel<<<1, 1, 0, s>>>(c->st);
       Fwd fr{batch, L, B, batch * L, L, 0, true, 1, 1, 0, 0, threshold};
       st = enqueue_forward(c, fr, s);
@@ -1369,7 +1412,7 @@ dinfer_status dinfer_generate(dinfer_ctx* c, const int32_t* prompt, int32_t batc
         st = enqueue_forward(c, fi, s);
         if (st != DINFER_OK) return st;
       }
-      advance_block_kernel<<<1, 1, 0, s>>>(c->st, B, 0, 0);
+      advance_block_kernel<<<1, 256, 0, s>>>(c->st, B, 0, 0, c->ids, c->mask, batch, L);
       CK(cudaGetLastError());
     }
   } else if (c->cache_mode == DINFER_CACHE_DUAL) {
@@ -1383,30 +1426,22 @@ dinfer_status dinfer_generate(dinfer_ctx* c, const int32_t* prompt, int32_t batc
     CK(cudaGraphLaunch(ex, s));
   } else {
     // windows of host-known positions: the blocks are enqueued from the host
-    // (no synchronisation), each as its refresh graph and a graph whose
-    // conditional WHILE node runs the block's cached iterations on the device
+    // (no synchronisation), each as a graph that runs it only while some
+    // sequence has masked positions left (refresh, then its cached iterations
+    // in a device-side loop)
     init_sequence_kernel<<<256, 256, 0, s>>>(c->prompt_dev, c->ids, c->mask, batch, prompt_len, L, c->desc.mask_id,
                                              c->st, nblk);
     CK(cudaGetLastError());
     const int thr = (int)(threshold * 1e6f);
     for (int b = 0; b < nblk; ++b) {
       const int s0 = prompt_len + b * B;
-      begin_block_kernel<<<1, 1, 0, s>>>(c->st);
-      CK(cudaGetLastError());
-      cudaGraphExec_t ex;
-      const Fwd fr{batch, L, B, batch * L, L, 0, true, 1, 1, 0, 0, threshold};
-      st = cached_graph(c, std::make_tuple(1, batch, L, B, 1 ^ thr * 2, 0),
-                        [&](GraphSet& gs) { return build_step_graph(c, fr, gs); }, &ex);
-      if (st != DINFER_OK) return st;
-      CK(cudaGraphLaunch(ex, s));
       int r0, r1;
       cache_window(c, s0, B, L, r0, r1);
+      cudaGraphExec_t ex;
       st = cached_graph(c, std::make_tuple(4, batch, L, B, thr, r0 * 65536 + (r1 - r0)),
-                        [&](GraphSet& gs) { return build_block_loop_graph(c, batch, L, B, s0, threshold, gs); }, &ex);
+                        [&](GraphSet& gs) { return build_block_graph(c, batch, L, B, s0, threshold, gs); }, &ex);
       if (st != DINFER_OK) return st;
       CK(cudaGraphLaunch(ex, s));
-      advance_block_kernel<<<1, 1, 0, s>>>(c->st, B, 0, 0);
-      CK(cudaGetLastError());
     }
   }
   // output: ids [batch, L]

@@ -296,6 +296,9 @@ __global__ void init_sequence_kernel(const int32_t* __restrict__ prompt, int32_t
     ids[i] = p < P ? prompt[(size_t)b * P + p] : mask_id;
     mask[i] = p < P ? 0 : 1;
   }
+  // blocks skipped after end-of-sequence report no iterations
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n_blocks && k < kMaxBlocks; k += gridDim.x * blockDim.x)
+    st->iters_per_block[k] = 0;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     st->block_start = P;
     st->block_index = 0;
@@ -306,6 +309,7 @@ __global__ void init_sequence_kernel(const int32_t* __restrict__ prompt, int32_t
     st->status = 0;
     st->diag[0] = 0;
     st->any_masked = 1;
+    st->any_left = 1;
   }
 }
 
@@ -320,11 +324,46 @@ __global__ void set_inner_cond_kernel(DevState* st, cudaGraphConditionalHandle h
   cudaGraphSetConditional(h, (st->any_masked && st->status == 0u) ? 1u : 0u);
 }
 
-// end of a block: move to the next one; outer loop continues while blocks remain
-__global__ void advance_block_kernel(DevState* st, int B, cudaGraphConditionalHandle h, int use_cond) {
-  st->block_index += 1;
-  st->block_start += B;
-  if (use_cond) cudaGraphSetConditional(h, (st->block_index < st->n_blocks && st->status == 0u) ? 1u : 0u);
+// End of a block (one CTA of 256 threads).  With an end-of-sequence id set,
+// a sequence whose finished block holds it ends there: its later positions
+// become the id, unmasked.  Then move to the next block; the outer loop
+// continues while blocks remain and some sequence has masked positions left.
+__global__ void __launch_bounds__(256) advance_block_kernel(DevState* st, int B, cudaGraphConditionalHandle h,
+                                                            int use_cond, int32_t* __restrict__ ids,
+                                                            uint8_t* __restrict__ mask, int batch, int L) {
+  const int s0 = st->block_start, eos = st->eos_id;
+  const int tail = s0 + B;
+  int left = 0;
+  for (int b = 0; b < batch; ++b) {
+    int32_t* x = ids + (size_t)b * L;
+    uint8_t* m = mask + (size_t)b * L;
+    int found = 0;
+    if (eos >= 0)
+      for (int r = threadIdx.x; r < B; r += blockDim.x) found |= (x[s0 + r] == eos);
+    if (__syncthreads_or(found)) {
+      for (int p = tail + threadIdx.x; p < L; p += blockDim.x) {
+        x[p] = eos;
+        m[p] = 0;
+      }
+    }
+    for (int p = tail + threadIdx.x; p < L; p += blockDim.x) left |= m[p] != 0;
+  }
+  left = __syncthreads_or(left);
+  if (threadIdx.x == 0) {
+    st->block_index += 1;
+    st->block_start += B;
+    st->any_left = left;
+    if (use_cond)
+      cudaGraphSetConditional(h, (st->block_index < st->n_blocks && st->status == 0u && left) ? 1u : 0u);
+  }
+}
+
+// The end-of-sequence id of the next generation (-1: none).
+__global__ void set_eos_kernel(DevState* st, int eos_id) { st->eos_id = eos_id; }
+
+// Condition of a block's conditional node: run it while masks are left.
+__global__ void set_block_cond_kernel(DevState* st, cudaGraphConditionalHandle h) {
+  cudaGraphSetConditional(h, (st->any_left && st->status == 0u) ? 1u : 0u);
 }
 
 // geometry of a stand-alone prefill / block step

@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
     L.dinfer_generate.restype = i32
     L.dinfer_set_debug_outputs.argtypes = [vp, vp, vp, vp]
     L.dinfer_set_debug_outputs.restype = i32
+    L.dinfer_set_eos.argtypes = [vp, i32]
+    L.dinfer_set_eos.restype = i32
     L.dinfer_set_cache_mode.argtypes = [vp, i32, i32]
     L.dinfer_set_cache_mode.restype = i32
     L.dinfer_set_debug_hidden.argtypes = [vp, vp, vp]
@@ -163,6 +165,10 @@ class Decoder:
 
     def set_debug_outputs(self, logits=None, tok=None, conf=None):
         _check(lib().dinfer_set_debug_outputs(self.h, _ptr(logits), _ptr(tok), _ptr(conf)), self.h)
+
+    def set_eos(self, eos_id: int = -1):
+        """End-of-sequence id of generate (-1: none)."""
+        _check(lib().dinfer_set_eos(self.h, int(eos_id)), self.h)
 
     CACHE_MODES = {"dual": 0, "none": 1, "prefix": 2, "vicinity": 3}
 

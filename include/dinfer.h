@@ -69,11 +69,11 @@ typedef struct dinfer_model_desc {
 } dinfer_model_desc;
 
 typedef struct dinfer_stats {
-  int32_t n_blocks;
+  int32_t n_blocks;        /* blocks of the generation (some skipped after end-of-sequence) */
   int32_t iterations;      /* denoising iterations, refreshes included */
-  int32_t refreshes;
+  int32_t refreshes;       /* blocks run */
   float ms_device;         /* device time of the call (CUDA events on the stream) */
-  int32_t* iters_per_block; /* optional caller array [n_blocks] (host), or NULL */
+  int32_t* iters_per_block; /* optional caller array [n_blocks] (host), or NULL; 0 for a skipped block */
 } dinfer_stats;
 
 /* Number of weight pointers a model takes:
@@ -117,6 +117,16 @@ const char* dinfer_last_error(const dinfer_ctx* ctx);
  * an unknown mode or window < 0. */
 enum { DINFER_CACHE_DUAL = 0, DINFER_CACHE_NONE = 1, DINFER_CACHE_PREFIX = 2, DINFER_CACHE_VICINITY = 3 };
 dinfer_status dinfer_set_cache_mode(dinfer_ctx* ctx, int32_t mode, int32_t window);
+
+/* End-of-sequence id of dinfer_generate (README "Step 3": the decoder takes
+ * an eos_id): when a block completes and a sequence's block holds eos_id,
+ * every later position of that sequence is set to eos_id (unmasked; tokens
+ * already committed are kept), and the generation stops once no sequence has
+ * masked positions left -- the remaining blocks' refreshes and iterations are
+ * skipped on the device.  -1 (the default) disables it: every generated
+ * position is decoded.  Errors: DINFER_EINVAL for an id outside [0, vocab)
+ * or equal to mask_id. */
+dinfer_status dinfer_set_eos(dinfer_ctx* ctx, int32_t eos_id);
 
 /* Block boundary (cache refresh): full forward over ids[batch, seq_len]
  * (device, int32), storing every layer's K/V of all positions in the dual

@@ -366,7 +366,7 @@ def oracle_generation(m, prompt, G, B, tau, max_blocks=None, **kw):
     return x, recs
 
 
-def follow_gpu(D, dec, m, prompt, G, B, tau, tol_fn, dev, cache_mode="dual", window=0):
+def follow_gpu(D, dec, m, prompt, G, B, tau, tol_fn, dev, cache_mode="dual", window=0, eos_id=None):
     """Run the generation on the GPU step by step (dinfer_prefill_cache /
     dinfer_block_step) and check every decision against the oracle's at the
     GPU's own state (the oracle keeps a dual cache filled at the same states).
@@ -383,6 +383,8 @@ def follow_gpu(D, dec, m, prompt, G, B, tau, tol_fn, dev, cache_mode="dual", win
     # pass 1: the GPU trajectory, with the oracle's decision at each GPU state
     for blk in range(G // B):
         s0 = P + blk * B
+        if not mask.any():
+            break  # every sequence ended (end-of-sequence)
         cache = O.Cache(m.desc, b, L)
         it = 0
         while mask[:, s0:s0 + B].any():
@@ -399,6 +401,8 @@ def follow_gpu(D, dec, m, prompt, G, B, tau, tol_fn, dev, cache_mode="dual", win
             recs.append(rec)
             one = gpu_compare(D, dec, [rec], m, B, tau, dict(delta=1e3), dev)
             x, mask = one["last_ids"].astype(np.int64), one["last_mask"].astype(bool)
+        if eos_id is not None:
+            O.eos_stop(x, mask, s0, B, eos_id)
     # pass 2: the comparison with the tolerance of these iterations
     tol = tol_fn(recs)
     stats = gpu_compare(D, dec, recs, m, B, tau, tol, dev)
