@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // Split-K fixup: block = (tile, 16-column chunk), 128 threads = the tile's
-// output rows.  Sums the partial slots of the tile's contributors (the CTAs
+// output rows; the partial slots are token-major.  Sums the partial slots of the tile's contributors (the CTAs
 // of the GEMM grid whose unit ranges overlap it) in CTA order, then applies
 // the GEMM's epilogue.  Tiles owned whole by one CTA were finished by it.
 template <int BN>
@@ -669,27 +669,23 @@ __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
   float v[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = 0.f;
+  // token-major slots [BN tokens][128 rows]: for each token the 32 threads
+  // of a warp read 32 consecutive rows, one whole 128-byte line
 #pragma unroll 1
-  for (int x0 = 0; x0 < nc; x0 += 4) {
-    float4 buf[4][4];
+  for (int x0 = 0; x0 < nc; x0 += 2) {
+    float buf[2][16];
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
+    for (int x = 0; x < 2; ++x)
       if (x0 + x < nc) {
-        const float4* src = reinterpret_cast<const float4*>(a.ws + (size_t)slot_idx[x0 + x] * (BN * 128)) +
-                            (size_t)row * (BN / 4) + c * 4;
+        const float* src = a.ws + (size_t)slot_idx[x0 + x] * (BN * 128) + (size_t)(c * 16) * 128 + row;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) buf[x][i] = __ldcg(src + i);
+        for (int i = 0; i < 16; ++i) buf[x][i] = __ldcg(src + (size_t)i * 128);
       }
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
+    for (int x = 0; x < 2; ++x)
       if (x0 + x < nc)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[4 * i] += buf[x][i].x;
-          v[4 * i + 1] += buf[x][i].y;
-          v[4 * i + 2] += buf[x][i].z;
-          v[4 * i + 3] += buf[x][i].w;
-        }
+        for (int i = 0; i < 16; ++i) v[i] += buf[x][i];
   }
   const int nt = t / a.m_tiles, mt = t % a.m_tiles;
   epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg, a.M, 0);
