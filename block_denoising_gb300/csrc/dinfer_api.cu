@@ -238,8 +238,9 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
   a.grid = gs.grid;
   const long long units = (long long)a.m_tiles * a.n_tiles * (a.stream_k ? a.k_tiles : 1);
   if ((unsigned long long)units * (unsigned long long)a.grid >= (1ull << 32)) return cudaErrorInvalidValue;
-  a.slot_tok_major = 1;  // partial slots [tokens][rows]: coalesced for the fixup and the residual norms
   const int tiles = a.m_tiles * a.n_tiles;
+  // split tiles are finished by the fixup kernel; residual GEMMs leave them
+  // to the next residual norm
   const bool fixup = a.stream_k && !defer_resid;
   cudaError_t e = cudaSuccess;
   switch (BN) {
@@ -1675,7 +1676,6 @@ extern "C" dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* 
   a.grid = std::min(gs.grid, kNoAllocMaxCtas);
   if ((unsigned long long)a.n_tiles * (a.stream_k ? a.k_tiles : 1) * a.grid >= (1ull << 32))
     return fail(c, DINFER_EINVAL, "GEMM too large for the allocation-free entry point");
-  a.slot_tok_major = 1;
   a.ws = g_noalloc_ptr[dev];
   a.status = g_noalloc_state_ptr[dev];
   a.state = g_noalloc_state_ptr[dev];

@@ -57,9 +57,8 @@ struct GemmArgs {
   int row_off;             // added to the position (first recomputed position of a window)
   const DevState* state;
   // stream-K partial tiles
-  float* ws;               // [grid][2][BN * 128] fp32
+  float* ws;               // [grid][2][BN tokens][128 rows] fp32 (token-major)
   int grid;                // CTAs of the GEMM launch (fixes the unit ranges)
-  int slot_tok_major;      // partial slots [BN tokens][128 rows] (residual GEMMs), else [128 rows][BN]
   DevState* status;
   // grouped mode (mixture-of-experts): the tiles of `groups` independent
   // GEMMs that share the maps.  Group e owns rows [g_row_off[e], g_row_off[e+1])
@@ -367,7 +366,38 @@ struct Pipe {
   int* rec;  // producer stage records [2 * kStages] (shared memory, not thread-local)
 };
 
-// TMA producer loop (one elected thread of warp 0).
+// Sum, in CTA order, the token-major partials of split tile t that the
+// contributors of the stream-K schedule published, for this thread's output
+// row and the 16 tokens of chunk c.
+template <int BN>
+__device__ __forceinline__ void sum_split_partials(const GemmArgs& a, int t, int row, int c, float (&v)[16]) {
+  Sched sc;
+  sc.G = a.grid;
+  sc.KT = a.k_tiles;
+  sc.U = (unsigned)(a.m_tiles * a.n_tiles) * a.k_tiles;
+  const unsigned tu0 = (unsigned)t * a.k_tiles;
+  const int c_first = sc.owner(tu0), c_last = sc.owner(tu0 + a.k_tiles - 1);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll 1
+  for (int cc = c_first; cc <= c_last; cc += 2) {
+    float buf[2][16];
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (cc + x <= c_last) {
+        const int slot = (cc + x) * 2 + (((unsigned)t == sc.start(cc + x) / sc.KT) ? 0 : 1);
+        const float* src = a.ws + (size_t)slot * (BN * 128) + (size_t)(c * 16) * 128 + row;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) buf[x][i] = __ldcg(src + (size_t)i * 128);
+      }
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (cc + x <= c_last)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] += buf[x][i];
+  }
+}
+
 // TMA producer loop (one elected thread of warp 0).  The weight tiles of the
 // first pipeline stages do not depend on the preceding kernel, so they are
 // requested before griddepcontrol.wait; the activation tiles after it.
@@ -561,27 +591,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       if (!whole) {
         // partial tile: slot 0 holds this CTA's part of its first tile, slot 1
-        // of its last; layout [row][BN] so each thread moves whole float4s
+        // of its last; token-major [BN][128], so a warp stores whole lines
         const int which = (t == sl.tf) ? 0 : 1;
         float* base = a.ws + ((size_t)blockIdx.x * 2 + which) * (BN * 128);
-        if (a.slot_tok_major) {
 #pragma unroll 1
-          for (int c = 0; c < BN / 16; ++c) {
-            float v[16];
-            tmem_ld16(tbase + c * 16, v);
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+          tmem_ld16(tbase + c * 16, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) base[(size_t)(c * 16 + i) * 128 + row] = v[i];
-          }
-        } else {
-          float4* slot = reinterpret_cast<float4*>(base) + (size_t)row * (BN / 4);
-#pragma unroll 1
-          for (int c = 0; c < BN / 16; ++c) {
-            float v[16];
-            tmem_ld16(tbase + c * 16, v);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              slot[c * 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          }
+          for (int i = 0; i < 16; ++i) base[(size_t)(c * 16 + i) * 128 + row] = v[i];
         }
         tc_fence_before();
         mbar_arrive(&p.tempty[acc]);
@@ -644,7 +662,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int BN>
 __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
   __shared__ float xchg[128 * 17];
-  __shared__ int slot_idx[32];
   pdl_wait();
   const int chunks = BN / 16;
   const int t = blockIdx.x / chunks, c = blockIdx.x % chunks;
@@ -659,34 +676,11 @@ __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
     pdl_trigger();
     return;
   }
-  const int nc = c_last - c_first + 1;
-  const int row = threadIdx.x;
-  if (row < nc && row < 32) {
-    const int cc = c_first + row;
-    slot_idx[row] = cc * 2 + ((t == (int)(sc.start(cc) / a.k_tiles)) ? 0 : 1);
-  }
-  __syncthreads();
-  float v[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = 0.f;
   // token-major slots [BN tokens][128 rows]: for each token the 32 threads
   // of a warp read 32 consecutive rows, one whole 128-byte line
-#pragma unroll 1
-  for (int x0 = 0; x0 < nc; x0 += 2) {
-    float buf[2][16];
-#pragma unroll
-    for (int x = 0; x < 2; ++x)
-      if (x0 + x < nc) {
-        const float* src = a.ws + (size_t)slot_idx[x0 + x] * (BN * 128) + (size_t)(c * 16) * 128 + row;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) buf[x][i] = __ldcg(src + (size_t)i * 128);
-      }
-#pragma unroll
-    for (int x = 0; x < 2; ++x)
-      if (x0 + x < nc)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] += buf[x][i];
-  }
+  const int row = threadIdx.x;
+  float v[16];
+  sum_split_partials<BN>(a, t, row, c, v);
   const int nt = t / a.m_tiles, mt = t % a.m_tiles;
   epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg, a.M, 0);
   pdl_trigger();
