@@ -499,7 +499,7 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
 # on a GB300, taken with the current gemm_tc_kernel (a change to that kernel
 # removes the entry until it is captured again).
 NCU_DRAM_BYTES = {
-    (1536, 24576, 4096): (213997824, 115565568),
+    (1536, 24576, 4096): (214055936, 115359488),
 }
 
 
@@ -512,10 +512,11 @@ def run_profile(args):
     cfg, run, _ = inputs.WORKLOADS[args.workload]
     b, P, G, B = run.batch, run.prompt_len, run.gen_length, run.block_length
     L = P + G
-    if args.profile in ("lmhead", "attention"):
-        # one kernel of the workload's cached iteration through the op API
+    if args.profile in ("lmhead", "attention", "attention_refresh"):
+        # one kernel of the workload's cached iteration (or, attention_refresh,
+        # of its refresh: every position a query row) through the op API
         ws = dinfer.OpWorkspace()
-        rows = b * B
+        rows = b * B if args.profile != "attention_refresh" else b * L
         if args.profile == "lmhead":
             X = inputs.normal_tensor(5, (rows, cfg.d_model), 1.0, 3, device="cuda")
             Wl = inputs.normal_tensor(6, (cfg.vocab, cfg.d_model), 0.02, 3, device="cuda")
@@ -525,7 +526,7 @@ def run_profile(args):
             q = inputs.normal_tensor(7, (rows, d), 1.0, 5, device="cuda")
             k = inputs.normal_tensor(8, (b, L, d), 1.0, 5, device="cuda")
             v = inputs.normal_tensor(9, (b, L, d), 1.0, 5, device="cuda")
-            call = lambda: dinfer.op_attention_bf16(q, k, v, B, ws)
+            call = lambda: dinfer.op_attention_bf16(q, k, v, rows // b, ws)
         for _ in range(3):
             call()
         torch.cuda.synchronize()
@@ -577,7 +578,8 @@ def main():
     ap.add_argument("--clock-log", default=None,
                     help="CSV of the nvidia-smi clock samples taken during the timed region "
                          "('{rank}' is replaced by the rank; default: the temp directory)")
-    ap.add_argument("--profile", choices=["iteration", "refresh", "gemm", "lmhead", "attention"], default=None)
+    ap.add_argument("--profile", choices=["iteration", "refresh", "gemm", "lmhead", "attention", "attention_refresh"],
+                    default=None)
     ap.add_argument("--gemm", type=int, nargs=3, default=[64, 24576, 4096], metavar=("M", "N", "K"))
     args = ap.parse_args()
     if args.profile:
