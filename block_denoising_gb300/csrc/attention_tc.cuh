@@ -409,10 +409,12 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
       } else {
         // partial (unnormalised O, m, l) in this CTA's shared memory, over the
         // K ring and the P buffers, merged below
+        // float4 column i of row r at (i ^ r) mod 32: the 32 rows a warp
+        // stores at once fall in different banks
         float4* po = reinterpret_cast<float4*>(sm + kAtcOffK) + r * 32;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          po[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+          po[i ^ (r & 31)] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
                               __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
         float* pml = reinterpret_cast<float*>(sm + kAtcOffP) + r * 2;
         pml[0] = m_used;
@@ -463,26 +465,44 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
         for (int sp = 0; sp < kAtcMaxSplits; ++sp) coef[t * kAtcMaxSplits + sp] = mv[sp] * inv;
       }
       named_bar_sync(1, 128);
-      for (int idx = t; idx < nr * 32; idx += 128) {
-        const int row = idx >> 5, c4 = (idx & 31) * 4;
-        const int rr = ra + row;
-        float4 o[kAtcMaxSplits];
+      // two items per thread per round: every remote load of the round is
+      // issued before any of its values is used (a store in between would
+      // order the next item's loads behind it)
+      const int n_items = nr * 32;
+      for (int base = t; base < n_items; base += 2 * 128) {
+        float4 o[2][kAtcMaxSplits];
 #pragma unroll
-        for (int sp = 0; sp < kAtcMaxSplits; ++sp)
-          if (sp < a.splits) o[sp] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(po, sp) + rr * 128 + c4);
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        for (int u = 0; u < 2; ++u) {
+          const int idx = base + u * 128;
+          if (idx < n_items) {
+            const int rr = ra + (idx >> 5), c4 = (idx & 31) * 4;
 #pragma unroll
-        for (int sp = 0; sp < kAtcMaxSplits; ++sp) {
-          if (sp < a.splits) {
-            const float w = coef[row * kAtcMaxSplits + sp];
-            acc0 = fmaf(w, o[sp].x, acc0);
-            acc1 = fmaf(w, o[sp].y, acc1);
-            acc2 = fmaf(w, o[sp].z, acc2);
-            acc3 = fmaf(w, o[sp].w, acc3);
+            for (int sp = 0; sp < kAtcMaxSplits; ++sp)
+              if (sp < a.splits)
+                o[u][sp] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(po, sp) + rr * 128 +
+                                                             (c4 ^ ((rr & 31) * 4)));
           }
         }
-        __nv_bfloat16* og = a.o + ((size_t)bi * a.rows_per_seq + row0 + rr) * a.d + hc + c4;
-        *reinterpret_cast<uint2*>(og) = make_uint2(pack_bf16x2(acc0, acc1), pack_bf16x2(acc2, acc3));
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int idx = base + u * 128;
+          if (idx < n_items) {
+            const int row = idx >> 5, c4 = (idx & 31) * 4;
+            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+            for (int sp = 0; sp < kAtcMaxSplits; ++sp) {
+              if (sp < a.splits) {
+                const float w = coef[row * kAtcMaxSplits + sp];
+                acc0 = fmaf(w, o[u][sp].x, acc0);
+                acc1 = fmaf(w, o[u][sp].y, acc1);
+                acc2 = fmaf(w, o[u][sp].z, acc2);
+                acc3 = fmaf(w, o[u][sp].w, acc3);
+              }
+            }
+            __nv_bfloat16* og = a.o + ((size_t)bi * a.rows_per_seq + row0 + ra + row) * a.d + hc + c4;
+            *reinterpret_cast<uint2*>(og) = make_uint2(pack_bf16x2(acc0, acc1), pack_bf16x2(acc2, acc3));
+          }
+        }
       }
     }
     cluster.sync();  // keep this CTA's shared memory alive until every peer has read it
