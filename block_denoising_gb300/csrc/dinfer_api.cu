@@ -1174,12 +1174,14 @@ dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* we
   AL(c->kc, c->cache_layer_elems() * desc->n_layers * es);
   AL(c->vc, c->cache_layer_elems() * desc->n_layers * es);
   const int half = desc->head_dim / 2;
-  AL(c->rope_cos, (size_t)desc->max_seq * half * 4);
-  AL(c->rope_sin, (size_t)desc->max_seq * half * 4);
+  // at least two positions: the GEMM epilogue steps RoPE by position 1's angle
+  const int rope_pos = desc->max_seq < 2 ? 2 : desc->max_seq;
+  AL(c->rope_cos, (size_t)rope_pos * half * 4);
+  AL(c->rope_sin, (size_t)rope_pos * half * 4);
   {
     // rotary table in double precision: angle = pos * theta^(-2i/hd)
-    std::vector<float> cs((size_t)desc->max_seq * half), sn((size_t)desc->max_seq * half);
-    for (int p = 0; p < desc->max_seq; ++p)
+    std::vector<float> cs((size_t)rope_pos * half), sn((size_t)rope_pos * half);
+    for (int p = 0; p < rope_pos; ++p)
       for (int i = 0; i < half; ++i) {
         const double inv = std::pow((double)desc->rope_theta, -2.0 * i / desc->head_dim);
         const double ang = (double)p * inv;

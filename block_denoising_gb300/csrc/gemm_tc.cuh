@@ -127,9 +127,13 @@ struct GemmCfg {
   static constexpr int kStageB = BN * 64 * 2;
   static constexpr int kStage = kStageA + kStageB;
   static constexpr int kStages = ST;
-  static constexpr int kXchgFloats = 128 * 17;
+  // epilogue row-pair exchange: two buffers used in turn where they fit
+  // beside the stages (227 KB per CTA), else one
+  static constexpr int kXchgBufs = (1024 + kStages * kStage + 2 * 128 * 17 * 4 + 512 <= 232448) ? 2 : 1;
+  static constexpr int kXchgFloats = kXchgBufs * 128 * 17;
   static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStage + kXchgFloats * 4 + 512;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  static_assert(kSmem <= 232448, "GEMM shared memory above 227 KB");
 };
 
 // ---------------------------------------------------------------------------
@@ -194,11 +198,15 @@ __device__ __forceinline__ void qkv_rope_fetch(const GemmArgs& a, int base_pos, 
 }
 
 // Epilogue of 16 tokens (m0..m0+15) of output row `row` of tile nt.  QKV
-// tiles take their RoPE factors from `rope` (cos then sin, fetched ahead by
-// the caller) or, when it is NULL, load them here.
+// tiles take their RoPE factors from `rope` (cos then sin, made by the
+// caller) or, when it is NULL, load them here.  `xchg` (128 x 17 floats)
+// pairs rows through shared memory.  A caller that finishes several chunks
+// either alternates two buffers, so that a chunk's writes never meet the
+// previous chunk's reads, or reuses one and asks for a barrier after the
+// reads (`sync_after`).
 template <int BN>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16], int row, int nt, int m0,
-                                               float* xchg, int m_lim, int out_base,
+                                               float* xchg, int m_lim, int out_base, bool sync_after,
                                                const float (*rope)[16] = nullptr, int base_pos_in = -1) {
   if (a.q_out != nullptr) {
     // ---- QKV: RoPE pairs (i, i + 64) sit in rows row and row ^ 64 ----
@@ -226,7 +234,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
     const float sgn = row < 64 ? -1.f : 1.f;
 #pragma unroll
     for (int c = 0; c < 16; ++c) o[c] = (which == 2) ? v[c] : fmaf(sgn * part[c], sn[c], v[c] * cs[c]);
-    named_bar_sync(1, 128);
+    if (sync_after) named_bar_sync(1, 128);
     __nv_bfloat16* __restrict__ dst = (which == 0 ? a.q_out : (which == 1 ? a.k_cache : a.v_cache)) + nn;
     int bi = m0 / a.rows_per_seq;
     int r = m0 - bi * a.rows_per_seq;
@@ -244,26 +252,28 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
     }
   } else if (a.a_mode == A_PAIR) {
     // ---- SwiGLU: gate row r (< 64) pairs with up row r + 64 ----
+    // the pair splits the 16 tokens: the gate row finishes tokens 0..7 and
+    // hands its values of tokens 8..15 to the up row, which finishes those
+    const bool gate_row = row < 64;
     float* mine = xchg + row * 17;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) mine[i] = v[i];
+    for (int i = 0; i < 8; ++i) mine[i] = gate_row ? v[8 + i] : v[i];
     named_bar_sync(1, 128);
-    float o[16];
-    const bool act_row = row < 64;
-    if (act_row) {
-      const float* up = xchg + (row + 64) * 17;
+    const float* part = xchg + (row ^ 64) * 17;
+    float o[8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float g = v[c];
-        o[c] = __fdividef(g, 1.0f + __expf(-g)) * up[c];  // rounded to bf16 next
-      }
+    for (int i = 0; i < 8; ++i) {
+      const float g = gate_row ? v[i] : part[i];
+      const float u = gate_row ? part[i] : v[8 + i];
+      o[i] = __fdividef(g, 1.0f + __expf(-g)) * u;  // rounded to bf16 next
     }
-    named_bar_sync(1, 128);
-    const int jf = nt * 64 + row;
-    if (act_row && jf < a.N) {
+    if (sync_after) named_bar_sync(1, 128);
+    const int jf = nt * 64 + (row & 63);
+    const int mh = m0 + (gate_row ? 0 : 8);
+    if (jf < a.N) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        if (m0 + c < m_lim) a.out_bf16[(size_t)(out_base + m0 + c) * a.ldo + jf] = __float2bfloat16_rn(o[c]);
+      for (int i = 0; i < 8; ++i)
+        if (mh + i < m_lim) a.out_bf16[(size_t)(out_base + mh + i) * a.ldo + jf] = __float2bfloat16_rn(o[i]);
     }
   } else {
     const int n = nt * 128 + row;
@@ -572,7 +582,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         a.q_out != nullptr ? (a.pos_from_state ? a.state->block_start : 0) + a.row_off : 0;
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;          // output feature row inside the tile
-    float rope[2][16];  // QKV: RoPE factors of the next chunk to finish
+    // QKV: RoPE factors of this row's frequency.  A whole tile loads those of
+    // its first token (and of the sequence start, where a tile wraps into
+    // the next sequence) ahead of its main loop; the following tokens step
+    // by one rotation of the frequency's angle (<= BN steps: an error of a
+    // few fp32 ulps, far below the bf16 rounding of q and k).
+    float rc = 1.f, rs = 0.f, rc0 = 1.f, rs0 = 0.f, step_c = 1.f, step_s = 0.f;
+    if (a.q_out != nullptr) {
+      step_c = __ldg(a.rope_cos + 64 + (row & 63));
+      step_s = __ldg(a.rope_sin + 64 + (row & 63));
+    }
+    int xb = 0;  // exchange buffer of the next pairing chunk
     for (int j = 0; j < sl.nseg; ++j) {
       int t, kb, ke;
       sl.seg(j, t, kb, ke);
@@ -584,7 +604,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       float hcur[16];  // residual: h of the chunk being finished
       // loads of the tile's first RoPE factors or residual values overlap its
       // main loop (a whole tile's h is written by this thread only)
-      if (a.q_out != nullptr && whole) qkv_rope_fetch(a, base_pos, row, tr.nt, tr.mt * BN, rope[0], rope[1]);
+      int rr = 0;  // QKV: offset of the chunk's first token in its sequence
+      if (a.q_out != nullptr && whole) {
+        rr = (tr.mt * BN) % a.rows_per_seq;
+        rc = __ldg(a.rope_cos + (base_pos + rr) * 64 + (row & 63));
+        rs = __ldg(a.rope_sin + (base_pos + rr) * 64 + (row & 63));
+        rc0 = __ldg(a.rope_cos + base_pos * 64 + (row & 63));
+        rs0 = __ldg(a.rope_sin + base_pos * 64 + (row & 63));
+      }
       if (a.resid != nullptr && whole) resid_load16(a, n, tr.mt * BN, hcur);
       if (!mbar_wait(&p.tfull[acc], use & 1, p.abort_flag)) break;
       tc_fence_after();
@@ -606,19 +633,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         continue;
       }
       if (a.q_out != nullptr) {
-        // QKV: the RoPE factors of chunk c + 1 load while chunk c is finished
-        float next[2][16];
 #pragma unroll 1
         for (int c = 0; c < BN / 16; ++c) {
           float v[16];
           tmem_ld16(tbase + c * 16, v);
-          if (c + 1 < BN / 16) qkv_rope_fetch(a, base_pos, row, tr.nt, tr.mt * BN + (c + 1) * 16, next[0], next[1]);
-          epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg, tr.m_lim, tr.out_base, rope, base_pos);
+          float rope[2][16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            rope[0][i] = next[0][i];
-            rope[1][i] = next[1][i];
+            rope[0][i] = rc;
+            rope[1][i] = rs;
+            if (++rr == a.rows_per_seq) {
+              rr = 0;
+              rc = rc0;
+              rs = rs0;
+            } else {
+              const float t = fmaf(rc, step_c, -rs * step_s);
+              rs = fmaf(rs, step_c, rc * step_s);
+              rc = t;
+            }
           }
+          epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg + xb * (128 * 17), tr.m_lim, tr.out_base,
+                             C::kXchgBufs == 1, rope, base_pos);
+          xb ^= C::kXchgBufs - 1;
         }
       } else if (a.resid != nullptr) {
         // residual: h of chunk c + 1 loads while chunk c is finished
@@ -639,7 +675,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int c = 0; c < BN / 16; ++c) {
           float v[16];
           tmem_ld16(tbase + c * 16, v);
-          epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg, tr.m_lim, tr.out_base);
+          epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg + xb * (128 * 17), tr.m_lim, tr.out_base,
+                             C::kXchgBufs == 1);
+          xb ^= C::kXchgBufs - 1;
         }
       }
       tc_fence_before();
@@ -682,7 +720,7 @@ __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
   float v[16];
   sum_split_partials<BN>(a, t, row, c, v);
   const int nt = t / a.m_tiles, mt = t % a.m_tiles;
-  epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg, a.M, 0);
+  epilogue_chunk<BN>(a, v, row, nt, mt * BN + c * 16, xchg, a.M, 0, false);
   pdl_trigger();
 }
 

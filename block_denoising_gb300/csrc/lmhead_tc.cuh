@@ -29,6 +29,7 @@ struct LmCfg {
   // states take the room
   static constexpr int kStages = BN == 64 ? 8 : gemm_default_stages<BN>();
   static constexpr int kSmem = GemmCfg<BN, kStages>::kSmem + kMaxM * 12 + 4 * 16 * 12 + 128;
+  static_assert(kSmem <= 232448, "LM-head shared memory above 227 KB");
 };
 
 template <int BN>
