@@ -6,18 +6,26 @@
 // suffix) with no mask: o = softmax(q k^T / sqrt(128)) v.
 //
 // One CTA = 128 query rows x one head x one range of 128-key chunks,
-// 192 threads:
-//   warp 0     TMA: Q once, then K and V chunks (2-stage ring, 3-D tensor maps
-//              so that keys past L and rows past the sequence read as zeros);
+// 320 threads:
+//   warp 0     TMA: Q once, then K and V chunks (2-stage rings with their own
+//              barriers: a K stage is refilled as soon as S of its chunk has
+//              been computed, a V stage once P V of its chunk has; 3-D tensor
+//              maps so that keys past L and rows past the sequence read as
+//              zeros);
 //   warp 1     TMEM allocation and the single-thread MMA issue:
 //              S_j = Q K_j^T into one of two TMEM buffers, then O += P_{j-1} V_{j-1}
 //              (V is the MN-major operand, P comes from shared memory);
-//   warps 2-5  one thread per query row: tcgen05.ld of the row of S, online
-//              softmax in the log2 domain, P = bf16(2^(s - m)) written to one of
+//   warps 2-9  softmax, two threads per query row: warp w reads TMEM lane
+//              quadrant w % 4 and takes key half (w - 2) / 4 (64 of the
+//              chunk's 128 keys; the two warps of a quadrant share the SM
+//              sub-partition and agree on the row max through shared memory):
+//              tcgen05.ld of its half row of S, online softmax in the log2
+//              domain, P = bf16(2^(s - m)) written to its 64-key slab of one of
 //              two shared-memory buffers in the 128-byte-swizzled K-major
 //              layout (so the softmax of chunk j overlaps P_{j-1} V_{j-1}),
-//              final O / l.  Warps whose 32 rows all lie past the sequence's
-//              rows (a 64-row block) only keep the barrier counts.
+//              final O / l for its 64 output columns.  Warps whose 32 rows all
+//              lie past the sequence's rows (a 64-row block) only keep the
+//              barrier counts.
 // The running max used for the exponent is raised only when a chunk's max
 // exceeds it by more than 8 (P stays <= 2^8); then O (in TMEM) and l are
 // rescaled once.  O / l is exact whatever max was used.
@@ -45,18 +53,21 @@ struct AttnTcArgs {
 };
 
 constexpr int kHd = 128;                // head dimension of the bf16 path
-constexpr int kAtcThreads = 192;
+constexpr int kAtcThreads = 320;
+constexpr int kAtcSoftmax = 256;        // softmax threads: 128 rows x 2 key halves
 constexpr int kAtcKeys = 128;           // keys per chunk
 constexpr int kAtcTile = 128 * 128 * 2; // one 128 x 128 bf16 operand (two 64-column swizzle slabs)
 constexpr int kAtcSlab = 128 * 128;     // bytes of one 64-column slab of 128 rows
 constexpr int kAtcStages = 2;
 constexpr int kAtcMaxSplits = 8;
-// Q | K[stages] | V[stages] | P[2] | barriers
+// Q | K[stages] | V[stages] | P[2] | barriers | row exchange [2 halves][128]
 constexpr int kAtcOffK = kAtcTile;
 constexpr int kAtcOffV = kAtcOffK + kAtcStages * kAtcTile;
 constexpr int kAtcOffP = kAtcOffV + kAtcStages * kAtcTile;
 constexpr int kAtcOffBar = kAtcOffP + 2 * kAtcTile;
-constexpr int kAtcSmem = 1024 + kAtcOffBar + 256;
+constexpr int kAtcOffX = kAtcOffBar + 256;
+constexpr int kAtcSmem = 1024 + kAtcOffX + 2 * 128 * 4;
+static_assert(kAtcSmem <= 232448, "attention shared memory above 227 KB");
 constexpr int kAtcTmemCols = 512;       // S0 | S1 | O | unused
 constexpr float kAtcLazy = 8.0f;        // log2 growth of the max tolerated before rescaling O
 
@@ -125,6 +136,14 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
   asm volatile("" : ATC_I32(x, 96));
 }
 
+// 64 consecutive TMEM columns of this warp's 32 lanes, one wait for both loads
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&x)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 0) : "r"(taddr));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 32) : "r"(taddr + 32));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : ATC_I32(x, 0)::"memory");
+  asm volatile("" : ATC_I32(x, 32));
+}
+
 // 2^x with the PTX approximate base-2 exponential (2^-inf = +0)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -143,9 +162,11 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kAtcOffBar);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;                 // [2]
-  uint64_t* kv_empty = kv_full + kAtcStages;    // [2]
-  uint64_t* s_full = kv_empty + kAtcStages;     // [2]
+  uint64_t* k_full = bars + 1;                  // [2]
+  uint64_t* k_empty = k_full + kAtcStages;      // [2]
+  uint64_t* v_full = k_empty + kAtcStages;      // [2]
+  uint64_t* v_empty = v_full + kAtcStages;      // [2]
+  uint64_t* s_full = v_empty + kAtcStages;      // [2]
   uint64_t* s_empty = s_full + 2;               // [2]
   uint64_t* p_full = s_empty + 2;               // [2]
   uint64_t* pv_done = p_full + 2;               // [2]
@@ -167,13 +188,15 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < kAtcStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 128);
-      mbar_init(&p_full[s], 128);
+      mbar_init(&s_empty[s], kAtcSoftmax);
+      mbar_init(&p_full[s], kAtcSoftmax);
       mbar_init(&pv_done[s], 1);
     }
     mbar_init(drain, 1);
@@ -217,24 +240,48 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
       mbar_arrive_expect_tx(q_full, kAtcTile);
       tma_load_3d(sm, &maps.q, q_full, hc, row0, bi);
       tma_load_3d(sm + kAtcSlab, &maps.q, q_full, hc + 64, row0, bi);
-      int issued = 0;
-      for (int j = 0; j < nck && !*abort_flag; ++j) {
+      int k_issued = 0, v_issued = 0;
+      // K of chunk j into stage j % 2 once S of chunk j - 2 completed
+      auto load_k = [&](int j) -> bool {
         const int st = j % kAtcStages;
-        if (!mbar_wait_diag(&kv_empty[st], ((j / kAtcStages) & 1) ^ 1, abort_flag, a.status, kDiagAttn, 1, j)) break;
-        issued = j + 1;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kAtcTile);
-        const int key0 = (c_begin + j) * kAtcKeys;
+        if (!mbar_wait_diag(&k_empty[st], ((j / kAtcStages) & 1) ^ 1, abort_flag, a.status, kDiagAttn, 1, j))
+          return false;
+        k_issued = j + 1;
+        mbar_arrive_expect_tx(&k_full[st], kAtcTile);
         uint8_t* kb = sm + kAtcOffK + st * kAtcTile;
+        const int key0 = (c_begin + j) * kAtcKeys;
+        tma_load_3d(kb, &maps.k, &k_full[st], hc, key0, bi);
+        tma_load_3d(kb + kAtcSlab, &maps.k, &k_full[st], hc + 64, key0, bi);
+        return true;
+      };
+      // V of chunk j into stage j % 2 once P V of chunk j - 2 completed
+      auto load_v = [&](int j) -> bool {
+        const int st = j % kAtcStages;
+        if (!mbar_wait_diag(&v_empty[st], ((j / kAtcStages) & 1) ^ 1, abort_flag, a.status, kDiagAttn, 10, j))
+          return false;
+        v_issued = j + 1;
+        mbar_arrive_expect_tx(&v_full[st], kAtcTile);
         uint8_t* vb = sm + kAtcOffV + st * kAtcTile;
-        tma_load_3d(kb, &maps.k, &kv_full[st], hc, key0, bi);
-        tma_load_3d(kb + kAtcSlab, &maps.k, &kv_full[st], hc + 64, key0, bi);
-        tma_load_3d(vb, &maps.v, &kv_full[st], hc, key0, bi);
-        tma_load_3d(vb + kAtcSlab, &maps.v, &kv_full[st], hc + 64, key0, bi);
+        const int key0 = (c_begin + j) * kAtcKeys;
+        tma_load_3d(vb, &maps.v, &v_full[st], hc, key0, bi);
+        tma_load_3d(vb + kAtcSlab, &maps.v, &v_full[st], hc + 64, key0, bi);
+        return true;
+      };
+      // K runs two chunks ahead of V: K_{j+2} waits for S_j, which the
+      // tensor pipe finishes before P_{j-1} V_{j-1}, so queuing it behind
+      // V_j costs nothing
+      bool go = true;
+      for (int j = 0; j < min(nck, kAtcStages) && go; ++j) go = load_k(j);
+      for (int j = 0; j < nck && go && !*abort_flag; ++j) {
+        go = load_v(j);
+        if (go && j + kAtcStages < nck) go = load_k(j + kAtcStages);
       }
       if (*abort_flag) {  // let the copies in flight land before the CTA exits
         mbar_wait_drain(q_full, 0);
-        for (int j = max(0, issued - kAtcStages); j < issued; ++j)
-          mbar_wait_drain(&kv_full[j % kAtcStages], (j / kAtcStages) & 1);
+        for (int j = max(0, k_issued - kAtcStages); j < k_issued; ++j)
+          mbar_wait_drain(&k_full[j % kAtcStages], (j / kAtcStages) & 1);
+        for (int j = max(0, v_issued - kAtcStages); j < v_issued; ++j)
+          mbar_wait_drain(&v_full[j % kAtcStages], (j / kAtcStages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -247,6 +294,7 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
       auto issue_pv = [&](int i) -> bool {
         const int st = i % kAtcStages, pb = i & 1;
         if (!mbar_wait_diag(&p_full[pb], (i >> 1) & 1, abort_flag, a.status, kDiagAttn, 2, i)) return false;
+        if (!mbar_wait_diag(&v_full[st], (i / kAtcStages) & 1, abort_flag, a.status, kDiagAttn, 11, i)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sm + kAtcOffV + st * kAtcTile);
         const uint32_t pa = p_addr + pb * kAtcTile;
@@ -256,14 +304,14 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
           const uint64_t bd = make_sw128_desc_mn(v_addr + kk * 2048, kAtcSlab);
           tc_mma_bf16(t_o, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&kv_empty[st]);
+        tc_commit(&v_empty[st]);
         tc_commit(&pv_done[pb]);
         return true;
       };
       bool ok = mbar_wait_diag(q_full, 0, abort_flag, a.status, kDiagAttn, 3, 0);
       for (int j = 0; j < nck && ok; ++j) {
         const int st = j % kAtcStages, sb = j & 1;
-        if (!mbar_wait_diag(&kv_full[st], (j / kAtcStages) & 1, abort_flag, a.status, kDiagAttn, 4, j)) { ok = false; break; }
+        if (!mbar_wait_diag(&k_full[st], (j / kAtcStages) & 1, abort_flag, a.status, kDiagAttn, 4, j)) { ok = false; break; }
         if (!mbar_wait_diag(&s_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag, a.status, kDiagAttn, 5, j)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm + kAtcOffK + st * kAtcTile);
@@ -274,6 +322,7 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
           tc_mma_bf16((tmem + sb * 128), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[sb]);
+        tc_commit(&k_empty[st]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok && nck > 0) issue_pv(nck - 1);
@@ -282,66 +331,82 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
     }
   } else {
     // ------------------------------ softmax / output ------------------------------
-    // Every wait's outcome is made warp-uniform: the TMEM accesses are warp-collective.
+    // Every wait's outcome is made warp-uniform: the TMEM accesses are
+    // warp-collective.  The two warps of a quadrant meet at the same number
+    // of pair barriers whatever their waits returned (a failed wait only
+    // skips work), so that a timed-out wait never leaves the partner blocked.
     const int q = warp & 3;
+    const int hk = (warp - 2) >> 2;         // key half: keys 64 hk .. 64 hk + 63 of a chunk
     const int r = q * 32 + lane;            // query row inside the tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const bool live = q * 32 < q_valid;     // warp-uniform
+    const bool live = q * 32 < q_valid;     // warp-uniform, the same for both halves
+    const int pair_bar = 2 + q;             // named barrier of the quadrant's two warps
+    float* xrow = reinterpret_cast<float*>(sm + kAtcOffX);  // [2 halves][128 rows]
     const float sc = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nck; ++j) {
       const int sb = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_diag(&s_full[sb], (j >> 1) & 1, abort_flag, a.status, kDiagAttn, 6, j))) {
+      if (ok && !__all_sync(0xffffffffu, mbar_wait_diag(&s_full[sb], (j >> 1) & 1, abort_flag, a.status,
+                                                        kDiagAttn, 6, j)))
         ok = false;
-        break;
-      }
       if (!live) {  // rows past the sequence: keep the counts only
         mbar_arrive(&s_empty[sb]);
         mbar_arrive(&p_full[sb]);
         continue;
       }
-      tc_fence_after();
-      uint32_t sv[128];
-      tmem_ld128((tmem + sb * 128) + lane_off, sv);
-      tc_fence_before();
-      mbar_arrive(&s_empty[sb]);
-      const int nvalid = a.L - (c_begin + j) * kAtcKeys;  // >= 1
-      if (nvalid < kAtcKeys) {
+      uint32_t sv[64];
+      float mh = -INFINITY;
+      if (ok) {
+        tc_fence_after();
+        tmem_ld64((tmem + sb * 128 + hk * 64) + lane_off, sv);
+        tc_fence_before();
+        mbar_arrive(&s_empty[sb]);
+        const int nvalid = a.L - (c_begin + j) * kAtcKeys - hk * 64;  // may be <= 0 in the upper half
+        if (nvalid < 64) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= nvalid) sv[i] = 0xff800000u;  // -inf: no key
-      }
-      float mx0 = __uint_as_float(sv[0]), mx1 = __uint_as_float(sv[1]);
-      float mx2 = __uint_as_float(sv[2]), mx3 = __uint_as_float(sv[3]);
+          for (int i = 0; i < 64; ++i)
+            if (i >= nvalid) sv[i] = 0xff800000u;  // -inf: no key
+        }
+        float mx0 = __uint_as_float(sv[0]), mx1 = __uint_as_float(sv[1]);
+        float mx2 = __uint_as_float(sv[2]), mx3 = __uint_as_float(sv[3]);
 #pragma unroll
-      for (int i = 4; i < 128; i += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sv[i]));
-        mx1 = fmaxf(mx1, __uint_as_float(sv[i + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sv[i + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sv[i + 3]));
+        for (int i = 4; i < 64; i += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sv[i]));
+          mx1 = fmaxf(mx1, __uint_as_float(sv[i + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sv[i + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sv[i + 3]));
+        }
+        mh = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;
       }
-      const float mj = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;
+      // the chunk's row max over both halves (the lower half holds key 0 of
+      // the chunk, a valid key, so mj is finite)
+      named_bar_sync(pair_bar, 64);  // the partner has read the previous chunk's value
+      xrow[hk * 128 + r] = mh;
+      named_bar_sync(pair_bar, 64);
+      const float mj = fmaxf(mh, xrow[(hk ^ 1) * 128 + r]);
+      if (!ok) continue;
       if (j == 0) {
         m_used = mj;
       } else {
         const bool grow = mj > m_used + kAtcLazy;
         if (__any_sync(0xffffffffu, grow)) {
-          // rescale O: it must hold every product issued so far (P_{j-1} V_{j-1})
+          // rescale this half's columns of O: O must hold every product
+          // issued so far (P_{j-1} V_{j-1})
           if (!__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag,
                                                       a.status, kDiagAttn, 7, j))) {
             ok = false;
-            break;
+            continue;
           }
           tc_fence_after();
           const float alpha = grow ? ex2_approx(m_used - mj) : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             float o16[16];
-            tmem_ld16(t_o + lane_off + c * 16, o16);
+            tmem_ld16(t_o + lane_off + hk * 64 + c * 16, o16);
 #pragma unroll
             for (int i = 0; i < 16; ++i) o16[i] *= alpha;
-            tmem_st16(t_o + lane_off + c * 16, o16);
+            tmem_st16(t_o + lane_off + hk * 64 + c * 16, o16);
           }
           tc_fence_before();
           l *= alpha;
@@ -352,30 +417,27 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
       if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[sb], ((j >> 1) & 1) ^ 1, abort_flag, a.status,
                                                              kDiagAttn, 8, j))) {
         ok = false;
-        break;
+        continue;
       }
       const float nm = -m_used;
-      uint8_t* prow = sm + kAtcOffP + sb * kAtcTile + r * 128;
+      uint8_t* prow = sm + kAtcOffP + sb * kAtcTile + hk * kAtcSlab + r * 128;
       float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
-      for (int kc = 0; kc < 2; ++kc) {
+      for (int u = 0; u < 8; ++u) {
+        const int i = u * 8;
+        float p[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = kc * 64 + u * 8;
-          float p[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) p[e] = ex2_approx(fmaf(__uint_as_float(sv[i + e]), sc, nm));
-          const uint4 w = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-                                     pack_bf16x2(p[6], p[7]));
-          // l sums the bf16 values the tensor cores multiply, so that O / l
-          // weights the keys exactly in proportion (one dominant key keeps
-          // weight 1 whatever its rounding)
-          rs0 += __uint_as_float(w.x << 16) + __uint_as_float(w.x & 0xffff0000u);
-          rs1 += __uint_as_float(w.y << 16) + __uint_as_float(w.y & 0xffff0000u);
-          rs2 += __uint_as_float(w.z << 16) + __uint_as_float(w.z & 0xffff0000u);
-          rs3 += __uint_as_float(w.w << 16) + __uint_as_float(w.w & 0xffff0000u);
-          *reinterpret_cast<uint4*>(prow + kc * kAtcSlab + ((u ^ (r & 7)) << 4)) = w;
-        }
+        for (int e = 0; e < 8; ++e) p[e] = ex2_approx(fmaf(__uint_as_float(sv[i + e]), sc, nm));
+        const uint4 w = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                                   pack_bf16x2(p[6], p[7]));
+        // l sums the bf16 values the tensor cores multiply, so that O / l
+        // weights the keys exactly in proportion (one dominant key keeps
+        // weight 1 whatever its rounding)
+        rs0 += __uint_as_float(w.x << 16) + __uint_as_float(w.x & 0xffff0000u);
+        rs1 += __uint_as_float(w.y << 16) + __uint_as_float(w.y & 0xffff0000u);
+        rs2 += __uint_as_float(w.z << 16) + __uint_as_float(w.z & 0xffff0000u);
+        rs3 += __uint_as_float(w.w << 16) + __uint_as_float(w.w & 0xffff0000u);
+        *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) = w;
       }
       l += (rs0 + rs1) + (rs2 + rs3);
       fence_async_shared();  // the P rows become visible to the tensor cores
@@ -387,18 +449,29 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
           !__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[(nck - 1) & 1], ((nck - 1) >> 1) & 1, abort_flag,
                                                   a.status, kDiagAttn, 9, nck)))
         ok = false;
-      tc_fence_after();
-      uint32_t ov[128];
-      tmem_ld128(t_o + lane_off, ov);
-      tc_fence_before();
-      if (!ok) l = 1.f;
+      uint32_t ov[64];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld64(t_o + lane_off + hk * 64, ov);
+        tc_fence_before();
+      }
+      // the row's normaliser: both halves' sums
+      named_bar_sync(pair_bar, 64);
+      xrow[hk * 128 + r] = l;
+      named_bar_sync(pair_bar, 64);
+      l += xrow[(hk ^ 1) * 128 + r];
+      if (!ok) {
+        l = 1.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) ov[i] = 0u;
+      }
       pdl_wait();
       if (a.splits == 1) {
         if (r < q_valid) {
           const float inv = 1.f / l;
-          uint4* og = reinterpret_cast<uint4*>(a.o + ((size_t)bi * a.rows_per_seq + row0 + r) * a.d + hc);
+          uint4* og = reinterpret_cast<uint4*>(a.o + ((size_t)bi * a.rows_per_seq + row0 + r) * a.d + hc + hk * 64);
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
+          for (int u = 0; u < 8; ++u) {
             const int i = u * 8;
             og[u] = make_uint4(pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv),
                                pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv),
@@ -413,12 +486,16 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
         // stores at once fall in different banks
         float4* po = reinterpret_cast<float4*>(sm + kAtcOffK) + r * 32;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          po[i ^ (r & 31)] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
-                              __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
-        float* pml = reinterpret_cast<float*>(sm + kAtcOffP) + r * 2;
-        pml[0] = m_used;
-        pml[1] = l;
+        for (int u = 0; u < 16; ++u) {
+          const int i = hk * 16 + u;
+          po[i ^ (r & 31)] = make_float4(__uint_as_float(ov[4 * u]), __uint_as_float(ov[4 * u + 1]),
+                                         __uint_as_float(ov[4 * u + 2]), __uint_as_float(ov[4 * u + 3]));
+        }
+        if (hk == 0) {
+          float* pml = reinterpret_cast<float*>(sm + kAtcOffP) + r * 2;
+          pml[0] = m_used;
+          pml[1] = l;
+        }
       }
     }
   }
@@ -431,7 +508,7 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
     if (warp >= 2) {
       // This CTA merges rows [ra, rb) of the tile over all splits.  Every
       // remote load of a step is issued before any of its values is used.
-      const int t = threadIdx.x - 64;  // 0..127
+      const int t = threadIdx.x - 64;  // 0..255
       const int rank = (int)cluster.block_rank();
       const int per = (q_valid + a.splits - 1) / a.splits;
       const int ra = rank * per, nr = max(0, min(q_valid, ra + per) - ra);
@@ -464,16 +541,16 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
 #pragma unroll
         for (int sp = 0; sp < kAtcMaxSplits; ++sp) coef[t * kAtcMaxSplits + sp] = mv[sp] * inv;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kAtcSoftmax);
       // two items per thread per round: every remote load of the round is
       // issued before any of its values is used (a store in between would
       // order the next item's loads behind it)
       const int n_items = nr * 32;
-      for (int base = t; base < n_items; base += 2 * 128) {
+      for (int base = t; base < n_items; base += 2 * kAtcSoftmax) {
         float4 o[2][kAtcMaxSplits];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int idx = base + u * 128;
+          const int idx = base + u * kAtcSoftmax;
           if (idx < n_items) {
             const int rr = ra + (idx >> 5), c4 = (idx & 31) * 4;
 #pragma unroll
@@ -485,7 +562,7 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int idx = base + u * 128;
+          const int idx = base + u * kAtcSoftmax;
           if (idx < n_items) {
             const int row = idx >> 5, c4 = (idx & 31) * 4;
             float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
