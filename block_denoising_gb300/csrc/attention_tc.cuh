@@ -7,28 +7,34 @@
 //
 // One CTA = 128 query rows x one head x one range of 128-key chunks,
 // 320 threads:
-//   warp 0     TMA: Q once, then K and V chunks (2-stage rings with their own
-//              barriers: a K stage is refilled as soon as S of its chunk has
-//              been computed, a V stage once P V of its chunk has; 3-D tensor
-//              maps so that keys past L and rows past the sequence read as
-//              zeros);
+//   warp 0     TMA: Q once, then K and V chunks (2-stage K and V rings with
+//              their own barriers: a K stage is refilled as soon as S of its
+//              chunk has been computed, a V stage once P V of its chunk has;
+//              3-D tensor maps so that keys past L and rows past the sequence
+//              read as zeros);
 //   warp 1     TMEM allocation and the single-thread MMA issue:
-//              S_j = Q K_j^T into one of two TMEM buffers, then O += P_{j-1} V_{j-1}
-//              (V is the MN-major operand, P comes from shared memory);
+//              S_j = Q K_j^T into one of two TMEM buffers, and for each key
+//              half h, O_h += P_{j,h} V_{j,h} (64 keys; P from shared memory,
+//              V the MN-major operand), in the order S_0, S_1, then per chunk
+//              j: P V of both halves, S_{j+2};
 //   warps 2-9  softmax, two threads per query row: warp w reads TMEM lane
-//              quadrant w % 4 and takes key half (w - 2) / 4 (64 of the
-//              chunk's 128 keys; the two warps of a quadrant share the SM
-//              sub-partition and agree on the row max through shared memory):
-//              tcgen05.ld of its half row of S, online softmax in the log2
-//              domain, P = bf16(2^(s - m)) written to its 64-key slab of one of
-//              two shared-memory buffers in the 128-byte-swizzled K-major
-//              layout (so the softmax of chunk j overlaps P_{j-1} V_{j-1}),
-//              final O / l for its 64 output columns.  Warps whose 32 rows all
-//              lie past the sequence's rows (a 64-row block) only keep the
-//              barrier counts.
-// The running max used for the exponent is raised only when a chunk's max
-// exceeds it by more than 8 (P stays <= 2^8); then O (in TMEM) and l are
-// rescaled once.  O / l is exact whatever max was used.
+//              quadrant w % 4 and takes key half h = (w - 2) / 4, keys
+//              64 h .. 64 h + 63 of every chunk.  Each half is an online
+//              softmax of its own (running max m_h, normaliser l_h and
+//              accumulator O_h in TMEM), so the two warps that share an SM
+//              sub-partition never wait for each other and hide each other's
+//              latencies: tcgen05.ld of the half row of S, log2-domain
+//              softmax, P = bf16(2^(s - m_h)) written to the half's 64-key
+//              slab of one of two shared-memory buffers in the
+//              128-byte-swizzled K-major layout (so the softmax of chunk j
+//              overlaps P_{j-1} V_{j-1}).  At the end the halves combine:
+//              m = max(m_0, m_1), O = sum_h 2^(m_h - m) O_h, l likewise, and
+//              each thread writes O / l for 64 output columns.  Warps whose 32
+//              rows all lie past the sequence's rows (a 64-row block) only
+//              keep the barrier counts.
+// A running max is raised only when a chunk's max exceeds it by more than 8
+// (P stays <= 2^8); then that half's O (in TMEM) and l are rescaled once.
+// O / l is exact whatever max was used.
 // Small grids (a batch-1 block) split the keys over up to 8 CTAs of a cluster;
 // partials (m, l, O) are merged through distributed shared memory.
 #pragma once
@@ -58,9 +64,9 @@ constexpr int kAtcSoftmax = 256;        // softmax threads: 128 rows x 2 key hal
 constexpr int kAtcKeys = 128;           // keys per chunk
 constexpr int kAtcTile = 128 * 128 * 2; // one 128 x 128 bf16 operand (two 64-column swizzle slabs)
 constexpr int kAtcSlab = 128 * 128;     // bytes of one 64-column slab of 128 rows
-constexpr int kAtcStages = 2;
+constexpr int kAtcStages = 2;           // K ring and V ring
 constexpr int kAtcMaxSplits = 8;
-// Q | K[stages] | V[stages] | P[2] | barriers | row exchange [2 halves][128]
+// Q | K[2] | V[2] | P[2] | barriers | row exchange [2 halves][128]
 constexpr int kAtcOffK = kAtcTile;
 constexpr int kAtcOffV = kAtcOffK + kAtcStages * kAtcTile;
 constexpr int kAtcOffP = kAtcOffV + kAtcStages * kAtcTile;
@@ -68,7 +74,8 @@ constexpr int kAtcOffBar = kAtcOffP + 2 * kAtcTile;
 constexpr int kAtcOffX = kAtcOffBar + 256;
 constexpr int kAtcSmem = 1024 + kAtcOffX + 2 * 128 * 4;
 static_assert(kAtcSmem <= 232448, "attention shared memory above 227 KB");
-constexpr int kAtcTmemCols = 512;       // S0 | S1 | O | unused
+constexpr int kAtcTmemCols = 512;       // S0 | S1 | O_0 | O_1
+constexpr int kAtcColO = 256;
 constexpr float kAtcLazy = 8.0f;        // log2 growth of the max tolerated before rescaling O
 
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
@@ -144,6 +151,14 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&x)[64]) {
   asm volatile("" : ATC_I32(x, 32));
 }
 
+// 32 TMEM columns at each of two addresses of this warp's 32 lanes, one wait
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&x)[32], uint32_t tb, uint32_t (&y)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 0) : "r"(ta));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(y, 0) : "r"(tb));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : ATC_I32(x, 0)::"memory");
+  asm volatile("" : ATC_I32(y, 0));
+}
+
 // 2^x with the PTX approximate base-2 exponential (2^-inf = +0)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -168,9 +183,9 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
   uint64_t* v_empty = v_full + kAtcStages;      // [2]
   uint64_t* s_full = v_empty + kAtcStages;      // [2]
   uint64_t* s_empty = s_full + 2;               // [2]
-  uint64_t* p_full = s_empty + 2;               // [2]
-  uint64_t* pv_done = p_full + 2;               // [2]
-  uint64_t* drain = pv_done + 2;
+  uint64_t* p_full = s_empty + 2;               // [half][2]
+  uint64_t* pv_done = p_full + 4;               // [half][2]
+  uint64_t* drain = pv_done + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -196,7 +211,9 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], kAtcSoftmax);
-      mbar_init(&p_full[s], kAtcSoftmax);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&p_full[s], kAtcSoftmax / 2);
       mbar_init(&pv_done[s], 1);
     }
     mbar_init(drain, 1);
@@ -217,9 +234,9 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
   // grid leaves and request its first weight tiles; it reads this grid's
   // output only after griddepcontrol.wait (the whole grid complete)
   if (threadIdx.x == 0) pdl_trigger();
-  // S buffer b at columns 128 b (computed, not an indexed array: local memory
-  // would live in L2 on an SM whose memory is carved out as shared memory)
-  const uint32_t t_o = tmem + 256;
+  // TMEM buffers at computed column offsets (not indexed arrays: local
+  // memory would live in L2 on an SM whose memory is carved out as shared
+  // memory): S buffer b at 128 b, O_h at 256 + 128 h
   const int hc = head * 128;  // first column of this head
 
   if (warp == 0) {
@@ -267,9 +284,8 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
         tma_load_3d(vb + kAtcSlab, &maps.v, &v_full[st], hc + 64, key0, bi);
         return true;
       };
-      // K runs two chunks ahead of V: K_{j+2} waits for S_j, which the
-      // tensor pipe finishes before P_{j-1} V_{j-1}, so queuing it behind
-      // V_j costs nothing
+      // K runs two chunks ahead of V: K_{j+2} waits for S_j, which is issued
+      // before P_{j-1} V_{j-1} completes (what V_{j+1} waits for)
       bool go = true;
       for (int j = 0; j < min(nck, kAtcStages) && go; ++j) go = load_k(j);
       for (int j = 0; j < nck && go && !*abort_flag; ++j) {
@@ -290,58 +306,64 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128) | (1u << 16);  // B (V) MN-major
       const uint32_t q_addr = smem_u32(sm), p_addr = smem_u32(sm + kAtcOffP);
-      // O += P_i V_i; P_i sits in buffer i & 1
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % kAtcStages, pb = i & 1;
-        if (!mbar_wait_diag(&p_full[pb], (i >> 1) & 1, abort_flag, a.status, kDiagAttn, 2, i)) return false;
-        if (!mbar_wait_diag(&v_full[st], (i / kAtcStages) & 1, abort_flag, a.status, kDiagAttn, 11, i)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sm + kAtcOffV + st * kAtcTile);
-        const uint32_t pa = p_addr + pb * kAtcTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
-          const uint64_t ad = make_sw128_desc(pa + (kk >> 2) * kAtcSlab + (kk & 3) * 32);
-          const uint64_t bd = make_sw128_desc_mn(v_addr + kk * 2048, kAtcSlab);
-          tc_mma_bf16(t_o, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&v_empty[st]);
-        tc_commit(&pv_done[pb]);
-        return true;
-      };
-      bool ok = mbar_wait_diag(q_full, 0, abort_flag, a.status, kDiagAttn, 3, 0);
-      for (int j = 0; j < nck && ok; ++j) {
+      // S_j = Q K_j^T into S buffer j & 1
+      auto issue_s = [&](int j) -> bool {
         const int st = j % kAtcStages, sb = j & 1;
-        if (!mbar_wait_diag(&k_full[st], (j / kAtcStages) & 1, abort_flag, a.status, kDiagAttn, 4, j)) { ok = false; break; }
-        if (!mbar_wait_diag(&s_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag, a.status, kDiagAttn, 5, j)) { ok = false; break; }
+        if (!mbar_wait_diag(&k_full[st], (j / kAtcStages) & 1, abort_flag, a.status, kDiagAttn, 4, j)) return false;
+        if (!mbar_wait_diag(&s_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag, a.status, kDiagAttn, 5, j)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sm + kAtcOffK + st * kAtcTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // 16 head dims per step
           const uint64_t ad = make_sw128_desc(q_addr + (kk >> 2) * kAtcSlab + (kk & 3) * 32);
           const uint64_t bd = make_sw128_desc(k_addr + (kk >> 2) * kAtcSlab + (kk & 3) * 32);
-          tc_mma_bf16((tmem + sb * 128), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + sb * 128, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[sb]);
         tc_commit(&k_empty[st]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        return true;
+      };
+      // O_h += P_{j,h} V_{j,h}: keys 64 h .. 64 h + 63 of chunk j, P in slab h
+      // of P buffer j & 1, V rows 64 h .. of V stage j % 2
+      auto issue_pv = [&](int j, int h) -> bool {
+        const int st = j % kAtcStages, pb = j & 1;
+        if (!mbar_wait_diag(&p_full[h * 2 + pb], (j >> 1) & 1, abort_flag, a.status, kDiagAttn, 2, j)) return false;
+        if (h == 0 && !mbar_wait_diag(&v_full[st], (j / kAtcStages) & 1, abort_flag, a.status, kDiagAttn, 11, j))
+          return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sm + kAtcOffV + st * kAtcTile);
+        const uint32_t pa = p_addr + pb * kAtcTile + h * kAtcSlab;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // 16 keys per step
+          const uint64_t ad = make_sw128_desc(pa + kk * 32);
+          const uint64_t bd = make_sw128_desc_mn(v_addr + (h * 4 + kk) * 2048, kAtcSlab);
+          tc_mma_bf16(tmem + kAtcColO + h * 128, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&pv_done[h * 2 + pb]);
+        if (h == 1) tc_commit(&v_empty[st]);  // both halves have read V_j
+        return true;
+      };
+      bool ok = mbar_wait_diag(q_full, 0, abort_flag, a.status, kDiagAttn, 3, 0);
+      for (int j = 0; j < min(nck, 2) && ok; ++j) ok = issue_s(j);
+      for (int j = 0; j < nck && ok; ++j) {
+        ok = issue_pv(j, 0) && issue_pv(j, 1);
+        if (ok && j + 2 < nck) ok = issue_s(j + 2);
       }
-      if (ok && nck > 0) issue_pv(nck - 1);
       tc_commit(drain);
       mbar_wait_drain(drain, 0);
     }
   } else {
     // ------------------------------ softmax / output ------------------------------
     // Every wait's outcome is made warp-uniform: the TMEM accesses are
-    // warp-collective.  The two warps of a quadrant meet at the same number
-    // of pair barriers whatever their waits returned (a failed wait only
-    // skips work), so that a timed-out wait never leaves the partner blocked.
+    // warp-collective.  The two warps of a quadrant meet only at the end, at
+    // the same pair barriers whatever their waits returned (a failed wait
+    // only skips work), so that a timed-out wait never leaves a warp blocked.
     const int q = warp & 3;
     const int hk = (warp - 2) >> 2;         // key half: keys 64 hk .. 64 hk + 63 of a chunk
     const int r = q * 32 + lane;            // query row inside the tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const bool live = q * 32 < q_valid;     // warp-uniform, the same for both halves
-    const int pair_bar = 2 + q;             // named barrier of the quadrant's two warps
-    float* xrow = reinterpret_cast<float*>(sm + kAtcOffX);  // [2 halves][128 rows]
+    const uint32_t t_oh = tmem + kAtcColO + hk * 128 + lane_off;  // this half's O
     const float sc = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
@@ -352,74 +374,67 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
         ok = false;
       if (!live) {  // rows past the sequence: keep the counts only
         mbar_arrive(&s_empty[sb]);
-        mbar_arrive(&p_full[sb]);
+        mbar_arrive(&p_full[hk * 2 + sb]);
         continue;
       }
-      uint32_t sv[64];
-      float mh = -INFINITY;
-      if (ok) {
-        tc_fence_after();
-        tmem_ld64((tmem + sb * 128 + hk * 64) + lane_off, sv);
-        tc_fence_before();
-        mbar_arrive(&s_empty[sb]);
-        const int nvalid = a.L - (c_begin + j) * kAtcKeys - hk * 64;  // may be <= 0 in the upper half
-        if (nvalid < 64) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i >= nvalid) sv[i] = 0xff800000u;  // -inf: no key
-        }
-        float mx0 = __uint_as_float(sv[0]), mx1 = __uint_as_float(sv[1]);
-        float mx2 = __uint_as_float(sv[2]), mx3 = __uint_as_float(sv[3]);
-#pragma unroll
-        for (int i = 4; i < 64; i += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sv[i]));
-          mx1 = fmaxf(mx1, __uint_as_float(sv[i + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sv[i + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sv[i + 3]));
-        }
-        mh = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;
-      }
-      // the chunk's row max over both halves (the lower half holds key 0 of
-      // the chunk, a valid key, so mj is finite)
-      named_bar_sync(pair_bar, 64);  // the partner has read the previous chunk's value
-      xrow[hk * 128 + r] = mh;
-      named_bar_sync(pair_bar, 64);
-      const float mj = fmaxf(mh, xrow[(hk ^ 1) * 128 + r]);
       if (!ok) continue;
-      if (j == 0) {
+      uint32_t sv[64];
+      tc_fence_after();
+      tmem_ld64((tmem + sb * 128 + hk * 64) + lane_off, sv);
+      tc_fence_before();
+      mbar_arrive(&s_empty[sb]);
+      const int nvalid = a.L - (c_begin + j) * kAtcKeys - hk * 64;  // <= 0: the upper half holds no key
+      if (nvalid < 64) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i >= nvalid) sv[i] = 0xff800000u;  // -inf: no key
+      }
+      float mx0 = __uint_as_float(sv[0]), mx1 = __uint_as_float(sv[1]);
+      float mx2 = __uint_as_float(sv[2]), mx3 = __uint_as_float(sv[3]);
+#pragma unroll
+      for (int i = 4; i < 64; i += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sv[i]));
+        mx1 = fmaxf(mx1, __uint_as_float(sv[i + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sv[i + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sv[i + 3]));
+      }
+      const float mj = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;  // -inf when the half holds no key
+      if (m_used == -INFINITY) {
+        // nothing accumulated yet (O_h and l hold zeros or nothing): start
+        // from this chunk's max, -inf again if it holds no key either
         m_used = mj;
       } else {
         const bool grow = mj > m_used + kAtcLazy;
         if (__any_sync(0xffffffffu, grow)) {
-          // rescale this half's columns of O: O must hold every product
-          // issued so far (P_{j-1} V_{j-1})
-          if (!__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag,
-                                                      a.status, kDiagAttn, 7, j))) {
+          // rescale O_h: it must hold every product issued so far (P_{j-1} V_{j-1})
+          if (!__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[hk * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1,
+                                                      abort_flag, a.status, kDiagAttn, 7, j))) {
             ok = false;
             continue;
           }
           tc_fence_after();
           const float alpha = grow ? ex2_approx(m_used - mj) : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 8; ++c) {
             float o16[16];
-            tmem_ld16(t_o + lane_off + hk * 64 + c * 16, o16);
+            tmem_ld16(t_oh + c * 16, o16);
 #pragma unroll
             for (int i = 0; i < 16; ++i) o16[i] *= alpha;
-            tmem_st16(t_o + lane_off + hk * 64 + c * 16, o16);
+            tmem_st16(t_oh + c * 16, o16);
           }
           tc_fence_before();
           l *= alpha;
           if (grow) m_used = mj;
         }
       }
-      // buffer sb is free once P_{j-2} V_{j-2} completed
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[sb], ((j >> 1) & 1) ^ 1, abort_flag, a.status,
-                                                             kDiagAttn, 8, j))) {
+      // this half's slab of buffer sb is free once P_{j-2} V_{j-2} of the half completed
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[hk * 2 + sb], ((j >> 1) & 1) ^ 1, abort_flag,
+                                                             a.status, kDiagAttn, 8, j))) {
         ok = false;
         continue;
       }
-      const float nm = -m_used;
+      // with no key seen yet (m_used = -inf) every p is 2^-inf = 0
+      const float nm = m_used == -INFINITY ? 0.f : -m_used;
       uint8_t* prow = sm + kAtcOffP + sb * kAtcTile + hk * kAtcSlab + r * 128;
       float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
@@ -442,60 +457,74 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
       l += (rs0 + rs1) + (rs2 + rs3);
       fence_async_shared();  // the P rows become visible to the tensor cores
       tc_fence_before();
-      mbar_arrive(&p_full[sb]);
+      mbar_arrive(&p_full[hk * 2 + sb]);
     }
     if (live) {
       if (ok && nck > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[(nck - 1) & 1], ((nck - 1) >> 1) & 1, abort_flag,
-                                                  a.status, kDiagAttn, 9, nck)))
+          !__all_sync(0xffffffffu, mbar_wait_diag(&pv_done[hk * 2 + ((nck - 1) & 1)], ((nck - 1) >> 1) & 1,
+                                                  abort_flag, a.status, kDiagAttn, 9, nck)))
         ok = false;
-      uint32_t ov[64];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld64(t_o + lane_off + hk * 64, ov);
-        tc_fence_before();
-      }
-      // the row's normaliser: both halves' sums
+      // combine the halves: both quadrant warps are past their last product,
+      // so every MMA of the CTA has completed and Q is free
+      const int pair_bar = 2 + q;             // named barrier of the quadrant's two warps
+      float* xm = reinterpret_cast<float*>(sm + kAtcOffBar + 256);  // [half][128] running max
+      float* xl = reinterpret_cast<float*>(sm);                     // [half][128] normaliser, over Q
       named_bar_sync(pair_bar, 64);
-      xrow[hk * 128 + r] = l;
+      xm[hk * 128 + r] = ok ? m_used : -INFINITY;
+      xl[hk * 128 + r] = ok ? l : 0.f;
       named_bar_sync(pair_bar, 64);
-      l += xrow[(hk ^ 1) * 128 + r];
-      if (!ok) {
-        l = 1.f;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) ov[i] = 0u;
-      }
+      const float m_o = xm[(hk ^ 1) * 128 + r], l_o = xl[(hk ^ 1) * 128 + r];
+      const float mown = ok ? m_used : -INFINITY;
+      const float m = fmaxf(mown, m_o);
+      // -inf - -inf is NaN: a half with no key (or a failed one) weighs 0
+      const float s_own = mown == -INFINITY ? 0.f : ex2_approx(mown - m);
+      const float s_oth = m_o == -INFINITY ? 0.f : ex2_approx(m_o - m);
+      const float lt = (ok ? l : 0.f) * s_own + l_o * s_oth;
+      const bool good = ok && lt > 0.f;
       pdl_wait();
-      if (a.splits == 1) {
-        if (r < q_valid) {
-          const float inv = 1.f / l;
-          uint4* og = reinterpret_cast<uint4*>(a.o + ((size_t)bi * a.rows_per_seq + row0 + r) * a.d + hc + hk * 64);
+      // this thread's 64 output columns, 32 at a time: O_own and O_other
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        const int c0 = hk * 64 + part * 32;
+        uint32_t oa[32], ob[32];
+        if (good) {
+          tc_fence_after();
+          tmem_ld32x2(tmem + kAtcColO + hk * 128 + lane_off + c0, oa,
+                      tmem + kAtcColO + (hk ^ 1) * 128 + lane_off + c0, ob);
+          tc_fence_before();
+        }
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          o[i] = good ? __uint_as_float(oa[i]) * s_own + __uint_as_float(ob[i]) * s_oth : 0.f;
+        if (a.splits == 1) {
+          if (r < q_valid) {
+            const float inv = good ? 1.f / lt : 0.f;
+            uint4* og = reinterpret_cast<uint4*>(a.o + ((size_t)bi * a.rows_per_seq + row0 + r) * a.d + hc + c0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = u * 8;
+              og[u] = make_uint4(pack_bf16x2(o[i] * inv, o[i + 1] * inv), pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
+                                 pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv), pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
+            }
+          }
+        } else {
+          // partial (O relative to m, m, l) in this CTA's shared memory, over
+          // the K ring and the P buffers, merged below; float4 column i of row
+          // r at (i ^ r) mod 32: the 32 rows a warp stores at once fall in
+          // different banks
+          float4* po = reinterpret_cast<float4*>(sm + kAtcOffK) + r * 32;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const int i = u * 8;
-            og[u] = make_uint4(pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv),
-                               pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv),
-                               pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv),
-                               pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv));
+            const int i = c0 / 4 + u;
+            po[i ^ (r & 31)] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
           }
         }
-      } else {
-        // partial (unnormalised O, m, l) in this CTA's shared memory, over the
-        // K ring and the P buffers, merged below
-        // float4 column i of row r at (i ^ r) mod 32: the 32 rows a warp
-        // stores at once fall in different banks
-        float4* po = reinterpret_cast<float4*>(sm + kAtcOffK) + r * 32;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int i = hk * 16 + u;
-          po[i ^ (r & 31)] = make_float4(__uint_as_float(ov[4 * u]), __uint_as_float(ov[4 * u + 1]),
-                                         __uint_as_float(ov[4 * u + 2]), __uint_as_float(ov[4 * u + 3]));
-        }
-        if (hk == 0) {
-          float* pml = reinterpret_cast<float*>(sm + kAtcOffP) + r * 2;
-          pml[0] = m_used;
-          pml[1] = l;
-        }
+      }
+      if (a.splits > 1 && hk == 0) {
+        float* pml = reinterpret_cast<float*>(sm + kAtcOffP) + r * 2;
+        pml[0] = good ? m : -INFINITY;
+        pml[1] = good ? lt : 0.f;
       }
     }
   }
@@ -534,10 +563,10 @@ __global__ void __launch_bounds__(kAtcThreads, 1)
         float lsum = 0.f;
 #pragma unroll
         for (int sp = 0; sp < kAtcMaxSplits; ++sp) {
-          mv[sp] = ex2_approx(mv[sp] - mmax);
+          mv[sp] = mv[sp] == -INFINITY ? 0.f : ex2_approx(mv[sp] - mmax);
           lsum = fmaf(mv[sp], lv[sp], lsum);
         }
-        const float inv = 1.f / lsum;
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
         for (int sp = 0; sp < kAtcMaxSplits; ++sp) coef[t * kAtcMaxSplits + sp] = mv[sp] * inv;
       }
