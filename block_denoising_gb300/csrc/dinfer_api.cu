@@ -27,6 +27,7 @@
 #include "attention.cuh"
 #include "attention_tc.cuh"
 #include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 #include "lmhead_tc.cuh"
 #include "moe.cuh"
 #include "noalloc.cuh"
@@ -95,6 +96,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 int g_num_sms[kMaxDevices] = {};
 bool g_attrs_done[kMaxDevices] = {};
+int g_pair_clusters[kMaxDevices] = {};  // co-resident 2-CTA clusters of the pair GEMM
 
 int current_device() {
   int dev = 0;
@@ -166,6 +168,30 @@ bool set_smem_attrs() {
                              LmCfg<256>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtcSmem) ==
         cudaSuccess;
+  ok &= cudaFuncSetAttribute(gemm_tc2_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Gemm2Cfg<256>::kSmem) == cudaSuccess;
+  {
+    // how many pairs run at once: clusters live inside one GPC, so SMs of a
+    // GPC with an odd count of free SMs may stay out
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * 256);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = Gemm2Cfg<256>::kSmem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = 2;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    // a failed query leaves the pair path off (one-CTA tiles everywhere)
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<256>, &cfg) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();
+    }
+    g_pair_clusters[dev] = n;
+  }
   ok &= cudaFuncSetAttribute(lmhead_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
         cudaSuccess;
   ok &= cudaFuncSetAttribute(attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
@@ -258,6 +284,53 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
       break;
   }
   return e;
+}
+
+// Pair-CTA GEMM (gemm_tc2_kernel): 256 weight rows x 256 tokens per tile,
+// whole tiles dealt round-robin over the co-resident pairs.  It pays where
+// the GEMM is tensor-bound (many token rows) and its tiles keep >= 85% of the
+// pairs busy; otherwise the one-CTA kernel (stream-K where needed) runs.
+constexpr int kPairBN = 256;
+int pair_clusters() {
+  set_smem_attrs();
+  return g_pair_clusters[current_device()];
+}
+bool use_pair_gemm(int M, int n_tiles) {
+  const int P = pair_clusters();
+  if (P < 1 || M < 512 || n_tiles % 2) return false;
+  const long long tiles = (long long)(n_tiles / 2) * ((M + kPairBN - 1) / kPairBN);
+  const long long per = (tiles + P - 1) / P;
+  return tiles * 100 >= per * P * 85;
+}
+// maps.b: the token operand with 128-row boxes (each CTA stages half a tile)
+cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s) {
+  a.m_tiles = (a.M + kPairBN - 1) / kPairBN;
+  a.k_tiles = a.K / 64;
+  a.stream_k = 0;
+  const long long tiles = (long long)(a.n_tiles / 2) * a.m_tiles;
+  const int pairs = (int)std::min<long long>(pair_clusters(), tiles);
+  if (pairs < 1 || a.n_tiles % 2) return cudaErrorInvalidValue;
+  a.grid = 2 * pairs;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = Gemm2Cfg<kPairBN>::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  if (g_pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  at[n].id = cudaLaunchAttributeClusterDimension;
+  at[n].val.clusterDim.x = 2;
+  at[n].val.clusterDim.y = 1;
+  at[n].val.clusterDim.z = 1;
+  ++n;
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<kPairBN>, maps, a);
 }
 
 // Grouped (MoE expert) GEMM: persistent grid, tiles from the device tables.
@@ -648,13 +721,19 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BNo) ||
       (!d.n_experts && !make_map(&mact.b, c->act, rows, F, BN)))
     return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
+  // many rows: the QKV and gate/up projections on 256 x 256 pair-CTA tiles
+  const bool pair_qkv = use_pair_gemm(rows, 3 * D / 128);
+  const bool pair_gu = !d.n_experts && use_pair_gemm(rows, F / 64);
+  GemmMaps mx2{};
+  if ((pair_qkv || pair_gu) && !make_map(&mx2.b, c->xn, rows, D, kPairBN / 2))
+    return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
   const int nthr = ((D / 16 + 31) / 32) * 32;  // fused-norm threads per row: whole warps
   if (nthr > 512 || D % 128) return fail(c, DINFER_EINVAL, "d_model unsupported by the fused residual norm");
   for (int l = 0; l < d.n_layers; ++l) {
     // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue
     {
-      GemmMaps m = mx;
+      GemmMaps m = pair_qkv ? mx2 : mx;
       m.a[0] = c->m_wq[l];
       m.a[1] = c->m_wk[l];
       m.a[2] = c->m_wv[l];
@@ -670,7 +749,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.rows_per_seq = f.rows_per_seq; a.seq_len = f.L; a.pos_from_state = f.pos_from_state;
       a.row_off = f.row_off;
       a.state = c->st; a.ws = c->gemm_ws; a.status = c->st;
-      CK(launch_gemm_tc(m, a, BN, s));
+      CK(pair_qkv ? launch_gemm_tc2(m, a, s) : launch_gemm_tc(m, a, BN, s));
     }
     // a3: attention over the dual cache
     CK(launch_attention(c->q, c->kc_layer(l), c->vc_layer(l), c->attn_o, f.batch, f.rows_per_seq, H, f.L, ap,
@@ -708,14 +787,14 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
     }
     // a5: SwiGLU FFN (gate/up with the SiLU*up epilogue, down + residual)
     {
-      GemmMaps m = mx;
+      GemmMaps m = pair_gu ? mx2 : mx;
       m.a[0] = c->m_wg[l];
       m.a[1] = c->m_wu[l];
       GemmArgs a{};
       a.M = rows; a.N = F; a.K = D; a.n_tiles = F / 64; a.a_mode = A_PAIR;
       a.out_bf16 = (__nv_bfloat16*)c->act; a.ldo = F;
       a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
-      CK(launch_gemm_tc(m, a, BN, s));
+      CK(pair_gu ? launch_gemm_tc2(m, a, s) : launch_gemm_tc(m, a, BN, s));
       GemmMaps m2 = mact;
       m2.a[0] = c->m_wd[l];
       GemmArgs b{};
@@ -1508,14 +1587,16 @@ dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_
   const int BN = bn_for_rows(M);
   if ((size_t)((M + BN - 1) / BN) * (N / 128) * 4 > kOpTicketBytes) return fail(c, DINFER_EINVAL, "too many tiles");
   if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
+  const bool pair = use_pair_gemm(M, N / 128);
   GemmMaps m{};
-  if (!make_map(&m.a[0], W, N, K, 128) || !make_map(&m.b, X, M, K, BN))
+  if (!make_map(&m.a[0], W, N, K, 128) || !make_map(&m.b, X, M, K, pair ? kPairBN / 2 : BN))
     return fail(c, DINFER_EINVAL, "tensor map encoding failed (alignment?)");
   GemmArgs a{};
   a.M = M; a.N = N; a.K = K; a.n_tiles = N / 128; a.a_mode = A_SINGLE;
   a.out_f32 = Y; a.ldo = N;
   a.ws = reinterpret_cast<float*>(o.data); a.status = o.st; a.state = o.st;
-  CK(launch_gemm_tc(m, a, BN, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CK(pair ? launch_gemm_tc2(m, a, s) : launch_gemm_tc(m, a, BN, s));
   return DINFER_OK;
 }
 

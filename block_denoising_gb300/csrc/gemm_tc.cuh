@@ -148,27 +148,48 @@ struct Sched {
   __host__ __device__ __forceinline__ int owner(unsigned u) const { return (int)(((u + 1) * G - 1) / U); }
 };
 
-template <int BN>
-__device__ __forceinline__ void load_stage_a(const GemmMaps& maps, const GemmArgs& a, uint8_t* stage, uint64_t* bar,
+// 2-D tiled TMA load into this CTA's shared memory, completing on the
+// mbarrier at shared::cluster address `bar`: this CTA's own, or (kPair, the
+// cta_group::2 form) the pair leader's.
+template <bool kPair>
+__device__ __forceinline__ void tma_load_2d_to(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                               uint64_t policy) {
+  if (kPair)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// The 128 weight rows of tile tr.nt, k-step k, into `stage`.
+template <bool kPair = false>
+__device__ __forceinline__ void load_stage_a(const GemmMaps& maps, const GemmArgs& a, uint8_t* stage, uint32_t bar,
                                              const TileRef& tr, int k, uint64_t pol_w) {
   uint8_t* sa = stage;
   const int kx = k * 64;
   const int nt = tr.nt;
   if (a.grouped) {
     if (a.a_mode == A_PAIR) {
-      tma_load_2d(sa, &maps.a[0], bar, kx, tr.a_base + nt * 64, pol_w);
-      tma_load_2d(sa + 64 * 128, &maps.a[0], bar, kx, tr.a_base + a.g_a_half + nt * 64, pol_w);
+      tma_load_2d_to<kPair>(sa, &maps.a[0], bar, kx, tr.a_base + nt * 64, pol_w);
+      tma_load_2d_to<kPair>(sa + 64 * 128, &maps.a[0], bar, kx, tr.a_base + a.g_a_half + nt * 64, pol_w);
     } else {
-      tma_load_2d(sa, &maps.a[0], bar, kx, tr.a_base + nt * 128, pol_w);
+      tma_load_2d_to<kPair>(sa, &maps.a[0], bar, kx, tr.a_base + nt * 128, pol_w);
     }
   } else if (a.a_mode == A_PAIR) {
-    tma_load_2d(sa, &maps.a[0], bar, kx, nt * 64, pol_w);
-    tma_load_2d(sa + 64 * 128, &maps.a[1], bar, kx, nt * 64, pol_w);
+    tma_load_2d_to<kPair>(sa, &maps.a[0], bar, kx, nt * 64, pol_w);
+    tma_load_2d_to<kPair>(sa + 64 * 128, &maps.a[1], bar, kx, nt * 64, pol_w);
   } else if (a.a_mode == A_THREE) {
     const int per = a.a_rows / 128;
-    tma_load_2d(sa, &maps.a[nt / per], bar, kx, (nt % per) * 128, pol_w);
+    tma_load_2d_to<kPair>(sa, &maps.a[nt / per], bar, kx, (nt % per) * 128, pol_w);
   } else {
-    tma_load_2d(sa, &maps.a[0], bar, kx, nt * 128, pol_w);
+    tma_load_2d_to<kPair>(sa, &maps.a[0], bar, kx, nt * 128, pol_w);
   }
 }
 template <int BN>
@@ -432,7 +453,7 @@ __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArg
       const TileRef tr = decode_tile<BN>(a, t);
       for (int k = kb; k < ke && pre < C::kStages; ++k, ++pre) {
         mbar_arrive_expect_tx(&p.full[pre], C::kStage);
-        load_stage_a<BN>(maps, a, p.stages + pre * C::kStage, &p.full[pre], tr, k, pol_w);
+        load_stage_a(maps, a, p.stages + pre * C::kStage, smem_u32(&p.full[pre]), tr, k, pol_w);
         pre_b[pre] = tr.b_row;
         pre_k[pre] = k;
       }
@@ -453,7 +474,7 @@ __device__ __forceinline__ void run_producer(const GemmMaps& maps, const GemmArg
       const uint32_t round = it / C::kStages;
       if (!mbar_wait(&p.empty[s], (round & 1) ^ 1, p.abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(&p.full[s], C::kStage);
-      load_stage_a<BN>(maps, a, p.stages + s * C::kStage, &p.full[s], tr, k, pol_w);
+      load_stage_a(maps, a, p.stages + s * C::kStage, smem_u32(&p.full[s]), tr, k, pol_w);
       load_stage_b<BN>(maps, p.stages + s * C::kStage, &p.full[s], tr.b_row, k, pol_x);
     }
     if (!ok) break;
@@ -531,6 +552,122 @@ __device__ __forceinline__ Pipe setup_pipe(uint8_t* smem_raw, float*& xchg, uint
   return p;
 }
 
+// Epilogue warps (2-5) of a GEMM CTA: finish the accumulator of each of the
+// CTA's nseg segments in turn.  seg_tile(j, t, kb, ke, tr) names segment j
+// (tile t, k-steps [kb, ke), operands and outputs tr); a segment that is not
+// a whole tile leaves token-major fp32 partials at partial_slot(t);
+// release(acc) hands accumulator acc back to the MMA issuer.  NXB: exchange
+// buffers (see epilogue_chunk).
+template <int BN, int NXB, class SegFn, class SlotFn, class ReleaseFn>
+__device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Pipe& p, uint32_t tmem_base, float* xchg,
+                                             int warp, int lane, int nseg, SegFn seg_tile, SlotFn partial_slot,
+                                             ReleaseFn release) {
+  pdl_wait();  // global writes only after the preceding kernel completed
+  const int base_pos =
+      a.q_out != nullptr ? (a.pos_from_state ? a.state->block_start : 0) + a.row_off : 0;
+  const int q = warp & 3;                 // TMEM lane quadrant of this warp
+  const int row = q * 32 + lane;          // output feature row inside the tile
+  // QKV: RoPE factors of this row's frequency.  A whole tile loads those of
+  // its first token (and of the sequence start, where a tile wraps into
+  // the next sequence) ahead of its main loop; the following tokens step
+  // by one rotation of the frequency's angle (<= BN steps: an error of a
+  // few fp32 ulps, far below the bf16 rounding of q and k).
+  float rc = 1.f, rs = 0.f, rc0 = 1.f, rs0 = 0.f, step_c = 1.f, step_s = 0.f;
+  if (a.q_out != nullptr) {
+    step_c = __ldg(a.rope_cos + 64 + (row & 63));
+    step_s = __ldg(a.rope_sin + 64 + (row & 63));
+  }
+  int xb = 0;  // exchange buffer of the next pairing chunk
+  for (int j = 0; j < nseg; ++j) {
+    int t, kb, ke;
+    TileRef tr;
+    seg_tile(j, t, kb, ke, tr);
+    const int acc = j & 1;
+    const uint32_t use = j >> 1;
+    const bool whole = (kb == 0 && ke == a.k_tiles);
+    const int n = tr.nt * 128 + row;
+    float hcur[16];  // residual: h of the chunk being finished
+    // loads of the tile's first RoPE factors or residual values overlap its
+    // main loop (a whole tile's h is written by this thread only)
+    int rr = 0;  // QKV: offset of the chunk's first token in its sequence
+    if (a.q_out != nullptr && whole) {
+      rr = (tr.mt * BN) % a.rows_per_seq;
+      rc = __ldg(a.rope_cos + (base_pos + rr) * 64 + (row & 63));
+      rs = __ldg(a.rope_sin + (base_pos + rr) * 64 + (row & 63));
+      rc0 = __ldg(a.rope_cos + base_pos * 64 + (row & 63));
+      rs0 = __ldg(a.rope_sin + base_pos * 64 + (row & 63));
+    }
+    if (a.resid != nullptr && whole) resid_load16(a, n, tr.mt * BN, hcur);
+    if (!mbar_wait(&p.tfull[acc], use & 1, p.abort_flag)) break;
+    tc_fence_after();
+    const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+    if (!whole) {
+      // partial tile: token-major [BN][128], so a warp stores whole lines
+      float* base = partial_slot(t);
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_ld16(tbase + c * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) base[(size_t)(c * 16 + i) * 128 + row] = v[i];
+      }
+      tc_fence_before();
+      release(acc);
+      continue;
+    }
+    if (a.q_out != nullptr) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_ld16(tbase + c * 16, v);
+        float rope[2][16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          rope[0][i] = rc;
+          rope[1][i] = rs;
+          if (++rr == a.rows_per_seq) {
+            rr = 0;
+            rc = rc0;
+            rs = rs0;
+          } else {
+            const float t = fmaf(rc, step_c, -rs * step_s);
+            rs = fmaf(rs, step_c, rc * step_s);
+            rc = t;
+          }
+        }
+        epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg + xb * (128 * 17), tr.m_lim, tr.out_base,
+                           NXB == 1, rope, base_pos);
+        xb ^= NXB - 1;
+      }
+    } else if (a.resid != nullptr) {
+      // residual: h of chunk c + 1 loads while chunk c is finished
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        const int m0 = tr.mt * BN + c * 16;
+        float v[16], hnext[16];
+        tmem_ld16(tbase + c * 16, v);
+        if (c + 1 < BN / 16) resid_load16(a, n, m0 + 16, hnext);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (m0 + i < a.M) a.resid[(size_t)(m0 + i) * a.N + n] = hcur[i] + v[i];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hcur[i] = hnext[i];
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_ld16(tbase + c * 16, v);
+        epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg + xb * (128 * 17), tr.m_lim, tr.out_base,
+                           NXB == 1);
+        xb ^= NXB - 1;
+      }
+    }
+    tc_fence_before();
+    release(acc);
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
@@ -576,113 +713,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (elect_one_sync()) run_mma<BN>(sl, p, tmem_base);
   } else {
-    // ------------------------------ epilogue ------------------------------
-    pdl_wait();  // global writes only after the preceding kernel completed
-    const int base_pos =
-        a.q_out != nullptr ? (a.pos_from_state ? a.state->block_start : 0) + a.row_off : 0;
-    const int q = warp & 3;                 // TMEM lane quadrant of this warp
-    const int row = q * 32 + lane;          // output feature row inside the tile
-    // QKV: RoPE factors of this row's frequency.  A whole tile loads those of
-    // its first token (and of the sequence start, where a tile wraps into
-    // the next sequence) ahead of its main loop; the following tokens step
-    // by one rotation of the frequency's angle (<= BN steps: an error of a
-    // few fp32 ulps, far below the bf16 rounding of q and k).
-    float rc = 1.f, rs = 0.f, rc0 = 1.f, rs0 = 0.f, step_c = 1.f, step_s = 0.f;
-    if (a.q_out != nullptr) {
-      step_c = __ldg(a.rope_cos + 64 + (row & 63));
-      step_s = __ldg(a.rope_sin + 64 + (row & 63));
-    }
-    int xb = 0;  // exchange buffer of the next pairing chunk
-    for (int j = 0; j < sl.nseg; ++j) {
-      int t, kb, ke;
-      sl.seg(j, t, kb, ke);
-      const TileRef tr = decode_tile<BN>(a, t);
-      const int acc = j & 1;
-      const uint32_t use = j >> 1;
-      const bool whole = (kb == 0 && ke == a.k_tiles);
-      const int n = tr.nt * 128 + row;
-      float hcur[16];  // residual: h of the chunk being finished
-      // loads of the tile's first RoPE factors or residual values overlap its
-      // main loop (a whole tile's h is written by this thread only)
-      int rr = 0;  // QKV: offset of the chunk's first token in its sequence
-      if (a.q_out != nullptr && whole) {
-        rr = (tr.mt * BN) % a.rows_per_seq;
-        rc = __ldg(a.rope_cos + (base_pos + rr) * 64 + (row & 63));
-        rs = __ldg(a.rope_sin + (base_pos + rr) * 64 + (row & 63));
-        rc0 = __ldg(a.rope_cos + base_pos * 64 + (row & 63));
-        rs0 = __ldg(a.rope_sin + base_pos * 64 + (row & 63));
-      }
-      if (a.resid != nullptr && whole) resid_load16(a, n, tr.mt * BN, hcur);
-      if (!mbar_wait(&p.tfull[acc], use & 1, p.abort_flag)) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      if (!whole) {
-        // partial tile: slot 0 holds this CTA's part of its first tile, slot 1
-        // of its last; token-major [BN][128], so a warp stores whole lines
-        const int which = (t == sl.tf) ? 0 : 1;
-        float* base = a.ws + ((size_t)blockIdx.x * 2 + which) * (BN * 128);
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          float v[16];
-          tmem_ld16(tbase + c * 16, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) base[(size_t)(c * 16 + i) * 128 + row] = v[i];
-        }
-        tc_fence_before();
-        mbar_arrive(&p.tempty[acc]);
-        continue;
-      }
-      if (a.q_out != nullptr) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          float v[16];
-          tmem_ld16(tbase + c * 16, v);
-          float rope[2][16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            rope[0][i] = rc;
-            rope[1][i] = rs;
-            if (++rr == a.rows_per_seq) {
-              rr = 0;
-              rc = rc0;
-              rs = rs0;
-            } else {
-              const float t = fmaf(rc, step_c, -rs * step_s);
-              rs = fmaf(rs, step_c, rc * step_s);
-              rc = t;
-            }
-          }
-          epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg + xb * (128 * 17), tr.m_lim, tr.out_base,
-                             C::kXchgBufs == 1, rope, base_pos);
-          xb ^= C::kXchgBufs - 1;
-        }
-      } else if (a.resid != nullptr) {
-        // residual: h of chunk c + 1 loads while chunk c is finished
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          const int m0 = tr.mt * BN + c * 16;
-          float v[16], hnext[16];
-          tmem_ld16(tbase + c * 16, v);
-          if (c + 1 < BN / 16) resid_load16(a, n, m0 + 16, hnext);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (m0 + i < a.M) a.resid[(size_t)(m0 + i) * a.N + n] = hcur[i] + v[i];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) hcur[i] = hnext[i];
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          float v[16];
-          tmem_ld16(tbase + c * 16, v);
-          epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg + xb * (128 * 17), tr.m_lim, tr.out_base,
-                             C::kXchgBufs == 1);
-          xb ^= C::kXchgBufs - 1;
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&p.tempty[acc]);
-    }
+    run_epilogue<BN, C::kXchgBufs>(
+        a, p, tmem_base, xchg, warp, lane, sl.nseg,
+        [&](int j, int& t, int& kb, int& ke, TileRef& tr) {
+          sl.seg(j, t, kb, ke);
+          tr = decode_tile<BN>(a, t);
+        },
+        // slot 0 holds this CTA's part of its first tile, slot 1 of its last
+        [&](int t) { return a.ws + ((size_t)blockIdx.x * 2 + (t == sl.tf ? 0 : 1)) * (BN * 128); },
+        [&](int acc) { mbar_arrive(&p.tempty[acc]); });
   }
 
   __syncthreads();

@@ -1,0 +1,282 @@
+// Pair-CTA tensor-core GEMM for sm_103a (tcgen05 cta_group::2): Y = X W^T for
+// many token rows (the block-boundary refresh, batched blocks), where the
+// GEMM is bound by the tensor cores rather than by the weight stream.
+//
+// A cluster of two CTAs on two SMs computes one 256 x BN tile: weight rows
+// are the MMA's M dimension (256 = 128 per CTA), tokens its N dimension.
+// Each CTA stages its own 128 weight rows and HALF of the BN token rows; the
+// leader CTA (cluster rank 0) issues tcgen05.mma.cta_group::2, which reads
+// both CTAs' shared memory and leaves each CTA's 128 x BN accumulator in its
+// own TMEM.  Per SM this halves the token bytes staged and read by the tensor
+// cores per MMA against a one-CTA 128 x BN tile, for the same work.
+//
+// Synchronisation across the pair:
+//   full[s]    (leader) both CTAs' copies of stage s complete on it: the
+//              leader expects the bytes of both, the peer's copies use the
+//              cta_group::2 form that signals the leader's barrier;
+//   empty[s]   (each CTA) the leader's commit, multicast to both CTAs, frees
+//              stage s in both;
+//   tfull[a]   (each CTA) the leader's commit after a tile's last k-step,
+//              multicast: accumulator a is ready in both TMEMs;
+//   tempty[a]  (leader) the 128 epilogue threads of BOTH CTAs arrive (the
+//              peer's remotely) once they have read accumulator a.
+// Tiles are whole (no split-K); the epilogue is the one-CTA kernel's
+// (run_epilogue), each CTA finishing its own 128 rows x BN tokens.
+#pragma once
+#include "gemm_tc.cuh"
+
+namespace dinfer {
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory location in CTA `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// one warp of each CTA of the pair allocates, together
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier at this offset in both CTAs of the pair once the
+// tcgen05 operations issued so far by this thread completed.
+__device__ __forceinline__ void tc_commit_pair_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// mbar_wait for a barrier that the other CTA of the pair also arrives on
+// (acquire at cluster scope), bounded like mbar_wait
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+template <int BN>  // tokens per pair tile (the MMA's N); each CTA stages BN / 2
+struct Gemm2Cfg {
+  static constexpr int kStageA = 128 * 64 * 2;
+  static constexpr int kStageB = (BN / 2) * 64 * 2;
+  static constexpr int kStage = kStageA + kStageB;
+  static constexpr int kXchgBufs = 2;
+  static constexpr int kXchgFloats = kXchgBufs * 128 * 17;
+  static constexpr int kStages = (232448 - 1024 - kXchgFloats * 4 - 512) / kStage;
+  static constexpr int kSmem = 1024 + kStages * kStage + kXchgFloats * 4 + 512;
+  static constexpr int kTmemCols = 2 * BN;
+  static_assert(kSmem <= 232448, "pair GEMM shared memory above 227 KB");
+  static_assert(kTmemCols <= 512, "two accumulators of BN columns must fit in TMEM");
+};
+
+// Pair tile t -> this CTA's 128-row tile: weight tile pair t / m_tiles
+// (rows 256 p .. 256 p + 255; this CTA's half is 128-row tile 2 p + rank),
+// token tile t % m_tiles.
+template <int BN>
+__device__ __forceinline__ TileRef pair_tile(const GemmArgs& a, int t, int rank) {
+  TileRef r;
+  const int np = t / a.m_tiles;
+  r.mt = t - np * a.m_tiles;
+  r.nt = 2 * np + rank;
+  r.a_base = 0;
+  r.b_row = r.mt * BN;
+  r.m_lim = a.M;
+  r.out_base = 0;
+  return r;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
+  using C = Gemm2Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Pipe p;
+  p.stages = smem;
+  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xchg + C::kXchgFloats);
+  p.full = bars;
+  p.empty = bars + C::kStages;
+  p.tfull = bars + 2 * C::kStages;
+  p.tempty = p.tfull + 2;
+  p.drain = p.tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p.drain + 1);
+  volatile int* misc = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  p.abort_flag = misc;
+  p.rec = nullptr;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const GemmArgs& a = args;
+  const int rank = (int)cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int tiles = (a.n_tiles / 2) * a.m_tiles;
+  const int nseg = pair < tiles ? (tiles - pair + npairs - 1) / npairs : 0;  // tiles pair, pair + npairs, ...
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&p.full[s], 1);
+      mbar_init(&p.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p.tfull[i], 1);
+      mbar_init(&p.tempty[i], 2 * 128);
+    }
+    mbar_init(p.drain, 1);
+    misc[0] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.b);
+    prefetch_tmap(&maps.a[0]);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  // both CTAs' barriers are initialised and their TMEM allocated before any
+  // copy or arrive of one CTA can reach the other
+  cluster_barrier();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) pdl_trigger();
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer (both CTAs) ------------------------------
+    if (elect_one_sync()) {
+      const uint64_t pol_w = l2_policy_evict_normal();  // every weight tile is read by m_tiles pairs
+      const uint64_t pol_x = l2_policy_evict_last();
+      const uint32_t full0 = mapa_shared(smem_u32(p.full), 0);  // the leader's full barriers
+      const int b_half = rank * (BN / 2);
+      uint32_t it = 0;
+      bool waited = false;  // griddepcontrol.wait: before the first token tile
+      for (int j = 0; j < nseg && !*p.abort_flag; ++j) {
+        const TileRef tr = pair_tile<BN>(a, pair + j * npairs, rank);
+        bool ok = true;
+        for (int k = 0; k < a.k_tiles; ++k, ++it) {
+          const int s = it % C::kStages;
+          const uint32_t round = it / C::kStages;
+          if (!mbar_wait(&p.empty[s], (round & 1) ^ 1, p.abort_flag)) { ok = false; break; }
+          if (rank == 0) mbar_arrive_expect_tx(&p.full[s], 2 * C::kStage);
+          uint8_t* st = p.stages + s * C::kStage;
+          const uint32_t fb = full0 + s * 8;
+          // the weights do not depend on the preceding kernel
+          load_stage_a<true>(maps, a, st, fb, tr, k, pol_w);
+          if (!waited) {
+            pdl_wait();
+            waited = true;
+          }
+          tma_load_2d_to<true>(st + C::kStageA, &maps.b, fb, k * 64, tr.b_row + b_half, pol_x);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer (leader only) ------------------------------
+    if (rank == 0 && elect_one_sync()) {
+      constexpr uint32_t idesc = make_idesc_bf16(256, BN);
+      uint32_t it = 0;
+      for (int j = 0; j < nseg && !*p.abort_flag; ++j) {
+        const int acc = j & 1;
+        const uint32_t use = j >> 1;
+        if (!mbar_wait_cluster(&p.tempty[acc], (use & 1) ^ 1, p.abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int k = 0; k < a.k_tiles; ++k, ++it) {
+          const int s = it % C::kStages;
+          if (!mbar_wait_cluster(&p.full[s], (it / C::kStages) & 1, p.abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(p.stages + s * C::kStage);
+          const uint64_t ad = make_sw128_desc(sa);
+          const uint64_t bd = make_sw128_desc(sa + C::kStageA);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_pair_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
+                             (k > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_pair_both(&p.empty[s]);
+        }
+        if (!ok) break;
+        tc_commit_pair_both(&p.tfull[acc]);
+      }
+      tc_commit_pair(p.drain);
+      mbar_wait(p.drain, 0, p.abort_flag);
+    }
+  } else {
+    // ------------------------------ epilogue (both CTAs) ------------------------------
+    const uint32_t tempty0 = mapa_shared(smem_u32(p.tempty), 0);  // the leader's
+    run_epilogue<BN, C::kXchgBufs>(
+        a, p, tmem_base, xchg, warp, lane, nseg,
+        [&](int j, int& t, int& kb, int& ke, TileRef& tr) {
+          t = pair + j * npairs;
+          kb = 0;
+          ke = a.k_tiles;
+          tr = pair_tile<BN>(a, t, rank);
+        },
+        [&](int) { return (float*)nullptr; },  // whole tiles only
+        [&](int acc) {
+          if (rank == 0)
+            mbar_arrive(&p.tempty[acc]);
+          else
+            mbar_arrive_cluster(tempty0 + acc * 8);
+        });
+  }
+
+  __syncthreads();
+  if (*p.abort_flag && threadIdx.x == 0) record_timeout(a.status, kDiagGemm, 4, (uint32_t)rank);
+  // neither CTA leaves (or frees its TMEM) while the leader's products may
+  // still read the peer's shared memory or write its TMEM, or the peer's
+  // copies and arrives may still reach the leader's barriers
+  tc_fence_before();
+  cluster_barrier();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace dinfer
