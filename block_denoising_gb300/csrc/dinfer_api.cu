@@ -302,14 +302,43 @@ bool use_pair_gemm(int M, int n_tiles) {
   const long long per = (tiles + P - 1) / P;
   return tiles * 100 >= per * P * 85;
 }
-// maps.b: the token operand with 128-row boxes (each CTA stages half a tile)
-cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s) {
+// A residual GEMM (its split tiles finished by the following residual norm)
+// of many rows takes pair tiles in stream-K order whatever its tile count.
+bool use_pair_gemm_resid(int M, int n_tiles) { return pair_clusters() >= 1 && M >= 512 && n_tiles % 2 == 0; }
+// Pairs of a pair-GEMM launch: all co-resident pairs in stream-K mode (at
+// least k_tiles / 14 units each, so that at most 16 pairs share a tile),
+// else one per tile up to that count.
+int pair_grid(const GemmArgs& a, int stream_k) {
+  const int m_tiles = (a.M + kPairBN - 1) / kPairBN;
+  const long long tiles = (long long)(a.n_tiles / 2) * m_tiles;
+  const long long P = pair_clusters();
+  if (!stream_k) return (int)std::min(P, tiles);
+  const int k_tiles = a.K / 64;
+  const long long min_units = (k_tiles + 13) / 14;
+  return (int)std::max<long long>(1, std::min(P, tiles * k_tiles / min_units));
+}
+ResidPlan resid_plan_pair(const GemmArgs& a, const float* ws) {
+  ResidPlan p;
+  p.ws = ws;
+  p.BN = kPairBN;
+  p.m_tiles = (a.M + kPairBN - 1) / kPairBN;
+  p.n_tiles = a.n_tiles;
+  p.k_tiles = a.K / 64;
+  p.stream_k = 1;
+  p.grid = pair_grid(a, 1);
+  p.pair = 1;
+  return p;
+}
+// maps.b: the token operand with 128-row boxes (each CTA stages half a tile).
+// stream_k only for residual GEMMs (split tiles stay as partials).
+cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, int stream_k = 0) {
   a.m_tiles = (a.M + kPairBN - 1) / kPairBN;
   a.k_tiles = a.K / 64;
-  a.stream_k = 0;
-  const long long tiles = (long long)(a.n_tiles / 2) * a.m_tiles;
-  const int pairs = (int)std::min<long long>(pair_clusters(), tiles);
+  a.stream_k = stream_k;
+  const int pairs = pair_grid(a, stream_k);
   if (pairs < 1 || a.n_tiles % 2) return cudaErrorInvalidValue;
+  const long long units = (long long)(a.n_tiles / 2) * a.m_tiles * (stream_k ? a.k_tiles : 1);
+  if ((unsigned long long)units * (unsigned long long)pairs >= (1ull << 32)) return cudaErrorInvalidValue;
   a.grid = 2 * pairs;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.grid);
@@ -437,6 +466,7 @@ ResidPlan resid_plan(const GemmArgs& a, int BN, const float* ws, bool whole_only
   const GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN, whole_only);
   p.stream_k = gs.stream_k;
   p.grid = gs.grid;
+  p.pair = 0;
   return p;
 }
 
@@ -724,8 +754,13 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   // many rows: the QKV and gate/up projections on 256 x 256 pair-CTA tiles
   const bool pair_qkv = use_pair_gemm(rows, 3 * D / 128);
   const bool pair_gu = !d.n_experts && use_pair_gemm(rows, F / 64);
-  GemmMaps mx2{};
-  if ((pair_qkv || pair_gu) && !make_map(&mx2.b, c->xn, rows, D, kPairBN / 2))
+  // ... and the O and down projections on pair tiles in stream-K order
+  const bool pair_o = use_pair_gemm_resid(rows, D / 128);
+  const bool pair_down = !d.n_experts && use_pair_gemm_resid(rows, D / 128);
+  GemmMaps mx2{}, mo2{}, mact2{};
+  if (((pair_qkv || pair_gu) && !make_map(&mx2.b, c->xn, rows, D, kPairBN / 2)) ||
+      (pair_o && !make_map(&mo2.b, c->attn_o, rows, D, kPairBN / 2)) ||
+      (pair_down && !make_map(&mact2.b, c->act, rows, F, kPairBN / 2)))
     return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
   const int nthr = ((D / 16 + 31) / 32) * 32;  // fused-norm threads per row: whole warps
@@ -756,15 +791,15 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
                         c->st, s));
     // a4: O projection + residual, fused with the FFN norm
     {
-      GemmMaps m = mo;
+      GemmMaps m = pair_o ? mo2 : mo;
       m.a[0] = c->m_wo[l];
       GemmArgs a{};
       a.M = rows; a.N = D; a.K = D; a.n_tiles = D / 128; a.a_mode = A_SINGLE;
       a.resid = c->h; a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
-      CK(launch_gemm_tc(m, a, BNo, s, true, o_whole));
+      CK(pair_o ? launch_gemm_tc2(m, a, s, 1) : launch_gemm_tc(m, a, BNo, s, true, o_whole));
       CK(launch_resid_norm(rows, nthr, s, c->h, (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, D,
                            d.rms_eps, f.rows_per_seq, f.L, 0, 0, (const DevState*)c->st,
-                           resid_plan(a, BNo, c->gemm_ws, o_whole)));
+                           pair_o ? resid_plan_pair(a, c->gemm_ws) : resid_plan(a, BNo, c->gemm_ws, o_whole)));
     }
     const bool last = l + 1 == d.n_layers;
     const void* gn = last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0);
@@ -795,15 +830,15 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.out_bf16 = (__nv_bfloat16*)c->act; a.ldo = F;
       a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
       CK(pair_gu ? launch_gemm_tc2(m, a, s) : launch_gemm_tc(m, a, BN, s));
-      GemmMaps m2 = mact;
+      GemmMaps m2 = pair_down ? mact2 : mact;
       m2.a[0] = c->m_wd[l];
       GemmArgs b{};
       b.M = rows; b.N = D; b.K = F; b.n_tiles = D / 128; b.a_mode = A_SINGLE;
       b.resid = c->h; b.ws = c->gemm_ws; b.status = c->st; b.state = c->st;
-      CK(launch_gemm_tc(m2, b, BN, s, true));
+      CK(pair_down ? launch_gemm_tc2(m2, b, s, 1) : launch_gemm_tc(m2, b, BN, s, true));
       CK(launch_resid_norm(nrows, nthr, s, c->h, (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps,
                            f.B, f.rows_per_seq, gather, -f.row_off, (const DevState*)c->st,
-                           resid_plan(b, BN, c->gemm_ws)));
+                           pair_down ? resid_plan_pair(b, c->gemm_ws) : resid_plan(b, BN, c->gemm_ws)));
       CK(debug_copy_hidden(c, f, l, s));
     }
   }

@@ -774,6 +774,10 @@ struct ResidPlan {
   const float* ws;
   int m_tiles, n_tiles, k_tiles, grid, BN;
   int stream_k;  // 0: the GEMM owned whole tiles, nothing left to add
+  // 1: the pair-CTA GEMM: grid counts pairs, a unit is (pair tile, k-step)
+  // with pair tile (nt / 2) * m_tiles + mt, and the slots of CTA 2 c + nt % 2
+  // of pair c hold rows of 128-row tile nt
+  int pair;
 };
 
 // x = h[src] at the thread's 16 features (row-kernel layout from f0) plus the
@@ -794,11 +798,12 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
   const int m = (int)src;
   const int mt = m / rp.BN, ml = m - mt * rp.BN;
   const int nt = f0 / 128, fl = f0 - nt * 128;
-  const int t = nt * rp.m_tiles + mt;
+  const int t = rp.pair ? (nt >> 1) * rp.m_tiles + mt : nt * rp.m_tiles + mt;
+  const int rank = rp.pair ? (nt & 1) : 0;
   Sched sc;
   sc.G = rp.grid;
   sc.KT = rp.k_tiles;
-  sc.U = (unsigned)(rp.m_tiles * rp.n_tiles) * rp.k_tiles;
+  sc.U = (unsigned)(rp.m_tiles * (rp.pair ? rp.n_tiles / 2 : rp.n_tiles)) * rp.k_tiles;
   const unsigned tu0 = (unsigned)t * rp.k_tiles;
   const int c_first = rp.stream_k ? sc.owner(tu0) : 0;
   const int c_last = rp.stream_k ? sc.owner(tu0 + rp.k_tiles - 1) : 0;
@@ -810,7 +815,8 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
       const int cc = c0 + q;
       if (cc <= c_last) {
         const int w = ((unsigned)t == sc.start(cc) / sc.KT) ? 0 : 1;
-        const float* sp = rp.ws + ((size_t)cc * 2 + w) * (rp.BN * 128) + (size_t)ml * 128 + fl;
+        const size_t slot = rp.pair ? (size_t)(2 * cc + rank) * 2 + w : (size_t)cc * 2 + w;
+        const float* sp = rp.ws + slot * (rp.BN * 128) + (size_t)ml * 128 + fl;
 #pragma unroll
         for (int i = 0; i < 4; ++i) buf[q][i] = __ldcg(reinterpret_cast<const float4*>(sp + kRowGroupStride * i));
       }

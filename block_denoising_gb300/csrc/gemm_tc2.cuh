@@ -20,8 +20,12 @@
 //              multicast: accumulator a is ready in both TMEMs;
 //   tempty[a]  (leader) the 128 epilogue threads of BOTH CTAs arrive (the
 //              peer's remotely) once they have read accumulator a.
-// Tiles are whole (no split-K); the epilogue is the one-CTA kernel's
-// (run_epilogue), each CTA finishing its own 128 rows x BN tokens.
+// Work is dealt in whole tiles, or stream-K: the (pair tile, k-step) units
+// split evenly over the pairs, both CTAs of a pair taking the same units for
+// their own rows.  The epilogue is the one-CTA kernel's (run_epilogue), each
+// CTA finishing its own 128 rows x BN tokens; a split tile leaves
+// token-major fp32 partials in the CTA's two workspace slots, which only a
+// residual GEMM may do (the following residual norm adds them).
 #pragma once
 #include "gemm_tc.cuh"
 
@@ -157,7 +161,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int rank = (int)cluster_ctarank();
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int tiles = (a.n_tiles / 2) * a.m_tiles;
-  const int nseg = pair < tiles ? (tiles - pair + npairs - 1) / npairs : 0;  // tiles pair, pair + npairs, ...
+  SegList sl;
+  if (a.stream_k) {
+    Sched sc;
+    sc.G = npairs;
+    sc.KT = a.k_tiles;
+    sc.U = (unsigned)tiles * a.k_tiles;
+    sl.init(1, a.k_tiles, sc.start(pair), sc.start(pair + 1));
+  } else {
+    sl.init(0, a.k_tiles, pair, tiles, npairs);  // tiles pair, pair + npairs, ...
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -194,10 +207,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int b_half = rank * (BN / 2);
       uint32_t it = 0;
       bool waited = false;  // griddepcontrol.wait: before the first token tile
-      for (int j = 0; j < nseg && !*p.abort_flag; ++j) {
-        const TileRef tr = pair_tile<BN>(a, pair + j * npairs, rank);
+      for (int j = 0; j < sl.nseg && !*p.abort_flag; ++j) {
+        int t, kb, ke;
+        sl.seg(j, t, kb, ke);
+        const TileRef tr = pair_tile<BN>(a, t, rank);
         bool ok = true;
-        for (int k = 0; k < a.k_tiles; ++k, ++it) {
+        for (int k = kb; k < ke; ++k, ++it) {
           const int s = it % C::kStages;
           const uint32_t round = it / C::kStages;
           if (!mbar_wait(&p.empty[s], (round & 1) ^ 1, p.abort_flag)) { ok = false; break; }
@@ -220,14 +235,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (rank == 0 && elect_one_sync()) {
       constexpr uint32_t idesc = make_idesc_bf16(256, BN);
       uint32_t it = 0;
-      for (int j = 0; j < nseg && !*p.abort_flag; ++j) {
+      for (int j = 0; j < sl.nseg && !*p.abort_flag; ++j) {
+        int t, kb, ke;
+        sl.seg(j, t, kb, ke);
         const int acc = j & 1;
         const uint32_t use = j >> 1;
         if (!mbar_wait_cluster(&p.tempty[acc], (use & 1) ^ 1, p.abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
-        for (int k = 0; k < a.k_tiles; ++k, ++it) {
+        for (int k = kb; k < ke; ++k, ++it) {
           const int s = it % C::kStages;
           if (!mbar_wait_cluster(&p.full[s], (it / C::kStages) & 1, p.abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -237,7 +254,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc_mma_pair_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
-                             (k > 0 || kk > 0) ? 1u : 0u);
+                             (k > kb || kk > 0) ? 1u : 0u);
           tc_commit_pair_both(&p.empty[s]);
         }
         if (!ok) break;
@@ -250,14 +267,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------ epilogue (both CTAs) ------------------------------
     const uint32_t tempty0 = mapa_shared(smem_u32(p.tempty), 0);  // the leader's
     run_epilogue<BN, C::kXchgBufs>(
-        a, p, tmem_base, xchg, warp, lane, nseg,
+        a, p, tmem_base, xchg, warp, lane, sl.nseg,
         [&](int j, int& t, int& kb, int& ke, TileRef& tr) {
-          t = pair + j * npairs;
-          kb = 0;
-          ke = a.k_tiles;
+          sl.seg(j, t, kb, ke);
           tr = pair_tile<BN>(a, t, rank);
         },
-        [&](int) { return (float*)nullptr; },  // whole tiles only
+        // this CTA's slots: 0 its part of the pair's first tile, 1 of its last
+        [&](int t) { return a.ws + ((size_t)blockIdx.x * 2 + (t == sl.tf ? 0 : 1)) * (BN * 128); },
         [&](int acc) {
           if (rank == 0)
             mbar_arrive(&p.tempty[acc]);
