@@ -155,11 +155,11 @@ bool set_smem_attrs() {
   if (g_attrs_done[dev]) return true;
   bool ok = true;
   ok &= cudaFuncSetAttribute(gemm_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GemmCfg<64>::kSmem) == cudaSuccess;
+                             GemmKCfg<64>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GemmCfg<128>::kSmem) == cudaSuccess;
+                             GemmKCfg<128>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GemmCfg<256>::kSmem) == cudaSuccess;
+                             GemmKCfg<256>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(lmhead_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              LmCfg<64>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(lmhead_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -271,15 +271,15 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
   cudaError_t e = cudaSuccess;
   switch (BN) {
     case 64:
-      e = launchk(gemm_tc_kernel<64>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<64>::kSmem, s, 1, maps, a);
+      e = launchk(gemm_tc_kernel<64>, dim3(a.grid), dim3(kGemmThreads), GemmKCfg<64>::kSmem, s, 1, maps, a);
       if (e == cudaSuccess && fixup) e = launchk(splitk_fixup_kernel<64>, dim3(tiles * 4), dim3(128), 0, s, 1, a);
       break;
     case 128:
-      e = launchk(gemm_tc_kernel<128>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<128>::kSmem, s, 1, maps, a);
+      e = launchk(gemm_tc_kernel<128>, dim3(a.grid), dim3(kGemmThreads), GemmKCfg<128>::kSmem, s, 1, maps, a);
       if (e == cudaSuccess && fixup) e = launchk(splitk_fixup_kernel<128>, dim3(tiles * 8), dim3(128), 0, s, 1, a);
       break;
     default:
-      e = launchk(gemm_tc_kernel<256>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<256>::kSmem, s, 1, maps, a);
+      e = launchk(gemm_tc_kernel<256>, dim3(a.grid), dim3(kGemmThreads), GemmKCfg<256>::kSmem, s, 1, maps, a);
       if (e == cudaSuccess && fixup) e = launchk(splitk_fixup_kernel<256>, dim3(tiles * 16), dim3(128), 0, s, 1, a);
       break;
   }
@@ -371,11 +371,11 @@ cudaError_t launch_gemm_grouped(const GemmMaps& maps, GemmArgs a, int BN, cudaSt
   a.grid = num_sms();
   switch (BN) {
     case 64:
-      return launchk(gemm_tc_kernel<64>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<64>::kSmem, s, 1, maps, a);
+      return launchk(gemm_tc_kernel<64>, dim3(a.grid), dim3(kGemmThreads), GemmKCfg<64>::kSmem, s, 1, maps, a);
     case 128:
-      return launchk(gemm_tc_kernel<128>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<128>::kSmem, s, 1, maps, a);
+      return launchk(gemm_tc_kernel<128>, dim3(a.grid), dim3(kGemmThreads), GemmKCfg<128>::kSmem, s, 1, maps, a);
     default:
-      return launchk(gemm_tc_kernel<256>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<256>::kSmem, s, 1, maps, a);
+      return launchk(gemm_tc_kernel<256>, dim3(a.grid), dim3(kGemmThreads), GemmKCfg<256>::kSmem, s, 1, maps, a);
   }
 }
 
@@ -1800,7 +1800,7 @@ extern "C" dinfer_status dinfer_op_gemm_bf16_noalloc(const void* X, const void* 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // No partial tile must start at zero: every slot the fixup reads is written
   // by the GEMM launch of the same call.
-  CK(launchk(gemm_tc_kernel<BN>, dim3(a.grid), dim3(kGemmThreads), GemmCfg<BN>::kSmem, s, 1, m, a));
+  CK(launchk(gemm_tc_kernel<BN>, dim3(a.grid), dim3(kGemmThreads), GemmKCfg<BN>::kSmem, s, 1, m, a));
   if (a.stream_k) CK(launchk(splitk_fixup_kernel<BN>, dim3(a.n_tiles * 4), dim3(128), 0, s, 1, a));
   return DINFER_OK;
 }

@@ -24,6 +24,12 @@
 
 namespace dinfer {
 
+// (xr + i xi)(yr + i yi)
+__device__ __forceinline__ void cmulf(float xr, float xi, float yr, float yi, float& zr, float& zi) {
+  zr = fmaf(xr, yr, -xi * yi);
+  zi = fmaf(xr, yi, xi * yr);
+}
+
 enum AMode : int {
   A_SINGLE = 0,  // one weight map, 128-row boxes
   A_THREE = 1,   // three maps (wq, wk, wv) of a_rows rows each, 128-row boxes
@@ -120,8 +126,16 @@ constexpr int kGemmThreads = 192;
 // of a CTA: nine 16 KB weight tiles at 64 tokens).
 template <int BN>
 constexpr int gemm_default_stages() { return BN == 64 ? 9 : (BN == 128 ? 6 : 4); }
+// the GEMM kernel stages QKV outputs where the buffers fit beside its stages
+// and two exchange buffers
+template <int BN>
+constexpr int gemm_default_staged() {
+  return 1024 + gemm_default_stages<BN>() * (128 + BN) * 128 + 2 * 128 * 17 * 4 + 2 * 16 * 128 * 2 + 512 <= 232448;
+}
 
-template <int BN, int ST = gemm_default_stages<BN>()>
+// STG: the QKV epilogue stages its bf16 outputs in shared memory (two
+// 16-token x 128-row buffers) and stores whole 16-byte vectors.
+template <int BN, int ST = gemm_default_stages<BN>(), int STG = 0>
 struct GemmCfg {
   static constexpr int kStageA = 128 * 64 * 2;
   static constexpr int kStageB = BN * 64 * 2;
@@ -131,10 +145,14 @@ struct GemmCfg {
   // beside the stages (227 KB per CTA), else one
   static constexpr int kXchgBufs = (1024 + kStages * kStage + 2 * 128 * 17 * 4 + 512 <= 232448) ? 2 : 1;
   static constexpr int kXchgFloats = kXchgBufs * 128 * 17;
-  static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStage + kXchgFloats * 4 + 512;
+  static constexpr int kStageOutBytes = STG ? 2 * 16 * 128 * 2 : 0;
+  static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStage + kXchgFloats * 4 + kStageOutBytes + 512;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static_assert(kSmem <= 232448, "GEMM shared memory above 227 KB");
 };
+// the configuration gemm_tc_kernel<BN> runs with
+template <int BN>
+using GemmKCfg = GemmCfg<BN, gemm_default_stages<BN>(), gemm_default_staged<BN>()>;
 
 // ---------------------------------------------------------------------------
 // schedule: contiguous unit ranges per CTA
@@ -228,7 +246,8 @@ __device__ __forceinline__ void qkv_rope_fetch(const GemmArgs& a, int base_pos, 
 template <int BN>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16], int row, int nt, int m0,
                                                float* xchg, int m_lim, int out_base, bool sync_after,
-                                               const float (*rope)[16] = nullptr, int base_pos_in = -1) {
+                                               const float (*rope)[16] = nullptr, int base_pos_in = -1,
+                                               __nv_bfloat16* stage = nullptr) {
   if (a.q_out != nullptr) {
     // ---- QKV: RoPE pairs (i, i + 64) sit in rows row and row ^ 64 ----
     const int d = a.d_model;
@@ -255,6 +274,29 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
     const float sgn = row < 64 ? -1.f : 1.f;
 #pragma unroll
     for (int c = 0; c < 16; ++c) o[c] = (which == 2) ? v[c] : fmaf(sgn * part[c], sn[c], v[c] * cs[c]);
+    if (stage != nullptr) {
+      // stage the chunk as [16 tokens][128 features] bf16, then each thread
+      // stores two 16-byte pieces (8 features of one token): whole 256-byte
+      // rows per token instead of 2-byte stores 2 * d bytes apart
+#pragma unroll
+      for (int c = 0; c < 16; ++c) stage[c * 128 + row] = __float2bfloat16_rn(o[c]);
+      named_bar_sync(1, 128);
+      __nv_bfloat16* __restrict__ dst0 = (which == 0 ? a.q_out : (which == 1 ? a.k_cache : a.v_cache)) +
+                                         (nt * 128 - which * d);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int piece = row + h * 128;  // 16 tokens x 16 pieces
+        const int c = piece >> 4, f8 = (piece & 15) * 8;
+        const int m = m0 + c;
+        if (m < a.M) {
+          const int bi = m / a.rows_per_seq, r = m - bi * a.rows_per_seq;
+          const size_t orow = which == 0 ? (size_t)m : (size_t)bi * a.seq_len + base_pos + r;
+          *reinterpret_cast<uint4*>(dst0 + orow * d + f8) = *reinterpret_cast<const uint4*>(stage + c * 128 + f8);
+        }
+      }
+      if (sync_after) named_bar_sync(1, 128);
+      return;
+    }
     if (sync_after) named_bar_sync(1, 128);
     __nv_bfloat16* __restrict__ dst = (which == 0 ? a.q_out : (which == 1 ? a.k_cache : a.v_cache)) + nn;
     int bi = m0 / a.rows_per_seq;
@@ -518,15 +560,16 @@ __device__ __forceinline__ void run_mma(const SegList& sl, const Pipe& p, uint32
 }
 
 // Carve the shared memory of a GEMM CTA and initialise its barriers.
-template <int BN, int ST = gemm_default_stages<BN>()>
+template <int BN, int ST = gemm_default_stages<BN>(), int STG = 0>
 __device__ __forceinline__ Pipe setup_pipe(uint8_t* smem_raw, float*& xchg, uint32_t*& tmem_slot,
                                            volatile int*& misc) {
-  using C = GemmCfg<BN, ST>;
+  using C = GemmCfg<BN, ST, STG>;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Pipe p;
   p.stages = smem;
   xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xchg + C::kXchgFloats);
+  // [kStageOutBytes of QKV output staging after the exchange buffers]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xchg + C::kXchgFloats) + C::kStageOutBytes);
   p.full = bars;
   p.empty = bars + C::kStages;
   p.tfull = bars + 2 * C::kStages;
@@ -557,11 +600,12 @@ __device__ __forceinline__ Pipe setup_pipe(uint8_t* smem_raw, float*& xchg, uint
 // (tile t, k-steps [kb, ke), operands and outputs tr); a segment that is not
 // a whole tile leaves token-major fp32 partials at partial_slot(t);
 // release(acc) hands accumulator acc back to the MMA issuer.  NXB: exchange
-// buffers (see epilogue_chunk).
+// buffers (see epilogue_chunk); stage_out: two QKV output staging buffers
+// (NULL: QKV outputs are stored directly), used in turn with NXB == 2.
 template <int BN, int NXB, class SegFn, class SlotFn, class ReleaseFn>
 __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Pipe& p, uint32_t tmem_base, float* xchg,
-                                             int warp, int lane, int nseg, SegFn seg_tile, SlotFn partial_slot,
-                                             ReleaseFn release) {
+                                             __nv_bfloat16* stage_out, int warp, int lane, int nseg,
+                                             SegFn seg_tile, SlotFn partial_slot, ReleaseFn release) {
   pdl_wait();  // global writes only after the preceding kernel completed
   const int base_pos =
       a.q_out != nullptr ? (a.pos_from_state ? a.state->block_start : 0) + a.row_off : 0;
@@ -577,6 +621,14 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Pipe& p, u
     step_c = __ldg(a.rope_cos + 64 + (row & 63));
     step_s = __ldg(a.rope_sin + 64 + (row & 63));
   }
+  // rotations by 2, 4, 8 and 16 positions: a chunk's 16 factors come from
+  // its first one at most four products deep, the next chunk's first one
+  // from a single product
+  float p2c, p2s, p4c, p4s, p8c, p8s, p16c, p16s;
+  cmulf(step_c, step_s, step_c, step_s, p2c, p2s);
+  cmulf(p2c, p2s, p2c, p2s, p4c, p4s);
+  cmulf(p4c, p4s, p4c, p4s, p8c, p8s);
+  cmulf(p8c, p8s, p8c, p8s, p16c, p16s);
   int xb = 0;  // exchange buffer of the next pairing chunk
   for (int j = 0; j < nseg; ++j) {
     int t, kb, ke;
@@ -621,22 +673,41 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Pipe& p, u
         float v[16];
         tmem_ld16(tbase + c * 16, v);
         float rope[2][16];
+        if (rr + 16 <= a.rows_per_seq) {
+          // the chunk stays inside one sequence
+          rope[0][0] = rc;
+          rope[1][0] = rs;
+          cmulf(rc, rs, step_c, step_s, rope[0][1], rope[1][1]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          rope[0][i] = rc;
-          rope[1][i] = rs;
-          if (++rr == a.rows_per_seq) {
+          for (int i = 0; i < 2; ++i) cmulf(rope[0][i], rope[1][i], p2c, p2s, rope[0][2 + i], rope[1][2 + i]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) cmulf(rope[0][i], rope[1][i], p4c, p4s, rope[0][4 + i], rope[1][4 + i]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cmulf(rope[0][i], rope[1][i], p8c, p8s, rope[0][8 + i], rope[1][8 + i]);
+          rr += 16;
+          if (rr == a.rows_per_seq) {
             rr = 0;
             rc = rc0;
             rs = rs0;
           } else {
-            const float t = fmaf(rc, step_c, -rs * step_s);
-            rs = fmaf(rs, step_c, rc * step_s);
-            rc = t;
+            cmulf(rope[0][0], rope[1][0], p16c, p16s, rc, rs);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            rope[0][i] = rc;
+            rope[1][i] = rs;
+            if (++rr == a.rows_per_seq) {
+              rr = 0;
+              rc = rc0;
+              rs = rs0;
+            } else {
+              cmulf(rope[0][i], rope[1][i], step_c, step_s, rc, rs);
+            }
           }
         }
         epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg + xb * (128 * 17), tr.m_lim, tr.out_base,
-                           NXB == 1, rope, base_pos);
+                           NXB == 1, rope, base_pos, stage_out ? stage_out + xb * (16 * 128) : nullptr);
         xb ^= NXB - 1;
       }
     } else if (a.resid != nullptr) {
@@ -671,12 +742,14 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Pipe& p, u
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
-  using C = GemmCfg<BN>;
+  using C = GemmKCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   float* xchg;
   uint32_t* tmem_slot;
   volatile int* misc;
-  const Pipe p = setup_pipe<BN>(smem_raw, xchg, tmem_slot, misc);
+  const Pipe p = setup_pipe<BN, C::kStages, C::kStageOutBytes ? 1 : 0>(smem_raw, xchg, tmem_slot, misc);
+  __nv_bfloat16* stage_out =
+      C::kStageOutBytes ? reinterpret_cast<__nv_bfloat16*>(xchg + C::kXchgFloats) : nullptr;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -714,7 +787,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (elect_one_sync()) run_mma<BN>(sl, p, tmem_base);
   } else {
     run_epilogue<BN, C::kXchgBufs>(
-        a, p, tmem_base, xchg, warp, lane, sl.nseg,
+        a, p, tmem_base, xchg, stage_out, warp, lane, sl.nseg,
         [&](int j, int& t, int& kb, int& ke, TileRef& tr) {
           sl.seg(j, t, kb, ke);
           tr = decode_tile<BN>(a, t);

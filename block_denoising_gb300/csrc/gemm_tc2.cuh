@@ -112,8 +112,9 @@ struct Gemm2Cfg {
   static constexpr int kStage = kStageA + kStageB;
   static constexpr int kXchgBufs = 2;
   static constexpr int kXchgFloats = kXchgBufs * 128 * 17;
-  static constexpr int kStages = (232448 - 1024 - kXchgFloats * 4 - 512) / kStage;
-  static constexpr int kSmem = 1024 + kStages * kStage + kXchgFloats * 4 + 512;
+  static constexpr int kStageOutBytes = 2 * 16 * 128 * 2;  // QKV output staging (see epilogue_chunk)
+  static constexpr int kStages = (232448 - 1024 - kXchgFloats * 4 - kStageOutBytes - 512) / kStage;
+  static constexpr int kSmem = 1024 + kStages * kStage + kXchgFloats * 4 + kStageOutBytes + 512;
   static constexpr int kTmemCols = 2 * BN;
   static_assert(kSmem <= 232448, "pair GEMM shared memory above 227 KB");
   static_assert(kTmemCols <= 512, "two accumulators of BN columns must fit in TMEM");
@@ -144,7 +145,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   Pipe p;
   p.stages = smem;
   float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xchg + C::kXchgFloats);
+  __nv_bfloat16* stage_out = reinterpret_cast<__nv_bfloat16*>(xchg + C::kXchgFloats);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(stage_out) + C::kStageOutBytes);
   p.full = bars;
   p.empty = bars + C::kStages;
   p.tfull = bars + 2 * C::kStages;
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------ epilogue (both CTAs) ------------------------------
     const uint32_t tempty0 = mapa_shared(smem_u32(p.tempty), 0);  // the leader's
     run_epilogue<BN, C::kXchgBufs>(
-        a, p, tmem_base, xchg, warp, lane, sl.nseg,
+        a, p, tmem_base, xchg, stage_out, warp, lane, sl.nseg,
         [&](int j, int& t, int& kb, int& ke, TileRef& tr) {
           sl.seg(j, t, kb, ke);
           tr = pair_tile<BN>(a, t, rank);
