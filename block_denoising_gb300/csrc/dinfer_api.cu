@@ -302,9 +302,12 @@ bool use_pair_gemm(int M, int n_tiles) {
   const long long per = (tiles + P - 1) / P;
   return tiles * 100 >= per * P * 85;
 }
-// A residual GEMM (its split tiles finished by the following residual norm)
-// of many rows takes pair tiles in stream-K order whatever its tile count.
-bool use_pair_gemm_resid(int M, int n_tiles) { return pair_clusters() >= 1 && M >= 512 && n_tiles % 2 == 0; }
+// A GEMM of enough rows to be bound by the tensor cores (>= 384: the time of
+// its MMAs at ~1.8 PFLOP/s exceeds that of reading its weights once) takes
+// pair tiles in stream-K order whatever its tile count; its split tiles are
+// finished by the following residual norm (residual GEMMs) or by
+// splitk_fixup_pair_kernel.
+bool use_pair_gemm_sk(int M, int n_tiles) { return pair_clusters() >= 1 && M >= 384 && n_tiles % 2 == 0; }
 // Pairs of a pair-GEMM launch: all co-resident pairs in stream-K mode (at
 // least k_tiles / 14 units each, so that at most 16 pairs share a tile),
 // else one per tile up to that count.
@@ -340,6 +343,7 @@ cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, in
   const long long units = (long long)(a.n_tiles / 2) * a.m_tiles * (stream_k ? a.k_tiles : 1);
   if ((unsigned long long)units * (unsigned long long)pairs >= (1ull << 32)) return cudaErrorInvalidValue;
   a.grid = 2 * pairs;
+  const long long tiles = (long long)(a.n_tiles / 2) * a.m_tiles;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kGemmThreads);
@@ -359,7 +363,11 @@ cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, in
   ++n;
   cfg.attrs = at;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<kPairBN>, maps, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<kPairBN>, maps, a);
+  if (e == cudaSuccess && stream_k && a.resid == nullptr)
+    e = launchk(splitk_fixup_pair_kernel<kPairBN>, dim3((unsigned)(tiles * 2 * (kPairBN / 16))), dim3(128), 0, s, 1,
+                a);
+  return e;
 }
 
 // Grouped (MoE expert) GEMM: persistent grid, tiles from the device tables.
@@ -751,12 +759,15 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BNo) ||
       (!d.n_experts && !make_map(&mact.b, c->act, rows, F, BN)))
     return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
-  // many rows: the QKV and gate/up projections on 256 x 256 pair-CTA tiles
-  const bool pair_qkv = use_pair_gemm(rows, 3 * D / 128);
-  const bool pair_gu = !d.n_experts && use_pair_gemm(rows, F / 64);
-  // ... and the O and down projections on pair tiles in stream-K order
-  const bool pair_o = use_pair_gemm_resid(rows, D / 128);
-  const bool pair_down = !d.n_experts && use_pair_gemm_resid(rows, D / 128);
+  // many rows: every projection on 256 x 256 pair-CTA tiles; QKV and gate/up
+  // in whole tiles where they keep the pairs busy, else (as the O and down
+  // projections) in stream-K order
+  const bool pair_qkv = use_pair_gemm_sk(rows, 3 * D / 128);
+  const int sk_qkv = pair_qkv && !use_pair_gemm(rows, 3 * D / 128);
+  const bool pair_gu = !d.n_experts && use_pair_gemm_sk(rows, F / 64);
+  const int sk_gu = pair_gu && !use_pair_gemm(rows, F / 64);
+  const bool pair_o = use_pair_gemm_sk(rows, D / 128);
+  const bool pair_down = !d.n_experts && use_pair_gemm_sk(rows, D / 128);
   GemmMaps mx2{}, mo2{}, mact2{};
   if (((pair_qkv || pair_gu) && !make_map(&mx2.b, c->xn, rows, D, kPairBN / 2)) ||
       (pair_o && !make_map(&mo2.b, c->attn_o, rows, D, kPairBN / 2)) ||
@@ -784,7 +795,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.rows_per_seq = f.rows_per_seq; a.seq_len = f.L; a.pos_from_state = f.pos_from_state;
       a.row_off = f.row_off;
       a.state = c->st; a.ws = c->gemm_ws; a.status = c->st;
-      CK(pair_qkv ? launch_gemm_tc2(m, a, s) : launch_gemm_tc(m, a, BN, s));
+      CK(pair_qkv ? launch_gemm_tc2(m, a, s, sk_qkv) : launch_gemm_tc(m, a, BN, s));
     }
     // a3: attention over the dual cache
     CK(launch_attention(c->q, c->kc_layer(l), c->vc_layer(l), c->attn_o, f.batch, f.rows_per_seq, H, f.L, ap,
@@ -829,7 +840,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.M = rows; a.N = F; a.K = D; a.n_tiles = F / 64; a.a_mode = A_PAIR;
       a.out_bf16 = (__nv_bfloat16*)c->act; a.ldo = F;
       a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
-      CK(pair_gu ? launch_gemm_tc2(m, a, s) : launch_gemm_tc(m, a, BN, s));
+      CK(pair_gu ? launch_gemm_tc2(m, a, s, sk_gu) : launch_gemm_tc(m, a, BN, s));
       GemmMaps m2 = pair_down ? mact2 : mact;
       m2.a[0] = c->m_wd[l];
       GemmArgs b{};
@@ -1622,7 +1633,8 @@ dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_
   const int BN = bn_for_rows(M);
   if ((size_t)((M + BN - 1) / BN) * (N / 128) * 4 > kOpTicketBytes) return fail(c, DINFER_EINVAL, "too many tiles");
   if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
-  const bool pair = use_pair_gemm(M, N / 128);
+  const bool pair = use_pair_gemm_sk(M, N / 128);
+  const int pair_sk = pair && !use_pair_gemm(M, N / 128);
   GemmMaps m{};
   if (!make_map(&m.a[0], W, N, K, 128) || !make_map(&m.b, X, M, K, pair ? kPairBN / 2 : BN))
     return fail(c, DINFER_EINVAL, "tensor map encoding failed (alignment?)");
@@ -1631,7 +1643,7 @@ dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_
   a.out_f32 = Y; a.ldo = N;
   a.ws = reinterpret_cast<float*>(o.data); a.status = o.st; a.state = o.st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  CK(pair ? launch_gemm_tc2(m, a, s) : launch_gemm_tc(m, a, BN, s));
+  CK(pair ? launch_gemm_tc2(m, a, s, pair_sk) : launch_gemm_tc(m, a, BN, s));
   return DINFER_OK;
 }
 

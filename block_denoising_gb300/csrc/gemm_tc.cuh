@@ -843,13 +843,34 @@ __global__ void __launch_bounds__(128) splitk_fixup_kernel(const GemmArgs a) {
 // layout (one weight tile of 128 features per 8 threads):
 //   h[src] += sum of the partials of every shared tile, in CTA order;
 //   out[r] = bf16(h[src] / sqrt(mean(h[src]^2) + eps) * g).
+// Pair-GEMM tile order: pair tile t -> (weight pair tile np, token tile mt).
+// Token tiles go in groups of kPairGroupM, each group swept weight-tile
+// major, so that the ~76 pairs running at once read a few weight tiles and at
+// most kPairGroupM token tiles (a few tens of MB, inside L2) whatever the
+// token count; with <= kPairGroupM token tiles this is t = np * m_tiles + mt.
+constexpr int kPairGroupM = 8;
+__host__ __device__ __forceinline__ void pair_tile_coords(int t, int m_tiles, int np_tiles, int& np, int& mt) {
+  const int per_group = kPairGroupM * np_tiles;
+  const int g = t / per_group;
+  const int w = t - g * per_group;
+  const int m0 = g * kPairGroupM;
+  const int gm = min(kPairGroupM, m_tiles - m0);
+  np = w / gm;
+  mt = m0 + (w - np * gm);
+}
+__host__ __device__ __forceinline__ int pair_tile_index(int np, int mt, int m_tiles, int np_tiles) {
+  const int g = mt / kPairGroupM, m0 = g * kPairGroupM;
+  const int gm = min(kPairGroupM, m_tiles - m0);
+  return g * kPairGroupM * np_tiles + np * gm + (mt - m0);
+}
+
 struct ResidPlan {
   const float* ws;
   int m_tiles, n_tiles, k_tiles, grid, BN;
   int stream_k;  // 0: the GEMM owned whole tiles, nothing left to add
   // 1: the pair-CTA GEMM: grid counts pairs, a unit is (pair tile, k-step)
-  // with pair tile (nt / 2) * m_tiles + mt, and the slots of CTA 2 c + nt % 2
-  // of pair c hold rows of 128-row tile nt
+  // with pair tile pair_tile_index(nt / 2, mt), and the slots of CTA
+  // 2 c + nt % 2 of pair c hold rows of 128-row tile nt
   int pair;
 };
 
@@ -871,7 +892,7 @@ __device__ __forceinline__ void resid_gather16(float* __restrict__ h, size_t src
   const int m = (int)src;
   const int mt = m / rp.BN, ml = m - mt * rp.BN;
   const int nt = f0 / 128, fl = f0 - nt * 128;
-  const int t = rp.pair ? (nt >> 1) * rp.m_tiles + mt : nt * rp.m_tiles + mt;
+  const int t = rp.pair ? pair_tile_index(nt >> 1, mt, rp.m_tiles, rp.n_tiles / 2) : nt * rp.m_tiles + mt;
   const int rank = rp.pair ? (nt & 1) : 0;
   Sched sc;
   sc.G = rp.grid;

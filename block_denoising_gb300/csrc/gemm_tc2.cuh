@@ -24,8 +24,9 @@
 // split evenly over the pairs, both CTAs of a pair taking the same units for
 // their own rows.  The epilogue is the one-CTA kernel's (run_epilogue), each
 // CTA finishing its own 128 rows x BN tokens; a split tile leaves
-// token-major fp32 partials in the CTA's two workspace slots, which only a
-// residual GEMM may do (the following residual norm adds them).
+// token-major fp32 partials in the CTA's two workspace slots, which the
+// following residual norm adds (residual GEMMs) or splitk_fixup_pair_kernel
+// sums and finishes with the same epilogue.
 #pragma once
 #include "gemm_tc.cuh"
 
@@ -120,14 +121,15 @@ struct Gemm2Cfg {
   static_assert(kTmemCols <= 512, "two accumulators of BN columns must fit in TMEM");
 };
 
-// Pair tile t -> this CTA's 128-row tile: weight tile pair t / m_tiles
-// (rows 256 p .. 256 p + 255; this CTA's half is 128-row tile 2 p + rank),
-// token tile t % m_tiles.
+// Pair tile t -> this CTA's 128-row tile of weight pair tile np (rows
+// 256 np .. 256 np + 255; this CTA's half is 128-row tile 2 np + rank) and
+// token tile mt (pair_tile_coords: the pairs running at once share a few of
+// each through L2).
 template <int BN>
 __device__ __forceinline__ TileRef pair_tile(const GemmArgs& a, int t, int rank) {
   TileRef r;
-  const int np = t / a.m_tiles;
-  r.mt = t - np * a.m_tiles;
+  int np;
+  pair_tile_coords(t, a.m_tiles, a.n_tiles / 2, np, r.mt);
   r.nt = 2 * np + rank;
   r.a_base = 0;
   r.b_row = r.mt * BN;
@@ -295,6 +297,58 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, C::kTmemCols);
   }
+}
+
+// Split-K fixup of the pair GEMM: block = (pair tile, CTA rank, 16-token
+// chunk), 128 threads = the rows of that CTA's half.  Sums, in pair order,
+// the partial slots of the pairs whose unit ranges overlap the tile (slots of
+// CTA 2 c + rank of pair c), then applies the GEMM's epilogue.  Tiles owned
+// whole by one pair were finished by it.
+template <int BN>
+__global__ void __launch_bounds__(128) splitk_fixup_pair_kernel(const GemmArgs a) {
+  __shared__ float xchg[128 * 17];
+  pdl_wait();
+  constexpr int chunks = BN / 16;
+  const int c = blockIdx.x % chunks;
+  const int half = blockIdx.x / chunks;
+  const int rank = half & 1, tp = half >> 1;
+  const int tiles = (a.n_tiles / 2) * a.m_tiles;
+  Sched sc;
+  sc.G = a.grid / 2;
+  sc.KT = a.k_tiles;
+  sc.U = (unsigned)tiles * a.k_tiles;
+  const unsigned tu0 = (unsigned)tp * a.k_tiles;
+  const int c_first = sc.owner(tu0), c_last = sc.owner(tu0 + a.k_tiles - 1);
+  if (c_first == c_last) {  // whole tile: done by the GEMM
+    pdl_trigger();
+    return;
+  }
+  const int row = threadIdx.x;
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = 0.f;
+#pragma unroll 1
+  for (int cc = c_first; cc <= c_last; cc += 2) {
+    float buf[2][16];
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (cc + x <= c_last) {
+        const int w = ((unsigned)tp == sc.start(cc + x) / sc.KT) ? 0 : 1;
+        const size_t slot = (size_t)(2 * (cc + x) + rank) * 2 + w;
+        const float* src = a.ws + slot * (BN * 128) + (size_t)(c * 16) * 128 + row;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) buf[x][i] = __ldcg(src + (size_t)i * 128);
+      }
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (cc + x <= c_last)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] += buf[x][i];
+  }
+  int np, mt;
+  pair_tile_coords(tp, a.m_tiles, a.n_tiles / 2, np, mt);
+  epilogue_chunk<BN>(a, v, row, 2 * np + rank, mt * BN + c * 16, xchg, a.M, 0, false);
+  pdl_trigger();
 }
 
 }  // namespace dinfer
