@@ -485,7 +485,7 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
     flops = 2.0 * M * N * K
     ach = flops / dt / 1e12
     rw = NCU_DRAM_BYTES.get((M, N, K))
-    return {"bound": "tensor", "kernel": f"gemm_tc_kernel<256> (refresh GEMM {M}x{N}x{K}, fp32 out)",
+    return {"bound": "tensor", "kernel": f"gemm_tc2_kernel<256> (pair-CTA tiles; refresh GEMM {M}x{N}x{K}, fp32 out)",
             "achieved": ach, "peak": peak_tflops, "peak_kind": "measured burst (kernel timed alone)",
             "unit": "TFLOP/s", "frac": ach / peak_tflops,
             "traffic": None if rw is None else rw[0] + rw[1], "traffic_unit": "DRAM bytes per launch (ncu)",
@@ -495,11 +495,11 @@ def gemm_roofline(cfg, run, dinfer, stream, peak_tflops):
 # DRAM bytes (read, write) of one launch of the dominant kernel, from
 #   python bench.py --profile gemm --gemm 1536 24576 4096 &&
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
-#       --profile-from-start off -k regex:gemm_tc -c 1 python bench.py --profile gemm --gemm 1536 24576 4096
-# on a GB300, taken with the current gemm_tc_kernel (a change to that kernel
+#       --profile-from-start off -k regex:gemm_tc2 -c 1 python bench.py --profile gemm --gemm 1536 24576 4096
+# on a GB300, taken with the current gemm_tc2_kernel (a change to that kernel
 # removes the entry until it is captured again).
 NCU_DRAM_BYTES = {
-    (1536, 24576, 4096): (214055936, 115359488),
+    (1536, 24576, 4096): (215467776, 119083776),
 }
 
 

@@ -247,7 +247,7 @@ template <int BN>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16], int row, int nt, int m0,
                                                float* xchg, int m_lim, int out_base, bool sync_after,
                                                const float (*rope)[16] = nullptr, int base_pos_in = -1,
-                                               __nv_bfloat16* stage = nullptr) {
+                                               __nv_bfloat16* stage = nullptr, bool stage_f32 = false) {
   if (a.q_out != nullptr) {
     // ---- QKV: RoPE pairs (i, i + 64) sit in rows row and row ^ 64 ----
     const int d = a.d_model;
@@ -338,6 +338,24 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, float (&v)[16]
       for (int i = 0; i < 8; ++i)
         if (mh + i < m_lim) a.out_bf16[(size_t)(out_base + mh + i) * a.ldo + jf] = __float2bfloat16_rn(o[i]);
     }
+  } else if (stage_f32 && a.resid == nullptr && a.out_bf16 == nullptr) {
+    // plain fp32 output: stage the chunk as [16 tokens][128 rows] in xchg
+    // (all 128 threads take part in the barrier), then each thread stores
+    // four 16-byte pieces -- whole 512-byte token rows
+    float* st = xchg;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) st[c * 128 + row] = v[c];
+    named_bar_sync(1, 128);
+    const int n0 = nt * 128;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int piece = row + h * 128;  // 16 tokens x 32 pieces
+      const int c = piece >> 5, f4 = (piece & 31) * 4;
+      if (m0 + c < m_lim && n0 + f4 < a.N)
+        *reinterpret_cast<float4*>(a.out_f32 + (size_t)(out_base + m0 + c) * a.ldo + n0 + f4) =
+            *reinterpret_cast<const float4*>(st + c * 128 + f4);
+    }
+    if (sync_after) named_bar_sync(1, 128);
   } else {
     const int n = nt * 128 + row;
     if (n < a.N) {
@@ -730,7 +748,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Pipe& p, u
         float v[16];
         tmem_ld16(tbase + c * 16, v);
         epilogue_chunk<BN>(a, v, row, tr.nt, tr.mt * BN + c * 16, xchg + xb * (128 * 17), tr.m_lim, tr.out_base,
-                           NXB == 1);
+                           NXB == 1, nullptr, -1, nullptr, stage_out != nullptr && NXB == 2);
         xb ^= NXB - 1;
       }
     }
