@@ -27,7 +27,12 @@ size_t dinfer_op_workspace_bytes(void);
 /* Y[m, n] = sum_k X[m, k] W[n, k]  (bf16 inputs, fp32 accumulate and output).
  * X [M, K] bf16, W [N, K] bf16 (row-major, 16-byte aligned), Y [M, N] fp32.
  * K % 64 == 0, N % 128 == 0, 1 <= M <= 1 << 20.  The tensor-core GEMM
- * (tcgen05, TMA, stream-K) used for every projection of the model. */
+ * (tcgen05, TMA, stream-K) used for every projection of the model: one-CTA
+ * tiles of 128 weight rows for few rows (weight streaming), pair-CTA tiles
+ * (tcgen05 cta_group::2, 256 weight rows x 256 rows per 2-CTA cluster) from
+ * 384 rows on (tensor-bound), as the model's forward chooses them; the sum
+ * order over k differs between the two, the results agree within fp32
+ * accumulation rounding. */
 dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_t M, int32_t N, int32_t K,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
