@@ -170,6 +170,8 @@ bool set_smem_attrs() {
         cudaSuccess;
   ok &= cudaFuncSetAttribute(gemm_tc2_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Gemm2Cfg<256>::kSmem) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(gemm_tc2_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Gemm2Cfg<128>::kSmem) == cudaSuccess;
   {
     // how many pairs run at once: clusters live inside one GPC, so SMs of a
     // GPC with an odd count of free SMs may stay out
@@ -286,33 +288,42 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
   return e;
 }
 
-// Pair-CTA GEMM (gemm_tc2_kernel): 256 weight rows x 256 tokens per tile,
-// whole tiles dealt round-robin over the co-resident pairs.  It pays where
-// the GEMM is tensor-bound (many token rows) and its tiles keep >= 85% of the
-// pairs busy; otherwise the one-CTA kernel (stream-K where needed) runs.
+// Pair-CTA GEMM (gemm_tc2_kernel): 256 weight rows x 256 (or 128) tokens per
+// tile on a 2-CTA cluster.  It pays where the GEMM is bound by the tensor
+// cores (>= 384 token rows: the time of its MMAs at ~1.8 PFLOP/s exceeds that
+// of reading its weights once); below that the one-CTA kernel streams the
+// weights.  Per GEMM: whole 256-token tiles dealt round-robin over the
+// co-resident pairs when they keep >= 85% of the pairs busy; else 256-token
+// tiles in stream-K order for a residual GEMM (the following residual norm
+// adds its split tiles at little cost); else, for the others, whole 128-token
+// tiles when those keep >= 80% of the pairs busy (no fixup launch), and
+// stream-K with splitk_fixup_pair_kernel otherwise.  (Measured at 1536 rows:
+// stream-K beats whole 128-token tiles for the O and down projections; at
+// 512 rows whole 128-token tiles beat stream-K + fixup for QKV and gate/up.)
 constexpr int kPairBN = 256;
+enum PairMode { PAIR_NONE = 0, PAIR_W256, PAIR_W128, PAIR_SK };
 int pair_clusters() {
   set_smem_attrs();
   return g_pair_clusters[current_device()];
 }
-bool use_pair_gemm(int M, int n_tiles) {
-  const int P = pair_clusters();
-  if (P < 1 || M < 512 || n_tiles % 2) return false;
-  const long long tiles = (long long)(n_tiles / 2) * ((M + kPairBN - 1) / kPairBN);
+bool pair_balanced(int M, int n_tiles, int bn, int pct) {
+  const long long P = pair_clusters();
+  const long long tiles = (long long)(n_tiles / 2) * ((M + bn - 1) / bn);
   const long long per = (tiles + P - 1) / P;
-  return tiles * 100 >= per * P * 85;
+  return tiles * 100 >= per * P * pct;
 }
-// A GEMM of enough rows to be bound by the tensor cores (>= 384: the time of
-// its MMAs at ~1.8 PFLOP/s exceeds that of reading its weights once) takes
-// pair tiles in stream-K order whatever its tile count; its split tiles are
-// finished by the following residual norm (residual GEMMs) or by
-// splitk_fixup_pair_kernel.
-bool use_pair_gemm_sk(int M, int n_tiles) { return pair_clusters() >= 1 && M >= 384 && n_tiles % 2 == 0; }
+PairMode pair_mode(int M, int n_tiles, bool resid) {
+  if (pair_clusters() < 1 || M < 384 || n_tiles % 2) return PAIR_NONE;
+  if (pair_balanced(M, n_tiles, 256, 85)) return PAIR_W256;
+  if (!resid && pair_balanced(M, n_tiles, 128, 80)) return PAIR_W128;
+  return PAIR_SK;
+}
+int pair_bn(PairMode pm) { return pm == PAIR_W128 ? 128 : 256; }
 // Pairs of a pair-GEMM launch: all co-resident pairs in stream-K mode (at
 // least k_tiles / 14 units each, so that at most 16 pairs share a tile),
 // else one per tile up to that count.
-int pair_grid(const GemmArgs& a, int stream_k) {
-  const int m_tiles = (a.M + kPairBN - 1) / kPairBN;
+int pair_grid(const GemmArgs& a, int stream_k, int bn = kPairBN) {
+  const int m_tiles = (a.M + bn - 1) / bn;
   const long long tiles = (long long)(a.n_tiles / 2) * m_tiles;
   const long long P = pair_clusters();
   if (!stream_k) return (int)std::min(P, tiles);
@@ -320,7 +331,21 @@ int pair_grid(const GemmArgs& a, int stream_k) {
   const long long min_units = (k_tiles + 13) / 14;
   return (int)std::max<long long>(1, std::min(P, tiles * k_tiles / min_units));
 }
-ResidPlan resid_plan_pair(const GemmArgs& a, const float* ws) {
+// the residual norm's view of a pair GEMM: whole tiles were added to h by
+// the GEMM; stream-K leaves split tiles in the pairs' slots
+ResidPlan resid_plan_pair(const GemmArgs& a, const float* ws, PairMode pm) {
+  if (pm != PAIR_SK) {
+    ResidPlan w{};
+    w.ws = ws;
+    w.BN = pair_bn(pm);
+    w.m_tiles = (a.M + w.BN - 1) / w.BN;
+    w.n_tiles = a.n_tiles;
+    w.k_tiles = a.K / 64;
+    w.stream_k = 0;
+    w.grid = 1;
+    w.pair = 1;
+    return w;
+  }
   ResidPlan p;
   p.ws = ws;
   p.BN = kPairBN;
@@ -332,13 +357,15 @@ ResidPlan resid_plan_pair(const GemmArgs& a, const float* ws) {
   p.pair = 1;
   return p;
 }
-// maps.b: the token operand with 128-row boxes (each CTA stages half a tile).
-// stream_k only for residual GEMMs (split tiles stay as partials).
-cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, int stream_k = 0) {
-  a.m_tiles = (a.M + kPairBN - 1) / kPairBN;
+// maps.b: the token operand with pair_bn(pm) / 2-row boxes (each CTA stages
+// half a tile).
+cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, PairMode pm) {
+  const int bn = pair_bn(pm);
+  const int stream_k = pm == PAIR_SK;
+  a.m_tiles = (a.M + bn - 1) / bn;
   a.k_tiles = a.K / 64;
   a.stream_k = stream_k;
-  const int pairs = pair_grid(a, stream_k);
+  const int pairs = pair_grid(a, stream_k, bn);
   if (pairs < 1 || a.n_tiles % 2) return cudaErrorInvalidValue;
   const long long units = (long long)(a.n_tiles / 2) * a.m_tiles * (stream_k ? a.k_tiles : 1);
   if ((unsigned long long)units * (unsigned long long)pairs >= (1ull << 32)) return cudaErrorInvalidValue;
@@ -347,7 +374,7 @@ cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, in
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = Gemm2Cfg<kPairBN>::kSmem;
+  cfg.dynamicSmemBytes = bn == 128 ? Gemm2Cfg<128>::kSmem : Gemm2Cfg<256>::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute at[2];
   int n = 0;
@@ -363,7 +390,8 @@ cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, in
   ++n;
   cfg.attrs = at;
   cfg.numAttrs = n;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<kPairBN>, maps, a);
+  cudaError_t e = bn == 128 ? cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<128>, maps, a)
+                            : cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<256>, maps, a);
   if (e == cudaSuccess && stream_k && a.resid == nullptr)
     e = launchk(splitk_fixup_pair_kernel<kPairBN>, dim3((unsigned)(tiles * 2 * (kPairBN / 16))), dim3(128), 0, s, 1,
                 a);
@@ -759,19 +787,18 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   if (!make_map(&mx.b, c->xn, rows, D, BN) || !make_map(&mo.b, c->attn_o, rows, D, BNo) ||
       (!d.n_experts && !make_map(&mact.b, c->act, rows, F, BN)))
     return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
-  // many rows: every projection on 256 x 256 pair-CTA tiles; QKV and gate/up
-  // in whole tiles where they keep the pairs busy, else (as the O and down
-  // projections) in stream-K order
-  const bool pair_qkv = use_pair_gemm_sk(rows, 3 * D / 128);
-  const int sk_qkv = pair_qkv && !use_pair_gemm(rows, 3 * D / 128);
-  const bool pair_gu = !d.n_experts && use_pair_gemm_sk(rows, F / 64);
-  const int sk_gu = pair_gu && !use_pair_gemm(rows, F / 64);
-  const bool pair_o = use_pair_gemm_sk(rows, D / 128);
-  const bool pair_down = !d.n_experts && use_pair_gemm_sk(rows, D / 128);
-  GemmMaps mx2{}, mo2{}, mact2{};
-  if (((pair_qkv || pair_gu) && !make_map(&mx2.b, c->xn, rows, D, kPairBN / 2)) ||
-      (pair_o && !make_map(&mo2.b, c->attn_o, rows, D, kPairBN / 2)) ||
-      (pair_down && !make_map(&mact2.b, c->act, rows, F, kPairBN / 2)))
+  // many rows: every projection on pair-CTA tiles (pair_mode)
+  const PairMode pm_qkv = pair_mode(rows, 3 * D / 128, false);
+  const PairMode pm_gu = d.n_experts ? PAIR_NONE : pair_mode(rows, F / 64, false);
+  const PairMode pm_o = pair_mode(rows, D / 128, true);
+  const PairMode pm_down = d.n_experts ? PAIR_NONE : pair_mode(rows, D / 128, true);
+  const bool pair_qkv = pm_qkv != PAIR_NONE, pair_gu = pm_gu != PAIR_NONE;
+  const bool pair_o = pm_o != PAIR_NONE, pair_down = pm_down != PAIR_NONE;
+  GemmMaps mxq{}, mxg{}, mo2{}, mact2{};
+  if ((pair_qkv && !make_map(&mxq.b, c->xn, rows, D, pair_bn(pm_qkv) / 2)) ||
+      (pair_gu && !make_map(&mxg.b, c->xn, rows, D, pair_bn(pm_gu) / 2)) ||
+      (pair_o && !make_map(&mo2.b, c->attn_o, rows, D, pair_bn(pm_o) / 2)) ||
+      (pair_down && !make_map(&mact2.b, c->act, rows, F, pair_bn(pm_down) / 2)))
     return fail(c, DINFER_ECUDA, "tensor map encoding failed for activations");
   const AttnPlan ap = plan_attention(f.batch, f.rows_per_seq, H, f.L);
   const int nthr = ((D / 16 + 31) / 32) * 32;  // fused-norm threads per row: whole warps
@@ -779,7 +806,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   for (int l = 0; l < d.n_layers; ++l) {
     // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue
     {
-      GemmMaps m = pair_qkv ? mx2 : mx;
+      GemmMaps m = pair_qkv ? mxq : mx;
       m.a[0] = c->m_wq[l];
       m.a[1] = c->m_wk[l];
       m.a[2] = c->m_wv[l];
@@ -795,7 +822,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.rows_per_seq = f.rows_per_seq; a.seq_len = f.L; a.pos_from_state = f.pos_from_state;
       a.row_off = f.row_off;
       a.state = c->st; a.ws = c->gemm_ws; a.status = c->st;
-      CK(pair_qkv ? launch_gemm_tc2(m, a, s, sk_qkv) : launch_gemm_tc(m, a, BN, s));
+      CK(pair_qkv ? launch_gemm_tc2(m, a, s, pm_qkv) : launch_gemm_tc(m, a, BN, s));
     }
     // a3: attention over the dual cache
     CK(launch_attention(c->q, c->kc_layer(l), c->vc_layer(l), c->attn_o, f.batch, f.rows_per_seq, H, f.L, ap,
@@ -807,10 +834,11 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       GemmArgs a{};
       a.M = rows; a.N = D; a.K = D; a.n_tiles = D / 128; a.a_mode = A_SINGLE;
       a.resid = c->h; a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
-      CK(pair_o ? launch_gemm_tc2(m, a, s, 1) : launch_gemm_tc(m, a, BNo, s, true, o_whole));
+      CK(pair_o ? launch_gemm_tc2(m, a, s, pm_o) : launch_gemm_tc(m, a, BNo, s, true, o_whole));
       CK(launch_resid_norm(rows, nthr, s, c->h, (const __nv_bfloat16*)c->LW(l, 5), (__nv_bfloat16*)c->xn, D,
                            d.rms_eps, f.rows_per_seq, f.L, 0, 0, (const DevState*)c->st,
-                           pair_o ? resid_plan_pair(a, c->gemm_ws) : resid_plan(a, BNo, c->gemm_ws, o_whole)));
+                           pair_o ? resid_plan_pair(a, c->gemm_ws, pm_o)
+                                  : resid_plan(a, BNo, c->gemm_ws, o_whole)));
     }
     const bool last = l + 1 == d.n_layers;
     const void* gn = last ? c->W(1 + 9 * d.n_layers) : c->LW(l + 1, 0);
@@ -833,23 +861,23 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
     }
     // a5: SwiGLU FFN (gate/up with the SiLU*up epilogue, down + residual)
     {
-      GemmMaps m = pair_gu ? mx2 : mx;
+      GemmMaps m = pair_gu ? mxg : mx;
       m.a[0] = c->m_wg[l];
       m.a[1] = c->m_wu[l];
       GemmArgs a{};
       a.M = rows; a.N = F; a.K = D; a.n_tiles = F / 64; a.a_mode = A_PAIR;
       a.out_bf16 = (__nv_bfloat16*)c->act; a.ldo = F;
       a.ws = c->gemm_ws; a.status = c->st; a.state = c->st;
-      CK(pair_gu ? launch_gemm_tc2(m, a, s, sk_gu) : launch_gemm_tc(m, a, BN, s));
+      CK(pair_gu ? launch_gemm_tc2(m, a, s, pm_gu) : launch_gemm_tc(m, a, BN, s));
       GemmMaps m2 = pair_down ? mact2 : mact;
       m2.a[0] = c->m_wd[l];
       GemmArgs b{};
       b.M = rows; b.N = D; b.K = F; b.n_tiles = D / 128; b.a_mode = A_SINGLE;
       b.resid = c->h; b.ws = c->gemm_ws; b.status = c->st; b.state = c->st;
-      CK(pair_down ? launch_gemm_tc2(m2, b, s, 1) : launch_gemm_tc(m2, b, BN, s, true));
+      CK(pair_down ? launch_gemm_tc2(m2, b, s, pm_down) : launch_gemm_tc(m2, b, BN, s, true));
       CK(launch_resid_norm(nrows, nthr, s, c->h, (const __nv_bfloat16*)gn, (__nv_bfloat16*)c->xn, D, d.rms_eps,
                            f.B, f.rows_per_seq, gather, -f.row_off, (const DevState*)c->st,
-                           pair_down ? resid_plan_pair(b, c->gemm_ws) : resid_plan(b, BN, c->gemm_ws)));
+                           pair_down ? resid_plan_pair(b, c->gemm_ws, pm_down) : resid_plan(b, BN, c->gemm_ws)));
       CK(debug_copy_hidden(c, f, l, s));
     }
   }
@@ -1633,17 +1661,17 @@ dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_
   const int BN = bn_for_rows(M);
   if ((size_t)((M + BN - 1) / BN) * (N / 128) * 4 > kOpTicketBytes) return fail(c, DINFER_EINVAL, "too many tiles");
   if (!set_smem_attrs()) return fail(c, DINFER_ECUDA, "cudaFuncSetAttribute failed");
-  const bool pair = use_pair_gemm_sk(M, N / 128);
-  const int pair_sk = pair && !use_pair_gemm(M, N / 128);
+  const PairMode pm = pair_mode(M, N / 128, false);
+  const bool pair = pm != PAIR_NONE;
   GemmMaps m{};
-  if (!make_map(&m.a[0], W, N, K, 128) || !make_map(&m.b, X, M, K, pair ? kPairBN / 2 : BN))
+  if (!make_map(&m.a[0], W, N, K, 128) || !make_map(&m.b, X, M, K, pair ? pair_bn(pm) / 2 : BN))
     return fail(c, DINFER_EINVAL, "tensor map encoding failed (alignment?)");
   GemmArgs a{};
   a.M = M; a.N = N; a.K = K; a.n_tiles = N / 128; a.a_mode = A_SINGLE;
   a.out_f32 = Y; a.ldo = N;
   a.ws = reinterpret_cast<float*>(o.data); a.status = o.st; a.state = o.st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  CK(pair ? launch_gemm_tc2(m, a, s, pair_sk) : launch_gemm_tc(m, a, BN, s));
+  CK(pair ? launch_gemm_tc2(m, a, s, pm) : launch_gemm_tc(m, a, BN, s));
   return DINFER_OK;
 }
 

@@ -52,8 +52,9 @@ GEMM_SHAPES = [
     (64, 4096, 12288),     # LLaDA-8B down projection (stream-K over long K)
     (200, 640, 320),       # token tile 256, ragged
     (1536, 1024, 512),     # refresh-like rows: several token tiles
-    (512, 4096, 4096),     # batch-16 block rows (pair-CTA tiles, stream-K + fixup)
-    (700, 8192, 1024),     # pair-CTA stream-K, ragged last token tile
+    (512, 4096, 4096),     # batch-16 block rows (whole 128-token pair-CTA tiles)
+    (700, 8192, 1024),     # whole 128-token pair-CTA tiles, ragged last token tile
+    (384, 2048, 1024),     # pair-CTA tiles in stream-K order + the pair split-K fixup
     (1536, 12288, 512),    # whole-tile schedule, several tiles per CTA
     (200, 24576, 256),     # whole-tile schedule, ragged token tile
 ]
