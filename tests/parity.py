@@ -85,8 +85,9 @@ def conf_interval(conf, delta):
 def flags_for(logits, conf, mask_block, tau, delta):
     """Block positions whose decision a logit error of at most delta could
     flip: top-2 logit gap < max(2 delta, 1e-2); tau inside the confidence
-    interval (or |conf - tau| < 1e-2); fallback (no confidence reachably above
-    tau): every masked position whose interval reaches the best one's."""
+    interval (or |conf - tau| < 1e-2); fallback (possible whenever no masked
+    confidence is certainly above tau, i.e. no interval lies wholly above it):
+    every masked position whose interval reaches the best one's."""
     b, B = conf.shape
     fl = np.zeros((b, B), dtype=bool)
     for i in range(b):
@@ -95,7 +96,7 @@ def flags_for(logits, conf, mask_block, tau, delta):
         lo, hi = conf_interval(conf[i], delta)
         fl[i] |= ((lo <= tau) & (tau < hi)) | (np.abs(conf[i] - tau) < FLAG_CONF)
         masked = mask_block[i]
-        if masked.any() and not (hi[masked] > tau).any():
+        if masked.any() and not (lo[masked] > tau).any():
             best = int(np.argmax(np.where(masked, conf[i], -np.inf)))
             fl[i] |= masked & (hi >= lo[best] - FLAG_CONF)
     return fl

@@ -116,3 +116,24 @@ def test_fp32_models_have_no_rounding_floor():
         O.linear = orig
     fin = np.isfinite(exact)
     assert np.max(np.abs(exact[fin] - approx[fin])) < 1e-4   # the stated fp32 tolerance holds
+
+
+def test_flags_cover_a_fallback_that_may_happen():
+    """The threshold rule's fallback (no masked confidence above tau: commit
+    the single most confident position) can happen as soon as no masked
+    confidence is certainly above tau; then every masked position that could
+    be the most confident is a decision that rounding may flip."""
+    tau, delta = 0.9, 0.57
+    conf = np.array([[0.7415, 0.7451, 0.05]])
+    lo, hi = PT.conf_interval(conf[0], delta)
+    assert hi[1] > tau > hi[0] and lo[1] < tau       # position 1 may reach tau, position 0 may not
+    logits = np.zeros((1, 3, 4))
+    logits[0, :, 0] = 10.0                             # wide top-2 gaps: no token flag
+    masked = np.array([[True, True, True]])
+    fl = PT.flags_for(logits, conf, masked, tau, delta)
+    assert fl[0, 0] and fl[0, 1]                       # the fallback choice between 0 and 1
+    assert not fl[0, 2]                                # 0.05 can never be the most confident
+    # a position certainly above tau: the commit is by threshold, no fallback
+    conf2 = np.array([[0.7415, 0.7451, 0.999]])
+    fl2 = PT.flags_for(logits, conf2, masked, tau, delta)
+    assert not fl2[0, 0] and fl2[0, 1] and not fl2[0, 2]
