@@ -172,6 +172,8 @@ bool set_smem_attrs() {
                              Gemm2Cfg<256>::kSmem) == cudaSuccess;
   ok &= cudaFuncSetAttribute(gemm_tc2_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Gemm2Cfg<128>::kSmem) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(gemm_tc2_kernel<176>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Gemm2Cfg<176>::kSmem) == cudaSuccess;
   {
     // how many pairs run at once: clusters live inside one GPC, so SMs of a
     // GPC with an odd count of free SMs may stay out
@@ -293,7 +295,9 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
 // cores (>= 384 token rows: the time of its MMAs at ~1.8 PFLOP/s exceeds that
 // of reading its weights once); below that the one-CTA kernel streams the
 // weights.  Per GEMM: whole 256-token tiles dealt round-robin over the
-// co-resident pairs when they keep >= 85% of the pairs busy; else 256-token
+// co-resident pairs when they keep >= 85% of the pairs busy, else whole
+// 176-token tiles when those do (1536 rows: 9 x 176 tokens, 144 tiles of a
+// 4096-wide projection in two waves of 76 pairs); else 256-token
 // tiles in stream-K order for a residual GEMM (the following residual norm
 // adds its split tiles at little cost); else, for the others, whole 128-token
 // tiles when those keep >= 80% of the pairs busy (no fixup launch), and
@@ -301,7 +305,7 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, GemmArgs a, int BN, cudaStream_
 // stream-K beats whole 128-token tiles for the O and down projections; at
 // 512 rows whole 128-token tiles beat stream-K + fixup for QKV and gate/up.)
 constexpr int kPairBN = 256;
-enum PairMode { PAIR_NONE = 0, PAIR_W256, PAIR_W128, PAIR_SK };
+enum PairMode { PAIR_NONE = 0, PAIR_W256, PAIR_W176, PAIR_W128, PAIR_SK };
 int pair_clusters() {
   set_smem_attrs();
   return g_pair_clusters[current_device()];
@@ -315,10 +319,11 @@ bool pair_balanced(int M, int n_tiles, int bn, int pct) {
 PairMode pair_mode(int M, int n_tiles, bool resid) {
   if (pair_clusters() < 1 || M < 384 || n_tiles % 2) return PAIR_NONE;
   if (pair_balanced(M, n_tiles, 256, 85)) return PAIR_W256;
+  if (pair_balanced(M, n_tiles, 176, 85)) return PAIR_W176;
   if (!resid && pair_balanced(M, n_tiles, 128, 80)) return PAIR_W128;
   return PAIR_SK;
 }
-int pair_bn(PairMode pm) { return pm == PAIR_W128 ? 128 : 256; }
+int pair_bn(PairMode pm) { return pm == PAIR_W128 ? 128 : (pm == PAIR_W176 ? 176 : 256); }
 // Pairs of a pair-GEMM launch: all co-resident pairs in stream-K mode (at
 // least k_tiles / 14 units each, so that at most 16 pairs share a tile),
 // else one per tile up to that count.
@@ -374,7 +379,8 @@ cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, Pa
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = bn == 128 ? Gemm2Cfg<128>::kSmem : Gemm2Cfg<256>::kSmem;
+  cfg.dynamicSmemBytes =
+      bn == 128 ? Gemm2Cfg<128>::kSmem : (bn == 176 ? Gemm2Cfg<176>::kSmem : Gemm2Cfg<256>::kSmem);
   cfg.stream = s;
   cudaLaunchAttribute at[2];
   int n = 0;
@@ -390,8 +396,9 @@ cudaError_t launch_gemm_tc2(const GemmMaps& maps, GemmArgs a, cudaStream_t s, Pa
   ++n;
   cfg.attrs = at;
   cfg.numAttrs = n;
-  cudaError_t e = bn == 128 ? cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<128>, maps, a)
-                            : cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<256>, maps, a);
+  cudaError_t e = bn == 128   ? cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<128>, maps, a)
+                  : bn == 176 ? cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<176>, maps, a)
+                              : cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<256>, maps, a);
   if (e == cudaSuccess && stream_k && a.resid == nullptr)
     e = launchk(splitk_fixup_pair_kernel<kPairBN>, dim3((unsigned)(tiles * 2 * (kPairBN / 16))), dim3(128), 0, s, 1,
                 a);

@@ -126,6 +126,10 @@ constexpr int kGemmThreads = 192;
 // of a CTA: nine 16 KB weight tiles at 64 tokens).
 template <int BN>
 constexpr int gemm_default_stages() { return BN == 64 ? 9 : (BN == 128 ? 6 : 4); }
+// TMEM column distance of the two accumulators: BN, or 256 for tiles wider
+// than 128 tokens (each accumulator starts on a 256-column boundary)
+template <int BN>
+__host__ __device__ constexpr int acc_stride() { return BN <= 128 ? BN : 256; }
 // the GEMM kernel stages QKV outputs where the buffers fit beside its stages
 // and two exchange buffers
 template <int BN>
@@ -554,7 +558,7 @@ __device__ __forceinline__ void run_mma(const SegList& sl, const Pipe& p, uint32
     const uint32_t use = j >> 1;
     if (!mbar_wait(&p.tempty[acc], (use & 1) ^ 1, p.abort_flag)) break;
     tc_fence_after();
-    const uint32_t d_tmem = tmem_base + acc * BN;
+    const uint32_t d_tmem = tmem_base + acc * acc_stride<BN>();
     bool ok = true;
     for (int k = kb; k < ke; ++k, ++it) {
       const int s = it % C::kStages;
@@ -670,7 +674,7 @@ __device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Pipe& p, u
     if (a.resid != nullptr && whole) resid_load16(a, n, tr.mt * BN, hcur);
     if (!mbar_wait(&p.tfull[acc], use & 1, p.abort_flag)) break;
     tc_fence_after();
-    const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+    const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * acc_stride<BN>();
     if (!whole) {
       // partial tile: token-major [BN][128], so a warp stores whole lines
       float* base = partial_slot(t);

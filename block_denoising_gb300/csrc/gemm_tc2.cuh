@@ -116,9 +116,11 @@ struct Gemm2Cfg {
   static constexpr int kStageOutBytes = 2 * 16 * 128 * 2;  // QKV output staging (see epilogue_chunk)
   static constexpr int kStages = (232448 - 1024 - kXchgFloats * 4 - kStageOutBytes - 512) / kStage;
   static constexpr int kSmem = 1024 + kStages * kStage + kXchgFloats * 4 + kStageOutBytes + 512;
-  static constexpr int kTmemCols = 2 * BN;
+  // two accumulators of BN columns, allocated as a power of two
+  static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;
   static_assert(kSmem <= 232448, "pair GEMM shared memory above 227 KB");
-  static_assert(kTmemCols <= 512, "two accumulators of BN columns must fit in TMEM");
+  static_assert(2 * BN <= 512 && BN % 16 == 0, "two accumulators of BN columns must fit in TMEM");
+  static_assert((BN / 2) * 128 % 1024 == 0, "each CTA's token half must keep the 1024-byte swizzle alignment");
 };
 
 // Pair tile t -> this CTA's 128-row tile of weight pair tile np (rows
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t use = j >> 1;
         if (!mbar_wait_cluster(&p.tempty[acc], (use & 1) ^ 1, p.abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * acc_stride<BN>();
         bool ok = true;
         for (int k = kb; k < ke; ++k, ++it) {
           const int s = it % C::kStages;

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int acc = j & 1;
       if (!mbar_wait(&p.tfull[acc], (j >> 1) & 1, p.abort_flag)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * acc_stride<BN>();
       const int n = nt * 128 + row;
       const bool valid = (n < la.V) && (n != la.mask_id);
 #pragma unroll 1

@@ -55,6 +55,7 @@ GEMM_SHAPES = [
     (512, 4096, 4096),     # batch-16 block rows (whole 128-token pair-CTA tiles)
     (700, 8192, 1024),     # whole 128-token pair-CTA tiles, ragged last token tile
     (384, 2048, 1024),     # pair-CTA tiles in stream-K order + the pair split-K fixup
+    (1536, 4096, 1024),    # whole 176-token pair-CTA tiles (9 token tiles, the last 128 of 176 rows)
     (1536, 12288, 512),    # whole-tile schedule, several tiles per CTA
     (200, 24576, 256),     # whole-tile schedule, ragged token tile
 ]
