@@ -361,7 +361,7 @@ def run_ours(args):
     for _ in range(args.steps):
         dec.generate(prompt_h, G, B, run.threshold, out=out_h)
     t_e2e = time.perf_counter() - t0
-    # ---- the cached iteration alone (spec roofline) and the refresh ----
+    # ---- the cached iteration alone (its HBM roofline) and the refresh --------
     ids = out_d.clone()
     ids[:, P:] = cfg.mask_id
     mask = torch.zeros((b, L), dtype=torch.uint8, device="cuda")

@@ -9,7 +9,7 @@ cached iterations; every GPU iteration starts from the oracle's state
 (teacher forcing, tests/parity.py) through dinfer_prefill_cache /
 dinfer_block_step.  bf16 tolerances are derived on the CPU over the same
 iterations; the report gives, per workload, the logit errors against that
-delta and against the benchmark spec's bound 3e-2, the flagged decisions, the
+delta and against the stated logit bound 3e-2, the flagged decisions, the
 per-layer divergence of the residual stream and the teacher-forced LM head.
 """
 import numpy as np

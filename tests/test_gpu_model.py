@@ -10,7 +10,7 @@ tests/parity.py and tests/test_tolerances.py); confidences at unflagged
 positions within 1e-2.  A decision is flagged (counted and reported, allowed
 to differ) only if a logit error within delta could flip it; every unflagged
 token and commit must match.  Each test also reports by how much the
-spec logit bound 3e-2 is missed, the per-layer divergence of the
+stated per-iteration logit bound 3e-2 is missed, the per-layer divergence of the
 residual stream, and the teacher-forced LM head (the GPU's own final normed
 rows through the oracle's LM head: within 1e-3).
 """
