@@ -22,8 +22,8 @@
 //              64 h .. 64 h + 63 of every chunk.  Each half is an online
 //              softmax of its own (running max m_h, normaliser l_h and
 //              accumulator O_h in TMEM), so the two warps that share an SM
-//              sub-partition never wait for each other and hide each other's
-//              latencies: tcgen05.ld of the half row of S, log2-domain
+//              sub-partition exchange nothing per chunk: tcgen05.ld of the
+//              half row of S, log2-domain
 //              softmax, P = bf16(2^(s - m_h)) written to the half's 64-key
 //              slab of one of two shared-memory buffers in the
 //              128-byte-swizzled K-major layout (so the softmax of chunk j
