@@ -244,10 +244,14 @@ GemmSched gemm_schedule(int M, int n_tiles, int K, int BN, bool whole_only = fal
 // The schedule a GEMM launch takes: gemm_schedule, except that a GEMM whose
 // split tiles would need a fixup launch (~5 us) takes whole tiles when one SM
 // streaming its weight tiles (~85 GB/s) is not slower than all SMs streaming
-// the whole matrix (~6.8 TB/s) plus that launch.
+// the whole matrix (~6.8 TB/s) plus that launch -- provided the whole tiles
+// occupy at least half of the SMs (a short-K tile streams at ~35 GB/s per SM,
+// so fewer whole tiles, as the MoE model's QKV and router GEMMs of a block,
+// are faster split).
 GemmSched launch_schedule(const GemmArgs& a, int BN, bool defer_resid, bool whole_only) {
   GemmSched gs = gemm_schedule(a.M, a.n_tiles, a.K, BN, whole_only);
-  if (gs.stream_k && !defer_resid && a.M <= 128) {
+  const long long all_tiles = (long long)((a.M + BN - 1) / BN) * a.n_tiles;
+  if (gs.stream_k && !defer_resid && a.M <= 128 && all_tiles * 2 >= num_sms()) {
     const long long tiles = (long long)((a.M + BN - 1) / BN) * a.n_tiles;
     const long long per = (tiles + num_sms() - 1) / num_sms();
     const long long tile_bytes = (long long)std::min(a.N, 128) * a.K * 2;
