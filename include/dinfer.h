@@ -16,12 +16,14 @@
  *   forward's block rows are decoded as iteration 1.  Then, while the block
  *   still has masked positions, a denoising iteration recomputes only the
  *   block's rows, which attend bidirectionally over the cached prefix, the
- *   block's fresh keys/values and the cached suffix.  Each iteration the LM
- *   head gives, per block position, the top-1 token and its softmax
- *   probability (confidence); every masked position whose confidence exceeds
+ *   block's fresh keys/values and the cached suffix (the default dual cache;
+ *   dinfer_set_cache_mode selects the other members of the family).  Each
+ *   iteration the LM head gives, per block position, the top-1 token and its
+ *   softmax probability (confidence); every masked position whose confidence exceeds
  *   the threshold is committed, or, if none does, the single most confident
  *   one (ties: lowest vocabulary index, lowest position).  The mask token's
- *   own logit is excluded from argmax and softmax.  eos_id is not used.
+ *   own logit is excluded from argmax and softmax.  eos_id is off unless
+ *   dinfer_set_eos sets it (end of sequence after a completed block).
  *
  * Conventions
  *   - All calls are asynchronous on the context's stream unless stated.
