@@ -294,6 +294,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the process group (with times:
+    the slowest replica's); the values themselves without a group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_tokens(world, steps, batch, gen_length):
+    """Generated tokens of all replicas over the timed steps: every rank runs
+    the whole workload (the batch-1 path does not shard)."""
+    return world * steps * batch * gen_length
+
+
 def progress(msg):
     print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
 
@@ -391,12 +408,9 @@ def run_ours(args):
 
     progress(f"iteration {us_iter:.1f} us, refresh {us_refresh:.1f} us")
 
-    # max over ranks
-    t = torch.tensor([t_dev, t_e2e], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    t_dev, t_e2e = float(t[0]), float(t[1])
-    tokens = world * args.steps * b * G
+    # max over ranks: the slowest replica's times
+    t_dev, t_e2e = max_over_ranks([t_dev, t_e2e], "cuda")
+    tokens = replica_tokens(world, args.steps, b, G)
     value = tokens / t_dev
     e2e = tokens / t_e2e
     if rank == 0:

@@ -43,3 +43,25 @@ def test_reference_arm_other_ranks_exit_without_work():
     p = _run({"RANK": "1"})
     assert p.returncode == 0, p.stderr[-2000:]
     assert p.stdout.strip() == ""
+
+
+def test_clock_summary_reads_the_sampled_gpu_and_its_throttle_reasons(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+    # nvidia-smi --format=csv,noheader,nounits rows: index, sm, max sm, power,
+    # active mask, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap
+    rows = [
+        "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "1, 1100, 2070, 300.0, 0x0000000000000008, Active, Not Active, Not Active, Not Active",
+        "0, 2040, 2070, 1390.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2055, 2070, 1200.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, [N/A], 2070, [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]",
+    ]
+    p = tmp_path / "clocks.csv"
+    p.write_text("\n".join(rows) + "\n")
+    s = bench.ClockSampler(str(p)).summary(0)
+    assert s["sm_mhz"] == 2055.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]  # GPU 1's hw_slowdown is another GPU's
+    assert s["samples"] == 4
+    s1 = bench.ClockSampler(str(p)).summary(1)
+    assert s1["sm_mhz"] == 1100.0 and s1["reasons"] == ["hw_slowdown"]
