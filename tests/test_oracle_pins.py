@@ -339,17 +339,31 @@ def test_in_place_cache_equals_explicit_concatenation():
     assert r.logits.shape == (1, 4, 32)
 
 
+def _same_trajectory(ta, tb, xa, xb):
+    """Equal ids, commits and (to rounding) logits at every iteration."""
+    np.testing.assert_array_equal(xa, xb)
+    assert len(ta) == len(tb)
+    for a, b in zip(ta, tb):
+        assert a.commit.tolist() == b.commit.tolist()
+        fin = np.isfinite(a.logits)
+        np.testing.assert_array_equal(fin, np.isfinite(b.logits))
+        np.testing.assert_allclose(a.logits[fin], b.logits[fin], rtol=1e-10, atol=1e-9)
+
+
 def test_one_layer_dual_cache_equals_no_cache():
     # with one layer the cached prefix/suffix K/V depend only on the embeddings
-    # and positions, so the dual cache is exact and the trajectories coincide
+    # and positions, so the dual cache is exact: the same logits at every
+    # iteration.  tau >= 1 commits one token per iteration, so every block runs
+    # cached iterations (at lower tau this model fills a block at once).
     desc = tiny_desc(n_layers=1, vocab=32, mask_id=31)
     m, _ = tiny_model(desc, std=0.5)
     prompt = np.array([[1, 5, 9, 2, 7]])
-    for tau in (0.9, 0.5, 0.2):
-        xa, ta = O.generate(m, prompt, 12, 4, tau, cache_mode="dual")
-        xb, tb = O.generate(m, prompt, 12, 4, tau, cache_mode="none")
-        np.testing.assert_array_equal(xa, xb)
-        assert [t.commit.tolist() for t in ta] == [t.commit.tolist() for t in tb]
+    for tau in (1.0, 0.9, 0.5):
+        xa, ta = O.generate(m, prompt, 12, 4, tau, cache_mode="dual", keep_logits=True)
+        xb, tb = O.generate(m, prompt, 12, 4, tau, cache_mode="none", keep_logits=True)
+        _same_trajectory(ta, tb, xa, xb)
+        if tau >= 1.0:
+            assert sum(t.iteration > 1 for t in ta) == 9          # 3 cached iterations per block
 
 
 def test_two_layer_dual_cache_is_an_approximation_after_commits():
@@ -382,12 +396,17 @@ def test_threshold_zero_is_blockwise_argmax_of_full_forward():
     desc = tiny_desc(vocab=32, mask_id=31)
     m, ws = tiny_model(desc)
     prompt = [1, 2, 3]
-    x, tr = O.generate(m, np.array([prompt]), 8, 4, 0.0)
+    x, tr = O.generate(m, np.array([prompt]), 8, 4, 0.0, keep_logits=True)
     assert O.iterations_per_block(tr) == {0: 1, 1: 1}
-    # brute force: each block is the argmax of one full forward over the current ids
+    # brute force: each block is the argmax of one full forward over the current
+    # ids, and its logits are that forward's (the argmax alone is a weak check:
+    # this small model puts one token far ahead at every position)
     ids = prompt + [31] * 8
-    for s in (3, 7):
-        lg = BF.forward_logits(desc, [w.tolist() for w in ws], ids)
+    for t, s in zip(tr, (3, 7)):
+        lg = np.array(BF.forward_logits(desc, [w.tolist() for w in ws], ids))
+        fin = np.isfinite(lg[s:s + 4])
+        np.testing.assert_array_equal(fin, np.isfinite(t.logits[0]))
+        np.testing.assert_allclose(t.logits[0][fin], lg[s:s + 4][fin], rtol=1e-9, atol=1e-9)
         for i in range(s, s + 4):
             ids[i] = int(np.argmax(lg[i]))
     assert x[0].tolist() == ids
@@ -688,11 +707,12 @@ def test_one_layer_every_cache_mode_equals_no_cache(mode):
     desc = tiny_desc(n_layers=1, vocab=32, mask_id=31)
     m, _ = tiny_model(desc, std=0.5)
     prompt = np.array([[1, 5, 9, 2, 7]])
-    for tau in (0.9, 0.5):
-        xa, ta = O.generate(m, prompt, 12, 4, tau, cache_mode=mode, window=2)
-        xb, tb = O.generate(m, prompt, 12, 4, tau, cache_mode="none")
-        np.testing.assert_array_equal(xa, xb)
-        assert [t.commit.tolist() for t in ta] == [t.commit.tolist() for t in tb]
+    for tau in (1.0, 0.9):
+        xa, ta = O.generate(m, prompt, 12, 4, tau, cache_mode=mode, window=2, keep_logits=True)
+        xb, tb = O.generate(m, prompt, 12, 4, tau, cache_mode="none", keep_logits=True)
+        _same_trajectory(ta, tb, xa, xb)
+        if tau >= 1.0:
+            assert sum(t.iteration > 1 for t in ta) == 9
 
 
 def test_vicinity_wider_than_the_sequence_is_no_cache():
@@ -744,9 +764,11 @@ def _eos_model():
 
 
 def _first_seen(x, P, B, k, avoid=()):
-    """An id that the generation x first produces in block k (>= 1)."""
-    for v in x[P + k * B:P + (k + 1) * B]:
-        if v not in x[P:P + k * B] and v not in avoid:
+    """An id that the generation x first produces in block k (>= 1), in a
+    block that also holds another id (so that rewriting the block would show)."""
+    blk = x[P + k * B:P + (k + 1) * B]
+    for v in blk:
+        if v not in x[P:P + k * B] and v not in avoid and (blk != v).any():
             return int(v)
     return None
 
@@ -819,3 +841,142 @@ def test_eos_in_the_prompt_does_not_stop():
             break
     x1, _ = O.generate(m, prompt, 12, 4, 0.6, eos_id=first)      # the prompt holds eos_id: no stop
     np.testing.assert_array_equal(x0, x1)
+
+
+# ---------------------------------------------------------------------------
+# more planted mistakes: the LM head, the activations, the cache and the
+# block loop.  Each must make a pin above fail.
+# ---------------------------------------------------------------------------
+_ORIG.update({k: getattr(O, k) for k in ("silu", "softmax", "lm_head_logits", "embed", "refresh_step",
+                                          "cached_step", "eos_stop", "recompute_window")})
+
+
+def _relu_for_silu(x):
+    return np.maximum(x, 0.0)
+
+
+def _rope_interleaved(x, pos, theta):
+    """Rotates the adjacent pairs (2i, 2i+1) instead of (i, i + hd/2)."""
+    x = np.asarray(x, dtype=np.float64)
+    hd = x.shape[-1]
+    inv = theta ** (-(2.0 * np.arange(hd // 2)) / hd)
+    ang = np.asarray(pos, dtype=np.float64)[:, None, None] * inv[None, None, :]
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., 0::2] = x1 * np.cos(ang) - x2 * np.sin(ang)
+    y[..., 1::2] = x2 * np.cos(ang) + x1 * np.sin(ang)
+    return y
+
+
+def _softmax_wrong_axis(x, axis=-1):
+    return _ORIG["softmax"](x, axis=-2 if x.ndim > 1 else axis)
+
+
+def _rms_eps_outside_sqrt(h, g, eps):
+    h = np.asarray(h, dtype=np.float64)
+    return h / (np.sqrt(np.mean(h * h, axis=-1, keepdims=True)) + 1e3 * eps) * np.asarray(g, dtype=np.float64)
+
+
+def _lm_head_keeps_mask(model, h):
+    d = model.desc
+    a = model.prec.r(O.rmsnorm(h, model.final_norm, d.rms_eps))
+    return d.logit_scale * O.linear(a, model.lm_head)
+
+
+def _lm_head_unscaled(model, h):
+    return _ORIG["lm_head_logits"](model, h) / model.desc.logit_scale
+
+
+def _lm_head_no_final_norm(model, h):
+    d = model.desc
+    logits = d.logit_scale * O.linear(model.prec.r(h), model.lm_head)
+    logits[:, d.mask_id] = -np.inf
+    return logits
+
+
+def _embed_off_by_one(model, ids):
+    return np.asarray(model.embed[(np.asarray(ids) + 1) % model.desc.vocab], dtype=np.float64)
+
+
+@pytest.mark.parametrize("name,fake", [
+    ("silu", _relu_for_silu),
+    ("rope", _rope_interleaved),
+    ("softmax", _softmax_wrong_axis),
+    ("rmsnorm", _rms_eps_outside_sqrt),
+    ("lm_head_logits", _lm_head_keeps_mask),
+    ("lm_head_logits", _lm_head_unscaled),
+    ("lm_head_logits", _lm_head_no_final_norm),
+    ("embed", _embed_off_by_one),
+])
+def test_planted_forward_mistake_is_caught(monkeypatch, name, fake):
+    desc = tiny_desc()
+    m, ws = tiny_model(desc, std=0.4)
+    assert _bruteforce_gap(m, ws, desc) < 1e-9
+    monkeypatch.setattr(O, name, fake)
+    assert _bruteforce_gap(m, ws, desc) > 1e-6
+
+
+def _refresh_block_rows_only(model, x, mask, s0, B, tau, cache, commit=True):
+    """A 'refresh' that computes only the block's rows: prefix and suffix K/V never cached."""
+    hid = O.forward(model, x, cache, np.arange(s0, s0 + B))
+    return O.decode_block(model, hid, x, mask, s0, B, tau, commit)
+
+
+def _cached_step_without_cache(model, x, mask, s0, B, tau, cache, commit=True):
+    """A cached iteration that attends over the block only (an empty cache)."""
+    fresh = O.Cache(model.desc, x.shape[0], x.shape[1])
+    hid = O.forward(model, x, fresh, np.arange(s0, s0 + B))
+    return O.decode_block(model, hid, x, mask, s0, B, tau, commit)
+
+
+def _eos_overwrites_the_block(x, mask, s0, B, eos_id):
+    """Fills from the block's first position, rewriting committed tokens."""
+    for i in range(x.shape[0]):
+        if (x[i, s0:s0 + B] == eos_id).any():
+            x[i, s0:] = eos_id
+            mask[i, s0:] = False
+
+
+def _eos_stops_every_sequence(x, mask, s0, B, eos_id):
+    """Ends the whole batch when any sequence's block holds eos_id."""
+    if (x[:, s0:s0 + B] == eos_id).any():
+        x[:, s0 + B:] = eos_id
+        mask[:, s0 + B:] = False
+
+
+def _vicinity_one_sided(cache_mode, s0, B, L, w=0):
+    if cache_mode == "vicinity":
+        return max(0, s0 - w), s0 + B
+    return _ORIG["recompute_window"](cache_mode, s0, B, L, w)
+
+
+def _pin_fails(pin, *args):
+    try:
+        pin(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+def _window_pins():
+    return [_pin_fails(test_recompute_windows, *case) for case in
+            test_recompute_windows.pytestmark[0].args[1]]
+
+
+@pytest.mark.parametrize("name,fake,pins", [
+    ("refresh_step", _refresh_block_rows_only, (test_threshold_zero_is_blockwise_argmax_of_full_forward,)),
+    ("cached_step", _cached_step_without_cache, (test_one_layer_dual_cache_equals_no_cache,)),
+    ("eos_stop", _eos_overwrites_the_block, (test_eos_in_a_block_ends_the_sequence_after_it,)),
+    ("eos_stop", _eos_stops_every_sequence, (test_eos_in_a_batch_stops_one_sequence_only,)),
+])
+def test_planted_loop_mistake_is_caught(monkeypatch, name, fake, pins):
+    for pin in pins:
+        assert not _pin_fails(pin)
+    monkeypatch.setattr(O, name, fake)
+    assert any(_pin_fails(pin) for pin in pins)
+
+
+def test_planted_window_mistake_is_caught(monkeypatch):
+    assert not any(_window_pins())
+    monkeypatch.setattr(O, "recompute_window", _vicinity_one_sided)
+    assert any(_window_pins())
