@@ -980,3 +980,86 @@ def test_planted_window_mistake_is_caught(monkeypatch):
     assert not any(_window_pins())
     monkeypatch.setattr(O, "recompute_window", _vicinity_one_sided)
     assert any(_window_pins())
+
+
+def _attention_causal(q, k, v, rows_per_group=1024):
+    """A causal LM's attention: query i sees keys up to its own position."""
+    q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
+    nq, nk = q.shape[0], k.shape[0]
+    s = np.einsum("qhd,khd->hqk", q, k) / np.sqrt(q.shape[-1])
+    later = np.arange(nk)[None, :] > np.arange(nq)[:, None] + (nk - nq)
+    return np.einsum("hqk,khd->qhd", _ORIG["softmax"](np.where(later[None], -np.inf, s), axis=-1), v)
+
+
+def _conf_squared(logits):
+    tok = np.argmax(logits, axis=-1)
+    lmax = logits[np.arange(logits.shape[0]), tok]
+    return tok.astype(np.int64), 1.0 / np.sum(np.exp(logits - lmax[:, None]), axis=-1) ** 2
+
+
+def _commit_ignores_mask(conf, masked, tau):
+    """Commits every confident position, masked or not."""
+    masked = np.asarray(masked, dtype=bool)
+    if not masked.any():
+        return np.zeros_like(masked)
+    sel = np.asarray(conf) > tau
+    if not (sel & masked).any():
+        c = np.where(masked, conf, -np.inf)
+        sel = np.zeros_like(masked)
+        sel[int(np.argmax(c))] = True
+    return sel
+
+
+def _window_decodes_first_rows(model, x, mask, s0, B, tau, cache, r0, r1, commit=True):
+    """Decodes the window's first B rows instead of the block's."""
+    hid = O.forward(model, x, cache, np.arange(r0, r1))
+    return O.decode_block(model, hid[:, :B], x, mask, s0, B, tau, commit)
+
+
+def _eos_seen_in_the_prompt(x, mask, s0, B, eos_id):
+    """Stops on eos_id anywhere before the block's end, the prompt included."""
+    for i in range(x.shape[0]):
+        if (x[i, :s0 + B] == eos_id).any():
+            x[i, s0 + B:] = eos_id
+            mask[i, s0 + B:] = False
+
+
+def _route_one_expert_short(a, router, top_k):
+    return _ORIG["route"](a, router, max(1, top_k - 1))
+
+
+def _decode_rewrites_committed(model, hidden, x, mask, s0, B, tau, commit=True):
+    """Also rewrites positions committed in earlier iterations with the new top-1."""
+    done = ~mask[:, s0:s0 + B].copy()
+    r = _ORIG["decode_block"](model, hidden, x, mask, s0, B, tau, commit)
+    if commit:
+        x[:, s0:s0 + B][done] = r.tok[done]
+    return r
+
+
+def _no_rounding(self, x):
+    return np.asarray(x, dtype=np.float64)
+
+
+_ORIG["decode_block"] = O.decode_block
+
+
+@pytest.mark.parametrize("owner,name,fake,pins", [
+    (O, "attention", _attention_causal, (test_bidirectional_no_causal_mask, test_attention_closed_forms)),
+    (O.Precision, "r", _no_rounding, (lambda: test_forward_matches_bruteforce("bf16"),)),
+    (O, "top1_confidence", _conf_squared, (test_top1_confidence_closed_form,)),
+    (O, "threshold_commit", _commit_ignores_mask,
+     (lambda: test_threshold_commit_cases(*test_threshold_commit_cases.pytestmark[0].args[1][1]),
+      test_eos_in_a_batch_stops_one_sequence_only)),
+    (O, "window_step", _window_decodes_first_rows, (test_vicinity_wider_than_the_sequence_is_no_cache,)),
+    (O, "eos_stop", _eos_seen_in_the_prompt, (test_eos_in_the_prompt_does_not_stop,)),
+    (O, "route", _route_one_expert_short, (test_moe_hand_example_weights_are_the_full_softmax,
+                                           test_route_topk_matches_full_sort)),
+    (O, "decode_block", _decode_rewrites_committed, (test_invariants_tiny_workload,)),
+], ids=["causal-attention", "no-bf16-rounding", "confidence-squared", "commit-ignores-mask",
+        "window-decodes-first-rows", "eos-in-prompt-stops", "top-k-minus-one", "decode-rewrites-committed"])
+def test_planted_mistake_fails_its_pin(monkeypatch, owner, name, fake, pins):
+    for pin in pins:
+        assert not _pin_fails(pin)
+    monkeypatch.setattr(owner, name, fake)
+    assert any(_pin_fails(pin) for pin in pins)
