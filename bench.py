@@ -71,11 +71,12 @@ def _ffn_flops_per_row(cfg):
 def iteration_bytes(cfg, b, L, B, experts=None):
     """Bytes one cached denoising iteration must move: every weight read once
     (embedding rows aside; of the experts, those the block's rows select) plus
-    the cached K/V of the L - B non-block positions."""
+    the cached K/V of the L - B non-block positions, at the model's storage
+    type (bf16; fp32 for the fp32 model)."""
     d, nl, V = cfg.d_model, cfg.n_layers, cfg.vocab
     w = nl * (4 * d * d + _ffn_params(cfg, experts)) + V * d
     kv = b * (L - B) * 2 * d * nl
-    return 2 * (w + kv)
+    return (4 if cfg.dtype == "fp32" else 2) * (w + kv)
 
 
 def iteration_flops(cfg, b, L, B):
