@@ -90,14 +90,22 @@ typedef struct dinfer_stats {
  * Returns -1 for an invalid description. */
 int32_t dinfer_num_weights(const dinfer_model_desc* desc);
 
-/* Validate the description, borrow the device weight pointers, allocate the
- * cache and workspaces for max_batch x max_seq, build tensor-memory
- * descriptors.  stream: the cudaStream_t every call of the context is
+/* The model and its decoder (dInfer README, "Step 3": the model is built
+ * from its configuration, its weights loaded in bf16, and wrapped with a
+ * decoder and a dual KV-cache factory).  Validates the description, borrows
+ * the device weight pointers (weights[i] as dinfer_num_weights orders them;
+ * they stay owned by the caller and must outlive the context), allocates the
+ * cache and workspaces for max_batch x max_seq and builds the weights' TMA
+ * tensor maps.  stream: the cudaStream_t every call of the context is
  * ordered on (NULL = the legacy default stream).
- * On failure *out is NULL and dinfer_last_error(NULL) explains why. */
+ * Errors: DINFER_EINVAL (bad description, NULL or misaligned weight),
+ * DINFER_ENOMEM (device allocation), DINFER_ECUDA (no device, a CUDA call
+ * failed).  On failure *out is NULL and dinfer_last_error(NULL) explains why. */
 dinfer_status dinfer_create(const dinfer_model_desc* desc, const void* const* weights, void* stream,
                             dinfer_ctx** out);
 
+/* Waits for the context's stream, then frees the cache, workspaces and
+ * graphs (not the borrowed weights).  NULL is ignored. */
 void dinfer_destroy(dinfer_ctx* ctx);
 
 /* Text of the last error of ctx (or of the last failed dinfer_create of this
@@ -130,34 +138,50 @@ dinfer_status dinfer_set_cache_mode(dinfer_ctx* ctx, int32_t mode, int32_t windo
  * or equal to mask_id. */
 dinfer_status dinfer_set_eos(dinfer_ctx* ctx, int32_t eos_id);
 
-/* Block boundary (cache refresh): full forward over ids[batch, seq_len]
- * (device, int32), storing every layer's K/V of all positions in the dual
- * cache; then decodes the block [block_start, block_start + block_len) and,
- * if commit != 0, applies one threshold commit to ids / mask (device, uint8,
+/* Block boundary (cache refresh; dInfer README, "Step 3": the dual KV cache
+ * of KVCacheFactory('dual'), the abstract's KV-cache manager): full forward
+ * over ids[batch, seq_len] (device, int32, row-major), storing every layer's
+ * K/V of all positions in the dual cache; then decodes the block
+ * [block_start, block_start + block_len) and, if commit != 0, applies one
+ * threshold commit (ThresholdParallelDecoder) to ids / mask (device, uint8,
  * 1 = masked) in place -- iteration 1 of the block.  committed: optional
- * device int32[batch] receiving the per-sequence commit count.  Requires
- * batch <= max_batch, seq_len <= max_seq, batch * block_len <= 1024. */
+ * device int32[batch] receiving the per-sequence commit count.  Asynchronous;
+ * device-side errors surface at dinfer_sync or the next synchronising call.
+ * Errors: DINFER_EINVAL (NULL or host ids / mask, batch > max_batch,
+ * seq_len > max_seq, batch * block_len > 1024, block outside the sequence,
+ * NaN threshold), DINFER_ECUDA. */
 dinfer_status dinfer_prefill_cache(dinfer_ctx* ctx, int32_t* ids, uint8_t* mask, int32_t batch, int32_t seq_len,
                                    int32_t block_start, int32_t block_len, float threshold, int32_t commit,
                                    int32_t* committed);
 
-/* One cached denoising iteration of the block set by the last
- * dinfer_prefill_cache: the block rows of ids [batch, seq_len] (device) -- or
- * the window the cache policy recomputes -- are re-run against the cache
- * (their fresh K/V overwrite their slots) and one threshold commit updates
- * ids / mask in place.  committed:
- * optional device int32[batch]; 0 for a sequence whose block had no mask. */
+/* One cached denoising iteration (dInfer README, "Step 3": the decoder's
+ * threshold parallel commit; the abstract's diffusion iteration manager) of
+ * the block set by the last dinfer_prefill_cache: the block rows of ids
+ * [batch, seq_len] (device) -- or the window the cache policy recomputes --
+ * are re-run against the cache (their fresh K/V overwrite their slots) and
+ * one threshold commit updates ids / mask in place.  committed: optional
+ * device int32[batch]; 0 for a sequence whose block had no mask.
+ * Asynchronous like dinfer_prefill_cache.  Errors: DINFER_ESTATE before any
+ * dinfer_prefill_cache, DINFER_EINVAL (NULL ids / mask, NaN threshold),
+ * DINFER_ECUDA. */
 dinfer_status dinfer_block_step(dinfer_ctx* ctx, int32_t* ids, uint8_t* mask, float threshold, int32_t* committed);
 
-/* Whole generation: prompt [batch, prompt_len] int32 -> out [batch,
- * prompt_len + gen_length] int32 (prompt kept).  prompt and out may be host
- * or device pointers; host buffers are copied inside the call.  Dual cache:
+/* Whole generation (dInfer README, "Step 3": generate(input_ids,
+ * gen_length, block_length) over BlockIteratorFactory's blocks; its
+ * introduction: CUDA graphs and iteration loops without stream bubbles):
+ * prompt [batch, prompt_len] int32 -> out [batch, prompt_len + gen_length]
+ * int32 (prompt kept), both caller-owned.  prompt and out may be host or
+ * device pointers; host buffers are copied inside the call.  Dual cache:
  * the block loop and the iteration loop run on the device (one CUDA graph
  * with conditional nodes).  Other cache policies: the host enqueues each
  * block (its refresh graph, then a graph whose conditional node runs the
  * block's iterations on the device) without waiting.  The call synchronises
  * once at the end.  gen_length must be a multiple of block_length.  stats may
- * be NULL. */
+ * be NULL.  Errors: DINFER_EINVAL (NULL buffers, gen_length not a positive
+ * multiple of block_length, sizes beyond the context, NaN threshold),
+ * DINFER_ECUDA, DINFER_EDEVICE (the device status word, read at the end: a
+ * token id out of range, a NaN confidence, an iteration overflow or a timed
+ * out pipeline wait; out is then not valid). */
 dinfer_status dinfer_generate(dinfer_ctx* ctx, const int32_t* prompt, int32_t batch, int32_t prompt_len,
                               int32_t gen_length, int32_t block_length, float threshold, int32_t* out,
                               dinfer_stats* stats);
@@ -178,7 +202,10 @@ dinfer_status dinfer_set_debug_outputs(dinfer_ctx* ctx, float* logits, int32_t* 
  * neither. */
 dinfer_status dinfer_set_debug_hidden(dinfer_ctx* ctx, float* hidden, void* final_in);
 
-/* Wait for the context's stream and report the device status word. */
+/* Wait for the context's stream and report the device status word:
+ * DINFER_OK, or DINFER_EDEVICE with the first failure described by
+ * dinfer_last_error.  The word keeps its bits until the next
+ * dinfer_prefill_cache or dinfer_generate clears it. */
 dinfer_status dinfer_sync(dinfer_ctx* ctx);
 
 /* Measurement hook for the byte count of a mixture-of-experts iteration (the
