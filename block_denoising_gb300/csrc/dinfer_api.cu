@@ -815,7 +815,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
   const int nthr = ((D / 16 + 31) / 32) * 32;  // fused-norm threads per row: whole warps
   if (nthr > 512 || D % 128) return fail(c, DINFER_EINVAL, "d_model unsupported by the fused residual norm");
   for (int l = 0; l < d.n_layers; ++l) {
-    // a2: QKV GEMM, RoPE and the dual-cache write in its epilogue
+    // QKV GEMM, RoPE and the dual-cache write in its epilogue
     {
       GemmMaps m = pair_qkv ? mxq : mx;
       m.a[0] = c->m_wq[l];
@@ -835,10 +835,10 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       a.state = c->st; a.ws = c->gemm_ws; a.status = c->st;
       CK(pair_qkv ? launch_gemm_tc2(m, a, s, pm_qkv) : launch_gemm_tc(m, a, BN, s));
     }
-    // a3: attention over the dual cache
+    // attention over the dual cache
     CK(launch_attention(c->q, c->kc_layer(l), c->vc_layer(l), c->attn_o, f.batch, f.rows_per_seq, H, f.L, ap,
                         c->st, s));
-    // a4: O projection + residual, fused with the FFN norm
+    // O projection + residual, fused with the FFN norm
     {
       GemmMaps m = pair_o ? mo2 : mo;
       m.a[0] = c->m_wo[l];
@@ -858,7 +858,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
     const int nrows = last ? f.batch * f.B : rows;
     const int gather = last && f.gathers_block() ? 1 : 0;
     if (d.n_experts) {
-      // a5': routed experts, then the weighted combine + residual + next norm
+      // MoE FFN: routed experts, then the weighted combine + residual + next norm
       MoeBufs mb{c->moe_logits, c->moe_topk_id, c->moe_topk_w, c->moe_rank, c->moe_chunk_cnt, c->moe_chunk_base,
                  c->moe_tables, c->moe_inv, c->moe_x, c->moe_act, c->moe_y, c->gemm_ws, c->st};
       CK(enqueue_moe_ffn(mb, c->xn, rows, D, d.n_experts, d.top_k, d.expert_ffn, c->m_router[l], c->m_w13[l],
@@ -870,7 +870,7 @@ dinfer_status enqueue_layers_bf16(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       CK(debug_copy_hidden(c, f, l, s));
       continue;
     }
-    // a5: SwiGLU FFN (gate/up with the SiLU*up epilogue, down + residual)
+    // SwiGLU FFN (gate/up with the SiLU*up epilogue, down + residual)
     {
       GemmMaps m = pair_gu ? mxg : mx;
       m.a[0] = c->m_wg[l];
@@ -943,7 +943,7 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
       CK(cudaGetLastError());
       CK(debug_copy_hidden(c, f, l, s));
     }
-    // a6: final norm of the block rows (gathered from the full sequence at a refresh)
+    // final norm of the block rows (gathered from the full sequence at a refresh)
     const int brows = f.batch * f.B;
     RowMap rb{f.B, f.rows_per_seq, 1, -f.row_off};
     rmsnorm_kernel<float, float><<<brows, 256, 0, s>>>(c->h, (const float*)c->W(1 + 9 * d.n_layers),
@@ -952,7 +952,7 @@ dinfer_status enqueue_forward(dinfer_ctx* c, const Fwd& f, cudaStream_t s) {
     CK(cudaGetLastError());
   }
 
-  // a6 + a7: LM head, online softmax, threshold commit
+  // LM head, online softmax, threshold commit
   const int brows = f.batch * f.B;
   if (c->dbg_final)
     CK(cudaMemcpyAsync(c->dbg_final, c->xn, (size_t)brows * D * c->esize(), cudaMemcpyDeviceToDevice, s));

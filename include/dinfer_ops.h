@@ -24,7 +24,9 @@ extern "C" {
  * and up to 64 query tiles x 64 heads of attention. */
 size_t dinfer_op_workspace_bytes(void);
 
-/* Y[m, n] = sum_k X[m, k] W[n, k]  (bf16 inputs, fp32 accumulate and output).
+/* Every projection of the forward (QKV, O, gate/up, down, router) of the
+ * bf16 model that dInfer README "Step 3" loads:
+ * Y[m, n] = sum_k X[m, k] W[n, k]  (bf16 inputs, fp32 accumulate and output).
  * X [M, K] bf16, W [N, K] bf16 (row-major, 16-byte aligned), Y [M, N] fp32.
  * K % 64 == 0, N % 128 == 0, 1 <= M <= 1 << 20.  The tensor-core GEMM
  * (tcgen05, TMA, stream-K) used for every projection of the model: one-CTA
@@ -36,8 +38,9 @@ size_t dinfer_op_workspace_bytes(void);
 dinfer_status dinfer_op_gemm_bf16(const void* X, const void* W, float* Y, int32_t M, int32_t N, int32_t K,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
-/* Fused LM head (dInfer decoding strategy: top-1 token and its softmax
- * probability per position, without materialising the logits):
+/* Fused LM head (the decoder of dInfer README "Step 3",
+ * ThresholdParallelDecoder, needs per position the top-1 token and its
+ * softmax probability; computed without materialising the logits):
  *   l[m, v] = scale * sum_k X[m, k] W[v, k], l[m, mask_id] = -inf,
  *   tok[m] = argmax_v l[m, v] (lowest index on ties),
  *   conf[m] = 1 / sum_v exp(l[m, v] - l[m, tok[m]]).
@@ -47,7 +50,8 @@ dinfer_status dinfer_op_lmhead_bf16(const void* X, const void* W, int32_t M, int
                                     float scale, int32_t* tok, float* conf, float* logits, void* workspace,
                                     size_t workspace_bytes, void* stream);
 
-/* Bidirectional attention of the block rows against the dual cache:
+/* Bidirectional attention of the block rows against the dual cache (dInfer
+ * README, "Step 3": KVCacheFactory('dual'); no causal mask in a diffusion LM):
  *   o[r, h, :] = sum_j softmax_j(q[r, h, :] . k[b, j, h, :] / sqrt(128)) v[b, j, h, :]
  * over all j < L of sequence b = r / rows_per_seq, no mask.  q, o
  * [batch * rows_per_seq, heads * 128] bf16; k, v [batch, L, heads * 128] bf16.
@@ -60,8 +64,9 @@ dinfer_status dinfer_op_attention_bf16(const void* q, const void* k, const void*
                                        int32_t rows_per_seq, int32_t L, int32_t heads, void* workspace,
                                        size_t workspace_bytes, void* stream);
 
-/* Routed expert FFN of a mixture-of-experts layer (LLaDA-MoE / OLMoE-style
- * routing), the a5' step of the denoising iteration:
+/* Routed expert FFN of a mixture-of-experts layer (the LLaDA-MoE model of
+ * dInfer README, "Step 3", an OLMoE-style model with fused experts), the
+ * expert step of the denoising iteration's FFN:
  *   p = softmax(X router^T) over E experts; the K experts of highest p (ties
  *   to the lower index); out[m] = sum over them of p_e * SwiGLU_e(X[m]) with
  *   SwiGLU_e(x) = (silu(x W_g,e^T) * x W_u,e^T) W_d,e^T  (weights not renormalised).
