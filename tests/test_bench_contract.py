@@ -65,3 +65,25 @@ def test_clock_summary_reads_the_sampled_gpu_and_its_throttle_reasons(tmp_path):
     assert s["samples"] == 4
     s1 = bench.ClockSampler(str(p)).summary(1)
     assert s1["sm_mhz"] == 1100.0 and s1["reasons"] == ["hw_slowdown"]
+
+
+def test_cpu_oracle_sample_extrapolation_arithmetic():
+    """A workload too large for the oracle is sampled (2 of its layers, 2 of
+    its sequences, block 0 and a middle block) and the whole generation's
+    time extrapolated: per block one refresh and (iterations - 1) cached
+    iterations at the sampled per-refresh and per-iteration times."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from block_denoising_gb300 import inputs
+    cfg = inputs.shrink(inputs.LLADA_8B, n_layers=4, d_model=256, n_heads=2, ffn=512, vocab=1024, mask_id=1023)
+    run = inputs.RunConfig(batch=3, prompt_len=32, gen_length=64, block_length=16, threshold=0.9)
+    assert not bench.tiny_sample(cfg, run)
+    ipb = [3, 1, 4, 2]
+    s = bench.oracle_sample(cfg, run, ipb)
+    assert s["extrapolated"] is True and s["kind"] == "oracle" and s["cores"] >= 1
+    r, i = s["us_per_refresh"] * 1e-6, s["us_per_iteration"] * 1e-6
+    total = 4 * r + (sum(ipb) - 4) * i
+    assert s["value"] == pytest.approx(3 * 64 / total, rel=1e-9)
+    assert "2 of 4 layers" in s["sample"] and "2 of 3 sequences" in s["sample"] and "block 2" in s["sample"]
+    u = bench.oracle_sample(cfg, run, None)      # without iteration counts: an upper bound
+    assert u["value"] == pytest.approx(3 * 64 / (4 * u["us_per_refresh"] * 1e-6), rel=1e-9)
