@@ -100,12 +100,15 @@ class ClockSampler:
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        self.f = None
         try:
             self.f = open(self.path, "w")
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms",
                                        "200"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
+            if self.f:
+                self.f.close()
         return self
 
     def __exit__(self, *a):

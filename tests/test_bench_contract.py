@@ -87,3 +87,15 @@ def test_cpu_oracle_sample_extrapolation_arithmetic():
     assert "2 of 4 layers" in s["sample"] and "2 of 3 sequences" in s["sample"] and "block 2" in s["sample"]
     u = bench.oracle_sample(cfg, run, None)      # without iteration counts: an upper bound
     assert u["value"] == pytest.approx(3 * 64 / (4 * u["us_per_refresh"] * 1e-6), rel=1e-9)
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    """Without nvidia-smi (here) the sampler records nothing and the summary
+    reports no clocks instead of failing the run."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("PATH", str(tmp_path))
+    with bench.ClockSampler(str(tmp_path / "c.csv")) as c:
+        pass
+    s = c.summary(0)
+    assert s["sm_mhz"] is None and s["reasons"] == []
