@@ -1,0 +1,167 @@
+"""The GPU parity harness checked on the CPU (no GPU): tests/parity.py's
+teacher-forced comparison is run against a stand-in for the library's
+decoder that answers with the oracle under its CPU model of the GPU's
+arithmetic.  Faithful, it must pass at the tolerance derived from the same
+model; with a planted mistake -- a wrong token or commit at a decision the
+tolerance does not flag, a logit off by more than delta, a confidence
+outside its interval -- the harness must report it.  This keeps the GPU
+parity tests from passing vacuously."""
+import numpy as np
+import pytest
+import torch
+
+from block_denoising_gb300 import inputs
+from oracle import dinfer_oracle as O
+from tests import parity as PT
+
+CFG = inputs.shrink(inputs.LLADA_8B, n_layers=1, d_model=256, n_heads=2, ffn=512, vocab=512, mask_id=511)
+P, G, B, TAU = 32, 32, 16, 0.9
+
+
+class StandIn:
+    """Answers prefill_cache / block_step like the library's Decoder, through
+    the debug outputs, from the oracle under parity.gpu_arithmetic();
+    `plant(logits, tok, conf, masked)` may alter what it reports and commits."""
+
+    def __init__(self, m, plant=None):
+        self.m, self.plant = m, plant
+        self.out = (None, None, None)
+        self.fin = None
+        self.cache = None
+        self.s0 = self.B = None
+        self.steps = 0
+
+    def set_debug_outputs(self, lg, tk, cf):
+        self.out = (lg, tk, cf)
+
+    def set_debug_hidden(self, hid, fin):
+        self.fin = fin
+
+    def sync(self):
+        pass
+
+    def prefill_cache(self, ids, mask, s0, b_len, tau, commit=True):
+        self.s0, self.B = s0, b_len
+        self.cache = O.Cache(self.m.desc, ids.shape[0], ids.shape[1])
+        self._step(ids, mask, tau, O.refresh_step)
+
+    def block_step(self, ids, mask, tau):
+        self._step(ids, mask, tau, O.cached_step)
+
+    def _step(self, ids, mask, tau, fn):
+        s0, Bl = self.s0, self.B
+        x = ids.numpy().astype(np.int64)
+        mk = mask.numpy().astype(bool)
+        with PT.gpu_arithmetic():
+            r = fn(self.m, x, mk, s0, Bl, tau, self.cache, commit=False)
+        logits, tok, conf = r.logits.copy(), r.tok.copy(), r.conf.copy()
+        if self.plant is not None:
+            logits, tok, conf = self.plant(self.steps, logits, tok, conf, mk[:, s0:s0 + Bl])
+        self.steps += 1
+        for i in range(x.shape[0]):
+            sel = O.threshold_commit(conf[i], mk[i, s0:s0 + Bl], tau)
+            x[i, s0:s0 + Bl][sel] = tok[i][sel]
+            mk[i, s0:s0 + Bl][sel] = False
+        lg, tk, cf = self.out
+        lg.copy_(torch.from_numpy(logits.reshape(lg.shape).astype(np.float32)))
+        tk.copy_(torch.from_numpy(tok.reshape(-1).astype(np.int32)))
+        cf.copy_(torch.from_numpy(conf.reshape(-1).astype(np.float32)))
+        ids.copy_(torch.from_numpy(x.astype(np.int32)))
+        mask.copy_(torch.from_numpy(mk.astype(np.uint8)))
+        if self.fin is not None:
+            a = self.m.prec.r(O.rmsnorm(r.hidden, self.m.final_norm, self.m.desc.rms_eps))
+            self.fin.copy_(torch.from_numpy(a.reshape(self.fin.shape).astype(np.float32)).to(self.fin.dtype))
+
+
+@pytest.fixture(scope="module")
+def case():
+    W = inputs.make_weights(CFG, 0)
+    m = O.Model(O.Desc.from_config(CFG), [w.float().numpy() for w in W])
+    prompt = inputs.make_prompt(CFG, 2, P).numpy()
+    _, recs = PT.oracle_generation(m, prompt, G, B, TAU)
+    tol = PT.tolerance_from_floor(*PT.model_floor(m, recs, B, TAU))
+    assert tol["delta"] > 0
+    return m, recs, tol
+
+
+def _run(case, plant=None):
+    m, recs, tol = case
+    return PT.gpu_compare(None, StandIn(m, plant), recs, m, B, TAU, tol, "cpu", lm_head_check=True)
+
+
+def _unflagged_position(recs, tol):
+    """(record, sequence, block position) of an unflagged decision: the one
+    with the widest top-2 logit margin over all records."""
+    best = (-np.inf, None)
+    for k, r in enumerate(recs):
+        fl = PT.flags_for(r.logits, r.conf, r.mask_before[:, r.s0:r.s0 + B], TAU, tol["delta"])
+        srt = np.sort(r.logits, axis=-1)
+        gap = np.where(fl, -np.inf, srt[..., -1] - srt[..., -2])
+        i, j = np.unravel_index(int(np.argmax(gap)), gap.shape)
+        if gap[i, j] > best[0]:
+            best = (gap[i, j], (k, int(i), int(j)))
+    assert best[1] is not None and np.isfinite(best[0])
+    return best[1]
+
+
+def test_faithful_stand_in_passes_and_checks_real_decisions(case):
+    m, recs, tol = case
+    st = _run(case)
+    PT.assert_parity(st, tol)
+    decisions = sum(r.conf.size for r in recs)
+    assert st["n"] > 0 and st["flagged"] < decisions         # some decisions are compared exactly
+    assert st["max_err"] > 0                                   # the stand-in really differs by rounding
+
+
+def test_wrong_unflagged_token_is_caught(case):
+    m, recs, tol = case
+    k, i, j = _unflagged_position(recs, tol)
+
+    def plant(step, logits, tok, conf, masked):
+        if step == k:
+            tok = tok.copy()
+            tok[i, j] = (tok[i, j] + 1) % (CFG.vocab - 1)
+        return logits, tok, conf
+
+    st = _run(case, plant)
+    assert st["unflagged_mismatch"] > 0
+    with pytest.raises(AssertionError):
+        PT.assert_parity(st, tol)
+
+
+def test_logit_beyond_delta_is_caught(case):
+    m, recs, tol = case
+
+    def plant(step, logits, tok, conf, masked):
+        logits = logits.copy()
+        logits[0, 0, 7] += 1.5 * tol["delta"]
+        return logits, tok, conf
+
+    st = _run(case, plant)
+    assert st["max_err"] >= 1.5 * tol["delta"] * 0.99
+    with pytest.raises(AssertionError):
+        PT.assert_parity(st, tol)
+
+
+def test_confidence_outside_its_interval_is_caught(case):
+    m, recs, tol = case
+
+    def plant(step, logits, tok, conf, masked):
+        return logits, tok, conf * 0.5
+
+    st = _run(case, plant)
+    assert st["conf_outside"] > 0
+    with pytest.raises(AssertionError):
+        PT.assert_parity(st, tol)
+
+
+def test_missing_commit_is_caught(case):
+    m, recs, tol = case
+
+    def plant(step, logits, tok, conf, masked):
+        # every confidence below the threshold: only the fallback position commits
+        return logits, tok, np.minimum(conf, TAU * 0.999)
+
+    st = _run(case, plant)
+    with pytest.raises(AssertionError):
+        PT.assert_parity(st, tol)
