@@ -165,3 +165,28 @@ def test_missing_commit_is_caught(case):
     st = _run(case, plant)
     with pytest.raises(AssertionError):
         PT.assert_parity(st, tol)
+
+
+def test_follow_gpu_checks_the_stand_ins_own_trajectory(case):
+    """parity.follow_gpu (used for the production graph path) follows the
+    decoder's own trajectory and compares every decision against the
+    oracle's at that state: faithful, it passes; committing a wrong token
+    wherever a decision is clear (top-2 margin far above 2 delta, confidence
+    far above the threshold), it fails."""
+    m, _, tol0 = case
+    prompt = inputs.make_prompt(CFG, 2, P).numpy()
+    tol_fn = lambda recs: PT.tolerance_from_floor(*PT.model_floor(m, recs, B, TAU))
+    x, st, recs, tol = PT.follow_gpu(None, StandIn(m), m, prompt, G, B, TAU, tol_fn, "cpu")
+    PT.assert_parity(st, tol, lm_head=False)
+    assert not (x == CFG.mask_id).any() and (x[:, :P] == prompt).all()
+
+    def plant(step, logits, tok, conf, masked):
+        srt = np.sort(logits, axis=-1)
+        clear = masked & (srt[..., -1] - srt[..., -2] > 6 * tol0["delta"]) & (conf > TAU + 0.05)
+        tok = np.where(clear, (tok + 1) % (CFG.vocab - 1), tok)
+        return logits, tok, conf
+
+    _, st2, _, tol2 = PT.follow_gpu(None, StandIn(m, plant), m, prompt, G, B, TAU, tol_fn, "cpu")
+    assert st2["unflagged_mismatch"] > 0
+    with pytest.raises(AssertionError):
+        PT.assert_parity(st2, tol2, lm_head=False)
