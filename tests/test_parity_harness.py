@@ -190,3 +190,32 @@ def test_follow_gpu_checks_the_stand_ins_own_trajectory(case):
     assert st2["unflagged_mismatch"] > 0
     with pytest.raises(AssertionError):
         PT.assert_parity(st2, tol2, lm_head=False)
+
+
+def test_route_flags_map_router_calls_to_sequences_and_block_rows():
+    """The oracle's forward routes layer by layer, sequence by sequence, over
+    the rows it computes (all positions at a refresh, the window otherwise);
+    route_flags_for must pick each sequence's block rows out of those calls."""
+    Bl, b, L, s0 = 4, 2, 12, 4
+
+    class R:
+        pass
+
+    def rec(iteration, window, margins):
+        r = R()
+        r.iteration, r.s0, r.window, r.margins = iteration, s0, window, margins
+        r.x_before = np.zeros((b, L), np.int64)
+        return r
+
+    big = lambda n: np.full(n, 1.0)
+    # refresh: rows 0..11; sequence 1's block row 2 (position 6) is a near-tie in layer 1
+    m1 = [big(L), big(L), big(L), big(L)]          # calls: (l0, s0), (l0, s1), (l1, s0), (l1, s1)
+    m1[3] = m1[3].copy(); m1[3][s0 + 2] = 0.001
+    # cached iteration recomputing the window [2, 10): sequence 0's block row 0 (position 4) in layer 0
+    m2 = [big(8), big(8), big(8), big(8)]
+    m2[0] = m2[0].copy(); m2[0][s0 - 2] = 0.001
+    f1, f2 = PT.route_flags_for([rec(1, (0, L), m1), rec(2, (2, 10), m2)], 0.02, Bl)
+    want1 = np.zeros((b, Bl), bool); want1[1, 2] = True
+    want2 = np.zeros((b, Bl), bool); want2[0, 0] = True
+    np.testing.assert_array_equal(f1, want1)
+    np.testing.assert_array_equal(f2, want2)
