@@ -219,3 +219,26 @@ def test_route_flags_map_router_calls_to_sequences_and_block_rows():
     want2 = np.zeros((b, Bl), bool); want2[0, 0] = True
     np.testing.assert_array_equal(f1, want1)
     np.testing.assert_array_equal(f2, want2)
+
+
+def test_confidence_interval_is_the_reach_of_a_delta_logit_error():
+    """conf_interval's ends are the confidences of the logits moved by delta
+    against and for the top token, and every logit error within delta that
+    keeps the argmax lands inside."""
+    rng = np.random.default_rng(5)
+    logits = rng.normal(size=(6, 50)) * 3.0
+    delta = 0.4
+    tok = logits.argmax(-1)
+    conf = 1.0 / np.exp(logits - logits.max(-1, keepdims=True)).sum(-1)
+    lo, hi = PT.conf_interval(conf, delta)
+    top = np.zeros_like(logits, bool); top[np.arange(6), tok] = True
+    worst = np.where(top, logits - delta, logits + delta)
+    best = np.where(top, logits + delta, logits - delta)
+    c = lambda l: np.exp(l[np.arange(6), tok]) / np.exp(l).sum(-1)
+    np.testing.assert_allclose(lo, c(worst), rtol=1e-12)
+    np.testing.assert_allclose(hi, c(best), rtol=1e-12)
+    for _ in range(200):
+        pert = logits + rng.uniform(-delta, delta, size=logits.shape)
+        keep = pert.argmax(-1) == tok
+        cp = c(pert)
+        assert np.all((cp[keep] >= lo[keep] - 1e-12) & (cp[keep] <= hi[keep] + 1e-12))
