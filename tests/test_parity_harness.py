@@ -242,3 +242,32 @@ def test_confidence_interval_is_the_reach_of_a_delta_logit_error():
         keep = pert.argmax(-1) == tok
         cp = c(pert)
         assert np.all((cp[keep] >= lo[keep] - 1e-12) & (cp[keep] <= hi[keep] + 1e-12))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_unflagged_decisions_survive_every_delta_logit_error(seed):
+    """flags_for is sound: at a position it leaves unflagged, no logit error
+    within delta changes the top-1 token or the commit decision."""
+    rng = np.random.default_rng(seed)
+    b, Bl, V, tau, delta = 2, 16, 40, 0.9, 0.15
+    logits = rng.normal(size=(b, Bl, V)) * rng.uniform(1.0, 4.0, size=(b, Bl, 1))
+    logits[..., V - 1] = -np.inf                                   # the mask token
+    masked = rng.random((b, Bl)) < 0.7
+    masked[:, 0] = True
+
+    def decide(lg):
+        tok, conf = np.zeros((b, Bl), np.int64), np.zeros((b, Bl))
+        com = np.zeros((b, Bl), bool)
+        for i in range(b):
+            tok[i], conf[i] = O.top1_confidence(lg[i])
+            com[i] = O.threshold_commit(conf[i], masked[i], tau)
+        return tok, conf, com
+
+    tok, conf, com = decide(logits)
+    fl = PT.flags_for(logits, conf, masked, tau, delta)
+    assert (~fl).any()
+    for _ in range(300):
+        pert = logits + rng.uniform(-delta, delta, size=logits.shape)
+        t2, _, c2 = decide(pert)
+        assert np.array_equal(t2[~fl], tok[~fl])
+        assert np.array_equal(c2[~fl], com[~fl])
