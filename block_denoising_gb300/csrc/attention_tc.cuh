@@ -129,21 +129,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
   ATC_I4(x, b), ATC_I4(x, (b) + 4), ATC_I4(x, (b) + 8), ATC_I4(x, (b) + 12), ATC_I4(x, (b) + 16),          \
       ATC_I4(x, (b) + 20), ATC_I4(x, (b) + 24), ATC_I4(x, (b) + 28)
 
-// 128 consecutive TMEM columns of this warp's 32 lanes, one wait for all four
-// loads.  The empty statements after the wait carry the registers, so no use
-// of them can be scheduled before the wait.
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 0) : "r"(taddr));
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 32) : "r"(taddr + 32));
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 64) : "r"(taddr + 64));
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 96) : "r"(taddr + 96));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : ATC_I32(x, 0)::"memory");
-  asm volatile("" : ATC_I32(x, 32));
-  asm volatile("" : ATC_I32(x, 64));
-  asm volatile("" : ATC_I32(x, 96));
-}
-
-// 64 consecutive TMEM columns of this warp's 32 lanes, one wait for both loads
+// 64 consecutive TMEM columns of this warp's 32 lanes, one wait for both
+// loads.  The empty statement after the wait carries the second load's
+// registers, so no use of them can be scheduled before the wait.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&x)[64]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 0) : "r"(taddr));
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];" : ATC_O32(x, 32) : "r"(taddr + 32));
